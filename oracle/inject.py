@@ -1,0 +1,69 @@
+"""Segment composition, slot mapping and the paged scatter-copy, in fp64.
+
+InferScale ("Méthodologie", phase 2, "Rotation Dynamique" and "Injection";
+"방법론" 동적 회전 / 주입): the retrieved facts are composed into one contiguous
+segment, each stored pre-RoPE key is rotated to its new serving position, and
+the composed K/V are scatter-copied into vLLM's paged KV cache; the engine then
+prefills only the query tokens.
+
+Readings where the pages are silent:
+* the facts follow each other in the order given (descending score when they
+  come from retrieval); token t of the segment (0-based) takes the absolute
+  position p = start + t, and p is both the RoPE position and the logical cache
+  index (vLLM convention);
+* the paged cache is vLLM-style: physical block b holds block_size consecutive
+  logical positions; ``slot(p) = block_table[p // bs] * bs + p % bs``; the cache
+  is laid out [L][2][num_blocks][bs][H][D] with K at index 0 and V at 1;
+* rotated keys are computed in fp64 and rounded to the cache type with
+  round-to-nearest-even; values are copied bit for bit;
+* every other element of the cache keeps its previous contents.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+from . import numerics, rope
+
+
+def compose(fact_ids, lengths, start: int):
+    """Token plan of one request: list of (fact, t_in_fact, position) and the
+    segment length."""
+    plan = []
+    t = 0
+    for f in fact_ids:
+        f = int(f)
+        for j in range(int(lengths[f])):
+            plan.append((f, j, start + t))
+            t += 1
+    return plan, t
+
+
+def slot(position: int, block_row, block_size: int) -> int:
+    return int(block_row[position // block_size]) * block_size + position % block_size
+
+
+def rotated_key_rows(k_token: np.ndarray, position: int, freqs: np.ndarray, style: int,
+                     kv_dtype: str) -> np.ndarray:
+    """fp64 rotated keys of one token: k_token [L][H][D] in storage encoding."""
+    return rope.rotate(numerics.decode(k_token, kv_dtype), position, freqs, style)
+
+
+def inject(cache: np.ndarray, kv_dtype: str, fact_kv, fact_ids, lengths, start: int,
+           block_row, block_size: int, freqs: np.ndarray, style: int):
+    """Scatter one request into ``cache`` (storage encoding, [L][2][NB][bs][H][D]),
+    in place.  ``fact_kv(f)`` returns (K, V) of fact f as [len][L][H][D] in
+    storage encoding.  Returns (plan, seg_len, slots)."""
+    plan, seg_len = compose(fact_ids, lengths, start)
+    slots = []
+    cur = None
+    for f, j, p in plan:
+        if cur is None or cur[0] != f:
+            cur = (f,) + tuple(fact_kv(f))
+        K, V = cur[1], cur[2]
+        s = slot(p, block_row, block_size)
+        slots.append(s)
+        blk, off = divmod(s, block_size)
+        k_rot = rotated_key_rows(K[j], p, freqs, style, kv_dtype)  # [L][H][D] fp64
+        cache[:, 0, blk, off] = numerics.encode(k_rot, kv_dtype)
+        cache[:, 1, blk, off] = V[j]
+    return plan, seg_len, np.asarray(slots, dtype=np.int64)

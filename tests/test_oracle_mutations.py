@@ -1,0 +1,159 @@
+"""Plant plausible mistakes in the oracle (on the CPU) and check a pin catches each.
+
+A pin set that a dropped term, a wrong sign, a wrong index or a swapped operand
+slips through would not pin anything; each case below patches one oracle
+function and requires at least one of the named pins to fail.
+"""
+import numpy as np
+import pytest
+
+import tests.test_oracle_pins as pins
+from oracle import inject, numerics, retrieval, rope
+
+
+def _fails(fn, *args):
+    try:
+        fn(*args)
+    except (AssertionError, IndexError, ValueError):
+        return True
+    return False
+
+
+def _rotate_wrong_sign(x, position, freqs, style):
+    x = np.asarray(x, dtype=np.float64)
+    ia, ib = rope.pair_indices(x.shape[-1], style)
+    phi = np.asarray(position, dtype=np.float64)[..., None] * freqs
+    c, s = np.cos(phi), np.sin(phi)
+    out = np.empty(np.broadcast_shapes(x.shape, phi.shape[:-1] + (x.shape[-1],)))
+    out[..., ia] = x[..., ia] * c + x[..., ib] * s
+    out[..., ib] = x[..., ib] * c - x[..., ia] * s
+    return out
+
+
+def _rotate_dropped_term(x, position, freqs, style):
+    x = np.asarray(x, dtype=np.float64)
+    ia, ib = rope.pair_indices(x.shape[-1], style)
+    phi = np.asarray(position, dtype=np.float64)[..., None] * freqs
+    out = np.empty(np.broadcast_shapes(x.shape, phi.shape[:-1] + (x.shape[-1],)))
+    out[..., ia] = x[..., ia] * np.cos(phi) - x[..., ib] * np.sin(phi)
+    out[..., ib] = x[..., ib] * np.cos(phi)
+    return out
+
+
+def _pairs_swapped(D, style):
+    half = D // 2
+    i = np.arange(half)
+    return (2 * i, 2 * i + 1) if style == 0 else (i, i + half)
+
+
+def test_mutation_rotation_sign(monkeypatch):
+    monkeypatch.setattr(rope, "rotate", _rotate_wrong_sign)
+    assert _fails(pins.test_rotation_hand_value)
+    assert _fails(pins.test_rotation_is_complex_multiplication, 0)
+
+
+def test_mutation_rotation_dropped_term(monkeypatch):
+    monkeypatch.setattr(rope, "rotate", _rotate_dropped_term)
+    assert _fails(pins.test_rotation_hand_value)
+    assert _fails(pins.test_rotation_group_properties, 0)
+    assert _fails(pins.test_theorem6_scores_depend_only_on_offset, 0)
+
+
+def test_mutation_pairing_swapped(monkeypatch):
+    monkeypatch.setattr(rope, "pair_indices", _pairs_swapped)
+    assert _fails(pins.test_rotation_pairing_styles)
+
+
+def test_mutation_frequency_exponent(monkeypatch):
+    orig = rope.inv_freq
+
+    def wrong(head_dim, theta, *a, **k):
+        return orig(2 * head_dim, theta, *a, **k)[: head_dim // 2]      # theta^(-i/D)
+    monkeypatch.setattr(rope, "inv_freq", wrong)
+    assert _fails(pins.test_inv_freq_plain_closed_forms)
+
+
+def test_mutation_llama3_factor_multiplied(monkeypatch):
+    orig = rope.inv_freq
+
+    def wrong(head_dim, theta, scaling=0, factor=1.0, *a, **k):
+        return orig(head_dim, theta, scaling, 1.0 / factor, *a, **k)
+    monkeypatch.setattr(rope, "inv_freq", wrong)
+    assert _fails(pins.test_llama31_scaling_regimes)
+
+
+def test_mutation_llama3_blend_swapped(monkeypatch):
+    orig = rope.inv_freq
+
+    def wrong(head_dim, theta, scaling=0, factor=1.0, low_freq_factor=1.0,
+              high_freq_factor=1.0, original_max_pos=0):
+        return orig(head_dim, theta, scaling, factor, high_freq_factor, low_freq_factor,
+                    original_max_pos)                                      # low/high swapped
+    monkeypatch.setattr(rope, "inv_freq", wrong)
+    assert _fails(pins.test_llama31_scaling_regimes)
+
+
+def test_mutation_slot_index_swapped(monkeypatch):
+    monkeypatch.setattr(inject, "slot",
+                        lambda p, row, bs: int(row[p % bs]) * bs + p // bs)
+    assert _fails(pins.test_slot_mapping_golden)
+    assert _fails(pins.test_theorem3_injection_equals_prompt_prefill, 0, False)
+
+
+def test_mutation_position_off_by_one(monkeypatch):
+    orig = inject.compose
+
+    def wrong(fact_ids, lengths, start):
+        return orig(fact_ids, lengths, start + 1)
+    monkeypatch.setattr(inject, "compose", wrong)
+    assert _fails(pins.test_theorem3_injection_equals_prompt_prefill, 0, False)
+    assert _fails(pins.test_compose_positions_and_lengths)
+
+
+def test_mutation_topk_ties_to_higher_id(monkeypatch):
+    def wrong(scores, ids, k):
+        order = np.lexsort((-np.asarray(ids), -np.asarray(scores, dtype=np.float64)))[:k]
+        return np.asarray(ids)[order], np.asarray(scores, dtype=np.float64)[order]
+    monkeypatch.setattr(retrieval, "topk", wrong)
+    assert _fails(pins.test_topk_brute_force_tiny_stores_with_ties)
+
+
+def test_mutation_cosine_unnormalised_query(monkeypatch):
+    def wrong(q, X):
+        X = np.asarray(X, dtype=np.float64)
+        n = np.linalg.norm(X, axis=1)
+        return np.where(n > 0, (X @ np.asarray(q, dtype=np.float64)) / np.where(n > 0, n, 1), 0.0)
+    monkeypatch.setattr(retrieval, "cosine_scores", wrong)
+    assert _fails(pins.test_cosine_closed_forms)
+
+
+def test_mutation_bf16_double_rounding(monkeypatch):
+    def wrong(x):
+        f = np.asarray(x, dtype=np.float64).astype(np.float32).view(np.uint32).astype(np.uint64)
+        return ((f + 0x7FFF + ((f >> 16) & 1)) >> 16).astype(np.uint16)
+    monkeypatch.setattr(numerics, "f64_to_bf16_bits", wrong)
+    assert _fails(pins.test_bf16_rounding_golden)
+
+
+def test_mutation_bf16_truncation(monkeypatch):
+    def wrong(x):
+        return (np.asarray(x, dtype=np.float64).astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    monkeypatch.setattr(numerics, "f64_to_bf16_bits", wrong)
+    assert _fails(pins.test_bf16_rounding_golden)
+
+
+@pytest.mark.parametrize("which", ["k", "v"])
+def test_mutation_scatter_drops_rotation_or_copy(monkeypatch, which):
+    orig = inject.rotated_key_rows
+    if which == "k":
+        monkeypatch.setattr(inject, "rotated_key_rows",
+                            lambda k, p, f, s, d: orig(k, 0, f, s, d))   # rotation skipped
+        assert _fails(pins.test_theorem3_injection_equals_prompt_prefill, 0, False)
+    else:
+        orig_inject = inject.inject
+
+        def wrong(cache, dt, fact_kv, *a):
+            return orig_inject(cache, dt, lambda f: (fact_kv(f)[0], fact_kv(f)[0]), *a)  # V := K
+        monkeypatch.setattr(inject, "inject", wrong)
+        assert _fails(pins.test_inject_tiny_canaries_and_copies, "f32")
+        assert _fails(pins.test_theorem3_injection_equals_prompt_prefill, 0, False)
