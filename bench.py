@@ -1,0 +1,476 @@
+"""Benchmark: injected KV tokens/s of retrieve + Chunked RoPE + paged scatter.
+
+One step = one is_retrieve_and_inject call over one batch of the workload
+(cosine similarity, top-k, segment plan, gather + rotate + scatter for every
+layer and KV head).  Default workload: the Llama-3.1-8B KV shape (32 layers, 8
+KV heads, head_dim 128, bf16), 2000 stored facts of U[10, 40] tokens, one query,
+k = 50, block size 16; synthetic, seeded.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  Under torchrun every rank runs its own
+replica on its own store (weak scaling, no collective on the data path); the
+timing is the max over ranks after a barrier.  ``--impl reference`` times the
+fp64 CPU oracle on the host cores instead (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "injected KV tokens/s (retrieve+RoPE+paged scatter) at k=50; % of HBM roofline"
+FALLBACK_HBM_GBS = 6800.0
+L2_FLUSH_BYTES = 512 << 20
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "inject_traffic.json")
+INJECT_SRC = os.path.join(ROOT, "kv_cache_injection_gb300", "csrc", "inject.cu")
+
+
+# ----------------------------------------------------------------------------- helpers
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), \
+        int(os.environ.get("LOCAL_RANK", 0))
+
+
+def rank_seed(base_seed: int, rank: int) -> int:
+    """Each rank's replica draws its own store (weak scaling)."""
+    return base_seed + 1000 * rank
+
+
+def reduce_max(value: float, device=None) -> float:
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def reduce_sum(value: float, device=None) -> float:
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+def measured_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
+    return {"hbm_gbs": FALLBACK_HBM_GBS, "source": "fallback"}
+
+
+def inject_source_hash() -> str:
+    with open(INJECT_SRC, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def ncu_traffic_per_token():
+    """DRAM bytes per injected token from the committed ncu summary, if it was
+    taken on the current inject kernel source."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    with open(TRAFFIC_FILE) as f:
+        d = json.load(f)
+    if d.get("inject_cu_sha256_16") != inject_source_hash():
+        return None
+    return float(d["dram_bytes_per_token"])
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.out = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        if not self.out:
+            return None
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ----------------------------------------------------------------------------- our arm
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+
+    from kv_cache_injection_gb300 import api
+    from kv_cache_injection_gb300 import build as kbuild
+    from synth import staging, workloads
+
+    kbuild.build()
+    torch.cuda.set_device(local_rank)
+    dev = f"cuda:{local_rank}"
+    spec = workloads.SPECS[args.workload]
+    overrides = {"seed": rank_seed(spec.seed, rank)}
+    if args.k:
+        overrides["k"] = args.k
+        overrides["tokens_cap"] = args.k * int(spec.length_dist[2] if spec.length_dist[0] == "uniform"
+                                                else spec.tokens_cap // spec.k)
+    wl = workloads.get(args.workload, **overrides)
+    s = wl.spec
+    store = staging.load_store(wl, api, device=local_rank)
+    inp = staging.device_inputs(wl, local_rank)
+    cache = staging.canary_cache(wl, local_rank)
+    Q, k = s.n_queries, s.k
+    ids = torch.empty((Q, k), dtype=torch.int64, device=dev)
+    scores = torch.empty((Q, k), dtype=torch.float32, device=dev)
+    seg_len = torch.empty(Q, dtype=torch.int32, device=dev)
+    rope = staging.rope_params(wl, api)
+    cdesc = api.make_cache_desc(s.block_size, wl.num_blocks, s.kv_dtype)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        api.is_retrieve_and_inject(store, inp["users"], inp["q_emb"], k, inp["seg_start"], rope,
+                                   inp["block_table"], cdesc, cache, ids, scores, seg_len, None,
+                                   stream=stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    bits = api.is_get_status(store)
+    if bits:
+        raise RuntimeError(f"device status bits 0x{bits:x} during warm-up")
+    tokens_per_step = int(seg_len.sum().item())
+
+    # Timed region: per-step CUDA events around the call, L2 flushed between steps.
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    api.is_reset_timing(store)
+    api.is_set_timing(store, True)
+    barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local_rank) as clocks:
+        for i in range(args.steps):
+            flush.zero_()
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        torch.cuda.synchronize()
+    barrier()
+    api.is_set_timing(store, False)
+    step_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+    total_ms_local = sum(step_ms)
+    stage_ms, stage_n = {}, {}
+    for name, st in (("similarity", 0), ("topk", 1), ("plan", 2), ("inject", 3)):
+        stage_ms[name], stage_n[name] = api.is_get_timing(store, st)
+    gpu_launches = int(sum(stage_n.values()))
+    bits = api.is_get_status(store)
+    if bits:
+        raise RuntimeError(f"device status bits 0x{bits:x} in the timed region")
+
+    total_ms = reduce_max(total_ms_local, dev)
+    total_tokens = reduce_sum(float(tokens_per_step * args.steps), dev)
+
+    # End to end through the public API with host buffers: H2D of the step's
+    # inputs from pinned memory, the call, D2H of the result, every step.
+    h_users = torch.from_numpy(wl.users).pin_memory()
+    edt = torch.float16 if s.emb_dtype == "f16" else torch.float32
+    h_q = torch.from_numpy(np.ascontiguousarray(wl.queries)).to(edt).pin_memory()
+    h_start = torch.from_numpy(wl.seg_start).pin_memory()
+    h_bt = torch.from_numpy(np.ascontiguousarray(wl.block_table)).pin_memory()
+    h_ids = torch.empty((Q, k), dtype=torch.int64).pin_memory()
+    h_scores = torch.empty((Q, k), dtype=torch.float32).pin_memory()
+    h_len = torch.empty(Q, dtype=torch.int32).pin_memory()
+    d_users, d_q = torch.empty_like(inp["users"]), torch.empty_like(inp["q_emb"])
+    d_start, d_bt = torch.empty_like(inp["seg_start"]), torch.empty_like(inp["block_table"])
+    h2d = sum(t.numel() * t.element_size() for t in (h_users, h_q, h_start, h_bt))
+    d2h = sum(t.numel() * t.element_size() for t in (h_ids, h_scores, h_len))
+    e2e_steps = max(3, args.steps)
+    e2e_s = 0.0
+    for i in range(args.warmup + e2e_steps):
+        flush.zero_()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        d_users.copy_(h_users, non_blocking=True)
+        d_q.copy_(h_q, non_blocking=True)
+        d_start.copy_(h_start, non_blocking=True)
+        d_bt.copy_(h_bt, non_blocking=True)
+        api.is_retrieve_and_inject(store, d_users, d_q, k, d_start, rope, d_bt, cdesc, cache, ids,
+                                   scores, seg_len, None, stream=stream)
+        h_ids.copy_(ids, non_blocking=True)
+        h_scores.copy_(scores, non_blocking=True)
+        h_len.copy_(seg_len, non_blocking=True)
+        torch.cuda.synchronize()
+        if i >= args.warmup:
+            e2e_s += time.perf_counter() - t0
+    e2e_s = reduce_max(e2e_s, dev)
+    e2e_tokens = reduce_sum(float(int(h_len.sum()) * e2e_steps), dev)
+
+    result = None
+    if rank == 0:
+        peaks = measured_peaks()
+        per_tok = 2 * s.token_elems * s.elt_bytes            # K + V read (= bytes written)
+        inject_bytes = 2 * per_tok * tokens_per_step          # read + write per launch
+        inject_ms = stage_ms["inject"] / max(1, stage_n["inject"])
+        achieved = inject_bytes / (inject_ms * 1e-3) / 1e9
+        traffic_tok = ncu_traffic_per_token()
+        emb_bytes = 0
+        for u in np.unique(wl.users):
+            emb_bytes += int((wl.fact_user == u).sum()) * s.emb_dim * (2 if s.emb_dtype == "f16" else 4)
+        path_bytes = inject_bytes + emb_bytes
+        step_avg_ms = total_ms_local / args.steps
+        result = {
+            "metric": METRIC,
+            "value": total_tokens / (total_ms * 1e-3),
+            "unit": "tokens/s",
+            "n_gpus": world,
+            "steps": args.steps,
+            "warmup": args.warmup,
+            "ms_per_step": total_ms / args.steps,
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": s.kv_dtype,
+            "data": "synthetic (seeded; LoCoMo and model weights not available)",
+            "config": {
+                "workload": (f"{s.name}: {s.num_layers} layers x {s.num_kv_heads} KV heads x "
+                             f"head_dim {s.head_dim} {s.kv_dtype}; {s.n_facts} facts "
+                             f"{s.length_dist}; {Q} quer{'y' if Q == 1 else 'ies'}, k={k}, "
+                             f"block {s.block_size}"),
+                "tokens_per_step": tokens_per_step,
+                "bytes_per_step": path_bytes,
+                "l2": f"flushed between steps ({L2_FLUSH_BYTES >> 20} MiB write, outside the events)",
+                "parallelism": f"replicas x{world} (one store per GPU, no collective)",
+            },
+            "roofline": {
+                "bound": "hbm",
+                "kernel": "inject (gather + Chunked RoPE + paged scatter)",
+                "achieved": achieved,
+                "peak": peaks["hbm_gbs"],
+                "peak_source": peaks["source"],
+                "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"],
+                "frac_of_nominal_8tbs": achieved / 8000.0,
+                "traffic": (traffic_tok * tokens_per_step) if traffic_tok else None,
+                "algorithmic_bytes": inject_bytes,
+                "avg_launch_ms": inject_ms,
+            },
+            "path_roofline": {
+                "bytes": path_bytes,
+                "achieved": path_bytes / (step_avg_ms * 1e-3) / 1e9,
+                "frac": path_bytes / (step_avg_ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                "unit": "GB/s",
+            },
+            "stage_ms": {n: stage_ms[n] / max(1, stage_n[n]) for n in stage_ms},
+            "e2e": {"value": e2e_tokens / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+            "gpu_launches": gpu_launches,
+            "clocks": clocks.summary(),
+        }
+        if args.cpu_baseline:
+            result["cpu_baseline"] = cpu_baseline(wl, budget_s=args.cpu_budget)
+    store.destroy()
+    return result
+
+
+# ----------------------------------------------------------------------------- oracle arm
+
+def oracle_step(wl, q: int, max_facts: int | None, kv_cache_fn):
+    """One query through the fp64 oracle: cosine top-k, then rotation and
+    scatter of (at most max_facts of) the retrieved facts into a host cache."""
+    from oracle import inject as oinject
+    from oracle import retrieval, rope
+    s = wl.spec
+    facts = wl.user_facts(int(wl.users[q]))
+    ids, _ = retrieval.retrieve(wl.queries[q].astype(np.float64), wl.emb[facts].astype(np.float64),
+                                facts, s.k)
+    use = ids if max_facts is None else ids[:max_facts]
+    r = s.rope
+    freqs = rope.inv_freq(s.head_dim, r.theta, r.scaling, r.factor, r.low_freq_factor,
+                          r.high_freq_factor, r.original_max_pos)
+    cache = kv_cache_fn()
+    _, T, _ = oinject.inject(cache, s.kv_dtype, wl_fact_kv(wl), use, wl.lengths,
+                             int(wl.seg_start[q]), wl.block_table[q], s.block_size, freqs, r.style)
+    return T
+
+
+_FACT_MEMO = {}
+
+
+def wl_fact_kv(wl):
+    from synth import kvgen
+
+    def get(f):
+        key = (wl.spec.name, wl.spec.seed, int(f))
+        if key not in _FACT_MEMO:
+            _FACT_MEMO[key] = (wl.fact_kv(int(f), kvgen.STREAM_K), wl.fact_kv(int(f), kvgen.STREAM_V))
+        return _FACT_MEMO[key]
+    return get
+
+
+def _prefetch_facts(wl, q, max_facts):
+    from oracle import retrieval
+    facts = wl.user_facts(int(wl.users[q]))
+    ids, _ = retrieval.retrieve(wl.queries[q].astype(np.float64), wl.emb[facts].astype(np.float64),
+                                facts, wl.spec.k)
+    get = wl_fact_kv(wl)
+    for f in ids[:max_facts]:
+        get(f)
+
+
+def _host_cache(wl):
+    from synth.workloads import cache_shape
+    s = wl.spec
+    shape = cache_shape(s, wl.num_blocks)
+    dt = np.float32 if s.kv_dtype == "f32" else np.uint16
+    return lambda: np.zeros(shape, dtype=dt)
+
+
+def cpu_baseline(wl, budget_s: float = 20.0, max_facts: int = 10) -> dict:
+    """Time the oracle, as it stands, on a bounded sample of the workload: the
+    retrieval of query 0 over its user's store plus rotation and scatter of its
+    first ``max_facts`` retrieved facts, repeated until ~budget_s of CPU time."""
+    _prefetch_facts(wl, 0, max_facts)
+    cache_fn = _host_cache(wl)
+    cache = cache_fn()
+    t0 = time.perf_counter()
+    tokens, reps = 0, 0
+    while True:
+        tokens += oracle_step(wl, 0, max_facts, lambda: cache)
+        reps += 1
+        if time.perf_counter() - t0 > budget_s or reps >= 50:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": tokens / dt, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": (f"{reps} x (cosine top-{wl.spec.k} over {int((wl.fact_user == wl.users[0]).sum())} "
+                       f"facts + fp64 RoPE/scatter of the first {max_facts} retrieved facts); "
+                       f"{tokens} tokens in {dt:.1f} s, numpy fp64, 1 thread")}
+
+
+def run_reference(args, rank, world):
+    from synth import workloads
+    if rank != 0:
+        return None
+    spec = workloads.SPECS[args.workload]
+    overrides = {"k": args.k} if args.k else {}
+    wl = workloads.get(args.workload, **overrides)
+    max_facts = 4
+    _prefetch_facts(wl, 0, max_facts)
+    cache = _host_cache(wl)()
+    for _ in range(args.warmup):
+        oracle_step(wl, 0, max_facts, lambda: cache)
+    t0 = time.perf_counter()
+    tokens = 0
+    for _ in range(args.steps):
+        tokens += oracle_step(wl, 0, max_facts, lambda: cache)
+    dt = time.perf_counter() - t0
+    value = tokens / dt
+    sample = (f"per step: cosine top-{wl.spec.k} over {spec.facts_per_user} facts + fp64 RoPE/scatter "
+              f"of the first {max_facts} retrieved facts ({tokens // max(1, args.steps)} tokens)")
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": dt * 1e3 / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+            "config": {"workload": f"{wl.spec.name} (oracle on host cores, bounded sample)"},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+# ----------------------------------------------------------------------------- main
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="llama31_8b")
+    ap.add_argument("--k", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    rank, world, local_rank = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        if args.impl == "reference":
+            if rank != 0:
+                return 0
+        else:
+            import torch
+            torch.cuda.set_device(local_rank)
+            dist.init_process_group("nccl")
+    if args.impl == "reference":
+        out = run_reference(args, rank, world)
+    else:
+        out = run_ours(args, rank, world, local_rank)
+    if rank == 0 and out is not None:
+        print(json.dumps(out), flush=True)
+    if world > 1 and args.impl == "ours":
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

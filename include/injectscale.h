@@ -1,0 +1,264 @@
+/*
+ * injectscale.h -- C ABI of libinjectscale.so: GPU-resident fact store,
+ * cosine top-k retrieval, Chunked RoPE and paged KV injection on one GB300.
+ *
+ * The operations follow InferScale ("InferScale: GPU-Native KV Injection for
+ * Personalized LLM Serving", arXiv 2607.27090): memory facts are encoded
+ * offline, their keys captured before the rotary embedding and stored with
+ * the raw values and a semantic embedding on the GPU; at serving time the
+ * relevant facts are retrieved, composed into one contiguous segment, their
+ * keys rotated to the serving positions (Chunked RoPE) and the K/V
+ * scatter-copied into a vLLM-style paged KV cache.  The pages give no API;
+ * the calls below follow their statement of the problem (store, retrieve,
+ * compose, rotate, inject).
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - Every call returns is_status_t and throws nothing.  Host-detectable
+ *   errors return before anything is enqueued; is_last_error_message() then
+ *   describes the error of the calling thread's last failed call.
+ * - Calls taking a cudaStream_t are asynchronous on that stream unless
+ *   stated.  Pointers documented "device" must be device (or managed)
+ *   memory owned by the caller and stay valid until the stream reaches the
+ *   call.  Pointers documented "host" are read before the call returns.
+ * - Device-detected errors (bad ids, block tables that do not cover a
+ *   position, ...) never trap: the offending write is skipped and a bit of
+ *   IS_ST_* is OR-ed into the store's device status word, read (and
+ *   cleared) by is_get_status().
+ * - A store is used by one stream at a time; calls on one store are not
+ *   thread-safe.
+ * - Dtypes: K/V in the store and in the cache share one dtype (f32, bf16 or
+ *   f16); embeddings and query embeddings share one dtype (f16 or f32).
+ *   Rotation arithmetic is fp32; rotated keys are rounded to the cache
+ *   dtype to nearest even; values are copied bit for bit.
+ */
+#ifndef INJECTSCALE_H
+#define INJECTSCALE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define IS_ABI_VERSION 1
+
+/* Hard limits (per call). */
+#define IS_MAX_K          1024   /* retrieval budget / facts per injected request */
+#define IS_MAX_QUERIES    1024   /* queries per retrieval call */
+#define IS_MAX_REQUESTS   4096   /* requests per injection call */
+#define IS_MAX_HEAD_DIM   512
+#define IS_MAX_POSITION   (1 << 24)  /* positions must stay below 2^24 */
+#define IS_EMB_TILE       128    /* embedding rows per store tile (one user per tile) */
+
+typedef enum {
+  IS_OK = 0,
+  IS_ERR_INVALID_ARG = 1,   /* null pointer, bad size, bad enum, dtype mismatch */
+  IS_ERR_OOM = 2,           /* device allocation failed at store creation */
+  IS_ERR_CAPACITY = 3,      /* store arena (facts, tokens, tiles) is full */
+  IS_ERR_OUT_OF_RANGE = 4,  /* host-visible index out of range (user, k > max_k, ...) */
+  IS_ERR_CUDA = 5,          /* a CUDA runtime call failed */
+  IS_ERR_TIMEOUT = 6,       /* a bounded device wait gave up (IS_ST_TIMEOUT latched) */
+  IS_ERR_DEVICE = 7,        /* is_get_status found device status bits set */
+  IS_ERR_UNSUPPORTED = 8    /* shape outside what the kernels handle */
+} is_status_t;
+
+/* Bits of the device status word (see is_get_status). */
+#define IS_ST_FACT_RANGE   0x01u  /* fact id < 0 or >= number of stored facts */
+#define IS_ST_FACT_USER    0x02u  /* fact id belongs to another user than requested */
+#define IS_ST_BLOCK_TABLE  0x04u  /* position / block_size >= max_blocks_per_seq */
+#define IS_ST_BLOCK_ID     0x08u  /* block table entry < 0 or >= num_blocks */
+#define IS_ST_USER_RANGE   0x10u  /* user id < 0 or >= max_users */
+#define IS_ST_POSITION     0x20u  /* seg_start < 0 or seg_start + length > IS_MAX_POSITION */
+#define IS_ST_COUNT        0x40u  /* n_ids[r] < 0 or > ids_stride */
+#define IS_ST_TIMEOUT      0x80u  /* a bounded device wait gave up */
+
+typedef enum { IS_F32 = 0, IS_BF16 = 1, IS_F16 = 2 } is_dtype_t;
+
+typedef struct is_store is_store_t;   /* opaque */
+
+/* Store capacity and model KV shape.  Fields set to 0 take the default noted. */
+typedef struct {
+  int32_t num_layers;        /* L */
+  int32_t num_kv_heads;      /* H (KV heads after grouping) */
+  int32_t head_dim;          /* D: power of two, 16 <= D <= IS_MAX_HEAD_DIM */
+  int32_t emb_dim;           /* E: multiple of 8 */
+  int32_t kv_dtype;          /* is_dtype_t of K/V */
+  int32_t emb_dtype;         /* is_dtype_t of embeddings: IS_F16 or IS_F32 */
+  int64_t max_facts;         /* arena capacity in facts */
+  int64_t max_tokens;        /* arena capacity in tokens (sum of fact lengths) */
+  int32_t max_users;         /* user ids are 0 .. max_users-1 */
+  int32_t max_queries;       /* per retrieval call, <= IS_MAX_QUERIES (0: 64) */
+  int32_t max_k;             /* retrieval budget / facts per request, <= IS_MAX_K (0: 256) */
+  int32_t max_requests;      /* per injection call, <= IS_MAX_REQUESTS (0: max_queries) */
+  int64_t max_facts_per_user;/* sizes the score scratch (0: max_facts) */
+} is_store_config_t;
+
+/* Rotary embedding of the model the facts were encoded with. */
+typedef struct {
+  double theta;              /* base, w_i = theta^(-2i/D) */
+  int32_t style;             /* 0 = NeoX half split (i, i+D/2); 1 = interleaved (2i, 2i+1) */
+  int32_t scaling;           /* 0 = none; 1 = Llama-3.1 frequency scaling */
+  double factor;             /* Llama-3.1: scale factor (e.g. 8) */
+  double low_freq_factor;    /* Llama-3.1: e.g. 1 */
+  double high_freq_factor;   /* Llama-3.1: e.g. 4 */
+  int32_t original_max_pos;  /* Llama-3.1: original context length (e.g. 8192) */
+} is_rope_params_t;
+
+/* vLLM-style paged cache [L][2][num_blocks][block_size][H][D]: for layer l,
+ * K at [l][0] and V at [l][1]; logical position p of a sequence lives in
+ * physical block block_table[p / block_size], row p % block_size. */
+typedef struct {
+  int32_t block_size;
+  int32_t num_blocks;
+  int32_t dtype;             /* is_dtype_t; must equal the store's kv_dtype */
+} is_cache_desc_t;
+
+typedef struct {
+  int64_t n_facts, n_tokens;
+  int32_t n_tiles, max_user_tiles;
+  int64_t max_user_facts;
+  int64_t kv_bytes, emb_bytes, scratch_bytes;
+  int32_t num_sms;
+} is_store_info_t;
+
+/* ---- store ------------------------------------------------------------------
+ * is_store_create: allocate a store for one model's KV shape on `device`:
+ * the token-major K/V arena [max_tokens][L][2][H][D], the embedding tiles,
+ * per-fact metadata and all per-call scratch, so that no later call
+ * allocates device memory.  InferScale keeps precomputed per-fact KV and a
+ * semantic embedding GPU-resident (abstract; "Conception de Système Native
+ * au GPU").  Synchronous.  Errors: IS_ERR_INVALID_ARG (bad config),
+ * IS_ERR_UNSUPPORTED (head_dim / row size the kernels do not handle),
+ * IS_ERR_OOM, IS_ERR_CUDA.  *out is owned by the caller; free with
+ * is_store_destroy. */
+is_status_t is_store_create(const is_store_config_t* config, int device, cudaStream_t stream,
+                            is_store_t** out);
+
+/* Free every allocation of the store.  Synchronises the device first. */
+is_status_t is_store_destroy(is_store_t* store);
+
+/* ---- is_store_add_facts -----------------------------------------------------
+ * Add n facts of one user.  Keys are captured before RoPE and values raw
+ * (Chunked RoPE, "Stockage Pré-RoPE"); the store deep-copies them.
+ *   user            0 <= user < max_users
+ *   lengths_host    host int32[n], tokens per fact, each >= 1
+ *   k_pre_rope, v   device or host (any UVA pointer), [sum(lengths)][L][H][D]
+ *                   in kv_dtype, facts back to back in order
+ *   emb             device or host, [n][E] in emb_dtype
+ *   fact_ids_out    host int64[n] (may be NULL): ids assigned, consecutive in
+ *                   insertion order across the store
+ * Facts of one user keep insertion order, which is also ascending id order.
+ * Synchronous with respect to the host (returns after the copies finished).
+ * Errors: IS_ERR_INVALID_ARG, IS_ERR_OUT_OF_RANGE (user), IS_ERR_CAPACITY
+ * (nothing is added), IS_ERR_CUDA. */
+is_status_t is_store_add_facts(is_store_t* store, int32_t user, int32_t n,
+                               const int32_t* lengths_host, const void* k_pre_rope,
+                               const void* v, const void* emb, int64_t* fact_ids_out_host,
+                               cudaStream_t stream);
+
+is_status_t is_store_info(const is_store_t* store, is_store_info_t* out);
+
+/* ---- is_retrieve_topk -------------------------------------------------------
+ * For each query q, the cosine similarity of q_emb[q] with every stored
+ * embedding of user users[q], then the k best (InferScale retrieves the
+ * relevant facts under a budget k: "Problématique", "Conception de Système
+ * Native au GPU"; the index it names is not described, so retrieval is exact).
+ *   Q               1 <= Q <= max_queries
+ *   users           device int32[Q]
+ *   q_emb           device [Q][E] in emb_dtype (need not be normalised)
+ *   k               1 <= k <= max_k
+ *   ids_out         device int64[Q][k]: descending score, ties to the lower
+ *                   fact id; rows of a user with fewer than k facts end in -1
+ *   scores_out      device float[Q][k]: cosine (fp32), -inf where id is -1
+ * A zero-norm embedding or query scores 0.  A bad user id latches
+ * IS_ST_USER_RANGE and yields an all -1 row. */
+is_status_t is_retrieve_topk(is_store_t* store, int32_t Q, const int32_t* users,
+                             const void* q_emb, int32_t k, int64_t* ids_out, float* scores_out,
+                             cudaStream_t stream);
+
+/* ---- is_inject --------------------------------------------------------------
+ * Compose each request's facts, in the order given, into one contiguous
+ * segment starting at seg_start[r]; rotate every stored pre-RoPE key to its
+ * serving position p = seg_start[r] + t (token t of the segment) and
+ * scatter-copy rotated K and raw V for all layers and KV heads into the
+ * paged cache ("Rotation Dynamique", "Injection"; exact by Theorem 6).
+ *   R                    1 <= R <= max_requests
+ *   fact_ids             device int64[R][ids_stride]; first n_ids[r] used
+ *   n_ids                device int32[R], 0 <= n_ids[r] <= ids_stride
+ *   ids_stride           1 <= ids_stride <= max_k
+ *   users                device int32[R] or NULL: if given, every fact of
+ *                        request r must belong to users[r]
+ *   seg_start            device int32[R], >= 0
+ *   rope                 host, read before return
+ *   block_table          device int32[R][max_blocks_per_seq]
+ *   cache, kv_cache      host descriptor / device cache [L][2][NB][bs][H][D]
+ *   seg_len_out          device int32[R] or NULL: tokens injected per request
+ *   slot_mapping_out     device int64[sum seg_len] or NULL: slot of every
+ *                        injected token, requests back to back
+ * An invalid fact (IS_ST_FACT_RANGE / IS_ST_FACT_USER) contributes no
+ * tokens; a position the block table does not map (IS_ST_BLOCK_TABLE,
+ * IS_ST_BLOCK_ID) is not written.  Cache elements of other slots are never
+ * touched.  Slots of one call must be distinct (two tokens on one slot race). */
+is_status_t is_inject(is_store_t* store, int32_t R, const int64_t* fact_ids,
+                      const int32_t* n_ids, int32_t ids_stride, const int32_t* users,
+                      const int32_t* seg_start, const is_rope_params_t* rope,
+                      const int32_t* block_table, int32_t max_blocks_per_seq,
+                      const is_cache_desc_t* cache, void* kv_cache, int32_t* seg_len_out,
+                      int64_t* slot_mapping_out, cudaStream_t stream);
+
+/* ---- is_retrieve_and_inject -------------------------------------------------
+ * is_retrieve_topk followed by is_inject of each query's k facts in
+ * descending-score order, with no host synchronisation between the stages
+ * (the ids never leave the device).  Arguments as in those calls; ids_out,
+ * scores_out (device [Q][k]), seg_len_out (device int32[Q]) and
+ * slot_mapping_out may each be NULL. */
+is_status_t is_retrieve_and_inject(is_store_t* store, int32_t Q, const int32_t* users,
+                                   const void* q_emb, int32_t k, const int32_t* seg_start,
+                                   const is_rope_params_t* rope, const int32_t* block_table,
+                                   int32_t max_blocks_per_seq, const is_cache_desc_t* cache,
+                                   void* kv_cache, int64_t* ids_out, float* scores_out,
+                                   int32_t* seg_len_out, int64_t* slot_mapping_out,
+                                   cudaStream_t stream);
+
+/* ---- status / diagnostics ---------------------------------------------------
+ * is_get_status: synchronise `stream`, read the device status word into
+ * *bits_out and clear it.  Returns IS_ERR_DEVICE if any bit was set,
+ * IS_ERR_TIMEOUT if IS_ST_TIMEOUT was, IS_ERR_CUDA if the stream reported an
+ * error. */
+is_status_t is_get_status(is_store_t* store, cudaStream_t stream, uint32_t* bits_out);
+
+/* Message of the calling thread's last failed call ("" if none). */
+const char* is_last_error_message(void);
+const char* is_status_string(is_status_t status);
+
+/* The rotation frequencies w_i (i < head_dim/2) the kernels use, in fp64,
+ * into host double[head_dim/2].  Plain: theta^(-2i/D); Llama-3.1 scaling:
+ * the published Llama 3.1 rule (wavelength bands original_max_pos /
+ * high_freq_factor and original_max_pos / low_freq_factor). */
+is_status_t is_rope_frequencies(const is_rope_params_t* rope, int32_t head_dim,
+                                double* inv_freq_out_host);
+
+/* ---- stage timing -------------------------------------------------------------
+ * When enabled, every kernel launch of the store is bracketed by CUDA events
+ * on its stream.  is_get_timing synchronises the device and returns, for a
+ * stage, the summed device time (ms) and the number of launches since the
+ * last reset.  Stages: IS_STAGE_SIMILARITY, IS_STAGE_TOPK, IS_STAGE_PLAN,
+ * IS_STAGE_INJECT. */
+#define IS_STAGE_SIMILARITY 0
+#define IS_STAGE_TOPK       1
+#define IS_STAGE_PLAN       2
+#define IS_STAGE_INJECT     3
+#define IS_NUM_STAGES       4
+is_status_t is_set_timing(is_store_t* store, int32_t enable);
+is_status_t is_get_timing(is_store_t* store, int32_t stage, double* total_ms, int64_t* launches);
+is_status_t is_reset_timing(is_store_t* store);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* INJECTSCALE_H */

@@ -1,0 +1,170 @@
+"""Python binding of the C ABI, same names as include/injectscale.h.
+
+Argument marshalling only: tensors become pointers, dicts become the C
+structs, non-OK statuses become ISError.  Every step of the path runs in the
+CUDA kernels of libinjectscale.so; nothing here computes.
+"""
+from __future__ import annotations
+
+import ctypes
+from ctypes import byref, c_double, c_int64, c_uint32, c_void_p
+
+import numpy as np
+
+from . import _lib
+from ._lib import CacheDesc, RopeParams, StoreConfig, StoreInfo
+
+DTYPE_CODES = {"f32": _lib.IS_F32, "bf16": _lib.IS_BF16, "f16": _lib.IS_F16}
+
+
+class ISError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        self.status = status
+        super().__init__(f"{_lib.STATUS_NAMES.get(status, status)}: {message}")
+
+
+def _check(status: int) -> None:
+    if status != _lib.IS_OK:
+        msg = _lib.load().is_last_error_message()
+        raise ISError(status, msg.decode() if msg else "")
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream if torch.cuda.is_available() else 0
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _ptr(t) -> int | None:
+    if t is None:
+        return None
+    if hasattr(t, "data_ptr"):
+        if not t.is_contiguous():
+            raise ValueError("tensor arguments must be contiguous")
+        return t.data_ptr()
+    return int(t)
+
+
+class Store:
+    """Owning handle of an is_store_t."""
+
+    def __init__(self, handle: int, config: StoreConfig, device: int):
+        self.handle = handle
+        self.config = config
+        self.device = device
+
+    def destroy(self) -> None:
+        if self.handle:
+            _check(_lib.load().is_store_destroy(c_void_p(self.handle)))
+            self.handle = 0
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.destroy()
+
+
+def make_config(**kw) -> StoreConfig:
+    c = StoreConfig()
+    for k, v in kw.items():
+        if k in ("kv_dtype", "emb_dtype") and isinstance(v, str):
+            v = DTYPE_CODES[v]
+        setattr(c, k, int(v))
+    return c
+
+
+def make_rope(theta: float, style: int = 0, scaling: int = 0, factor: float = 1.0,
+              low_freq_factor: float = 1.0, high_freq_factor: float = 1.0,
+              original_max_pos: int = 0) -> RopeParams:
+    return RopeParams(theta, style, scaling, factor, low_freq_factor, high_freq_factor,
+                      original_max_pos)
+
+
+def make_cache_desc(block_size: int, num_blocks: int, dtype) -> CacheDesc:
+    return CacheDesc(block_size, num_blocks, DTYPE_CODES[dtype] if isinstance(dtype, str) else dtype)
+
+
+def is_store_create(config: StoreConfig, device: int = 0, stream=None) -> Store:
+    h = c_void_p()
+    _check(_lib.load().is_store_create(byref(config), device, _stream(stream), byref(h)))
+    return Store(h.value, config, device)
+
+
+def is_store_destroy(store: Store) -> None:
+    store.destroy()
+
+
+def is_store_add_facts(store: Store, user: int, lengths, k_pre_rope, v, emb, stream=None) -> np.ndarray:
+    lengths = np.ascontiguousarray(lengths, dtype=np.int32)
+    ids = np.empty(len(lengths), dtype=np.int64)
+    _check(_lib.load().is_store_add_facts(
+        c_void_p(store.handle), int(user), len(lengths),
+        lengths.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)), _ptr(k_pre_rope), _ptr(v),
+        _ptr(emb), ids.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), _stream(stream)))
+    return ids
+
+
+def is_store_info(store: Store) -> dict:
+    info = StoreInfo()
+    _check(_lib.load().is_store_info(c_void_p(store.handle), byref(info)))
+    return {name: getattr(info, name) for name, _ in StoreInfo._fields_}
+
+
+def is_retrieve_topk(store: Store, users, q_emb, k: int, ids_out, scores_out, stream=None) -> None:
+    _check(_lib.load().is_retrieve_topk(
+        c_void_p(store.handle), int(users.shape[0]), _ptr(users), _ptr(q_emb), int(k),
+        _ptr(ids_out), _ptr(scores_out), _stream(stream)))
+
+
+def is_inject(store: Store, fact_ids, n_ids, seg_start, rope: RopeParams, block_table,
+              cache: CacheDesc, kv_cache, users=None, seg_len_out=None, slot_mapping_out=None,
+              stream=None) -> None:
+    R, stride = int(fact_ids.shape[0]), int(fact_ids.shape[1])
+    _check(_lib.load().is_inject(
+        c_void_p(store.handle), R, _ptr(fact_ids), _ptr(n_ids), stride, _ptr(users),
+        _ptr(seg_start), byref(rope), _ptr(block_table), int(block_table.shape[1]), byref(cache),
+        _ptr(kv_cache), _ptr(seg_len_out), _ptr(slot_mapping_out), _stream(stream)))
+
+
+def is_retrieve_and_inject(store: Store, users, q_emb, k: int, seg_start, rope: RopeParams,
+                           block_table, cache: CacheDesc, kv_cache, ids_out=None, scores_out=None,
+                           seg_len_out=None, slot_mapping_out=None, stream=None) -> None:
+    _check(_lib.load().is_retrieve_and_inject(
+        c_void_p(store.handle), int(users.shape[0]), _ptr(users), _ptr(q_emb), int(k),
+        _ptr(seg_start), byref(rope), _ptr(block_table), int(block_table.shape[1]), byref(cache),
+        _ptr(kv_cache), _ptr(ids_out), _ptr(scores_out), _ptr(seg_len_out),
+        _ptr(slot_mapping_out), _stream(stream)))
+
+
+def is_get_status(store: Store, stream=None) -> int:
+    """Device status bits since the last read (cleared).  Raises only on CUDA errors."""
+    bits = c_uint32()
+    st = _lib.load().is_get_status(c_void_p(store.handle), _stream(stream), byref(bits))
+    if st not in (_lib.IS_OK, 6, 7):
+        _check(st)
+    return int(bits.value)
+
+
+def is_rope_frequencies(rope: RopeParams, head_dim: int) -> np.ndarray:
+    out = np.empty(head_dim // 2, dtype=np.float64)
+    _check(_lib.load().is_rope_frequencies(byref(rope), int(head_dim),
+                                           out.ctypes.data_as(ctypes.POINTER(ctypes.c_double))))
+    return out
+
+
+def is_set_timing(store: Store, enable: bool) -> None:
+    _check(_lib.load().is_set_timing(c_void_p(store.handle), 1 if enable else 0))
+
+
+def is_get_timing(store: Store, stage: int) -> tuple[float, int]:
+    ms, n = c_double(), c_int64()
+    _check(_lib.load().is_get_timing(c_void_p(store.handle), int(stage), byref(ms), byref(n)))
+    return ms.value, n.value
+
+
+def is_reset_timing(store: Store) -> None:
+    _check(_lib.load().is_reset_timing(c_void_p(store.handle)))

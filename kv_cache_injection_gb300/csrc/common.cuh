@@ -1,0 +1,220 @@
+// Device helpers and launch-parameter structs shared by the kernels of
+// libinjectscale.so (GB300, sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "injectscale.h"
+
+namespace isk {
+
+constexpr int kMaxHalfDim = IS_MAX_HEAD_DIM / 2;
+constexpr int kTile = IS_EMB_TILE;
+
+// Rotation frequencies as turns per position (w_i / 2 pi), each split into
+// two floats hi + lo so that the angle reduction runs in fp32 (see
+// angle_turns).  Passed by value as a kernel parameter (2 KiB).
+struct RopeTurns {
+  float hi[kMaxHalfDim];
+  float lo[kMaxHalfDim];
+};
+
+// Everything the gather + Chunked RoPE + paged scatter kernel reads.
+struct InjectArgs {
+  const uint8_t* kv;            // store arena [max_tokens][L][2][H][D]
+  const int64_t* fact_tok;      // first arena token of each fact
+  const int32_t* fact_len;
+  const int32_t* fact_user;
+  int64_t n_facts;
+  const int64_t* ids;           // [R][ids_stride]
+  int32_t ids_stride;
+  const int32_t* n_ids;         // [R] facts per request (after planning)
+  const int32_t* fact_seg_off;  // [R][seg_stride]: exclusive prefix of fact lengths
+  int32_t seg_stride;
+  const int32_t* seg_len;       // [R]
+  const int32_t* seg_start;     // [R]
+  const int32_t* block_table;   // [R][max_blocks]
+  int32_t max_blocks;
+  uint8_t* cache;               // [L][2][num_blocks][bs][H][D]
+  int32_t block_size;
+  int32_t num_blocks;
+  int64_t* slot_mapping;        // [sum seg_len] or null
+  uint32_t* status;
+  int32_t R;
+  int32_t L;
+  int32_t row_bytes;            // H * D * elt
+  int32_t half_vecs;            // NeoX: 16-byte vectors per half head (D / 2 / VE)
+  int32_t head_vecs;            // 16-byte vectors per head (D / VE)
+};
+
+// Segment planning for an explicit fact list (is_inject).
+struct PlanArgs {
+  const int64_t* ids;
+  int32_t ids_stride;
+  const int32_t* n_ids_in;      // caller's counts [R]
+  const int32_t* users;         // [R] or null
+  const int32_t* seg_start;
+  const int32_t* fact_len;
+  const int32_t* fact_user;
+  int64_t n_facts;
+  int32_t* n_ids_out;           // [R]
+  int32_t* fact_seg_off;        // [R][seg_stride]
+  int32_t seg_stride;
+  int32_t* seg_len;             // [R]
+  uint32_t* status;
+  int32_t R;
+};
+
+struct SimArgs {
+  const void* emb;              // tiles [n_tiles * kTile][E]
+  const float* emb_inv_norm;    // [n_tiles * kTile]
+  const int32_t* user_nfacts;   // [max_users]
+  const int32_t* user_tile_off; // [max_users + 1]
+  const int32_t* user_tiles;    // tiles of each user, in fill order
+  const int32_t* users;         // [Q]
+  const void* q_emb;            // [Q][E]
+  float* scores;                // [Q][score_stride]
+  int64_t score_stride;
+  uint32_t* status;
+  int32_t Q;
+  int32_t E;
+  int32_t max_users;
+};
+
+struct TopkArgs {
+  const float* scores;
+  int64_t score_stride;
+  const int32_t* users;
+  const int32_t* user_nfacts;
+  const int32_t* user_tile_off;
+  const int32_t* user_tiles;
+  const int32_t* tile_fact;     // [n_tiles * kTile] fact id per embedding row
+  const int32_t* fact_len;
+  const int32_t* seg_start;     // [Q] or null (retrieval only)
+  int64_t* ids_out;             // [Q][k]
+  float* scores_out;            // [Q][k]
+  int32_t* n_ids_out;           // [Q] or null
+  int32_t* fact_seg_off;        // [Q][seg_stride] or null
+  int32_t seg_stride;
+  int32_t* seg_len;             // [Q] or null
+  uint32_t* status;
+  int32_t Q;
+  int32_t k;
+  int32_t max_users;
+};
+
+// ------------------------------------------------------------------ device helpers
+
+__device__ __forceinline__ void latch(uint32_t* status, uint32_t bits) { atomicOr(status, bits); }
+
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+// 16-byte streaming load of data that is read once: no L1 allocation,
+// evict-first in L2 so it does not push out cache lines attention will read.
+__device__ __forceinline__ uint4 ld_once(const void* ptr, uint64_t policy) {
+  uint4 r;
+  asm("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+      : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+      : "l"(ptr), "l"(policy));
+  return r;
+}
+
+__device__ __forceinline__ void st_v4(void* ptr, const uint4& v) {
+  asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(ptr), "r"(v.x), "r"(v.y),
+               "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
+__device__ __forceinline__ uint4 shfl_xor4(const uint4& v, int mask) {
+  uint4 r;
+  r.x = __shfl_xor_sync(0xffffffffu, v.x, mask);
+  r.y = __shfl_xor_sync(0xffffffffu, v.y, mask);
+  r.z = __shfl_xor_sync(0xffffffffu, v.z, mask);
+  r.w = __shfl_xor_sync(0xffffffffu, v.w, mask);
+  return r;
+}
+
+// Element access on a 16-byte vector of T.
+template <typename T> struct Vec;
+
+template <> struct Vec<float> {
+  static constexpr int N = 4;
+  __device__ __forceinline__ static void unpack(const uint4& v, float* f) {
+    f[0] = __uint_as_float(v.x); f[1] = __uint_as_float(v.y);
+    f[2] = __uint_as_float(v.z); f[3] = __uint_as_float(v.w);
+  }
+  __device__ __forceinline__ static uint4 pack(const float* f) {
+    return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]),
+                      __float_as_uint(f[3]));
+  }
+};
+
+template <> struct Vec<__nv_bfloat16> {
+  static constexpr int N = 8;
+  __device__ __forceinline__ static void unpack(const uint4& v, float* f) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      f[2 * i] = __uint_as_float(w[i] << 16);
+      f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+  }
+  __device__ __forceinline__ static uint32_t pack2(float lo, float hi) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);   // round to nearest even
+    return *reinterpret_cast<uint32_t*>(&h);
+  }
+  __device__ __forceinline__ static uint4 pack(const float* f) {
+    return make_uint4(pack2(f[0], f[1]), pack2(f[2], f[3]), pack2(f[4], f[5]), pack2(f[6], f[7]));
+  }
+};
+
+template <> struct Vec<__half> {
+  static constexpr int N = 8;
+  __device__ __forceinline__ static void unpack(const uint4& v, float* f) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      __half2 h = *reinterpret_cast<const __half2*>(&w[i]);
+      float2 t = __half22float2(h);
+      f[2 * i] = t.x;
+      f[2 * i + 1] = t.y;
+    }
+  }
+  __device__ __forceinline__ static uint32_t pack2(float lo, float hi) {
+    __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+  }
+  __device__ __forceinline__ static uint4 pack(const float* f) {
+    return make_uint4(pack2(f[0], f[1]), pack2(f[2], f[3]), pack2(f[4], f[5]), pack2(f[6], f[7]));
+  }
+};
+
+// Fraction of a turn, in [-1/2, 1/2], of the angle p * w_i = 2 pi p t_i, with
+// t_i = hi + lo.  p * hi is split exactly into a rounded product and its
+// error term (Dekker's product through a fused multiply-add); the integer part
+// of the rounded product is removed exactly, so the result keeps fp32
+// precision relative to 1/2 whatever the size of p (p < 2^24).
+__device__ __forceinline__ float angle_turns(float p, float hi, float lo) {
+  const float prod = p * hi;
+  const float err = fmaf(p, hi, -prod);
+  const float frac = prod - rintf(prod);
+  return frac + fmaf(p, lo, err);
+}
+
+// Order-preserving map of fp32 scores onto uint32 keys (larger score, larger key).
+__device__ __forceinline__ uint32_t score_key(float s) {
+  const uint32_t b = __float_as_uint(s);
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ float key_score(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
+}  // namespace isk

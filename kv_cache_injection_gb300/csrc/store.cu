@@ -1,0 +1,754 @@
+// C ABI of libinjectscale.so: the GPU fact store, argument validation and
+// the launch sequences of the retrieval and injection calls.
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "injectscale.h"
+#include "internal.h"
+
+using namespace isk;
+
+namespace {
+
+thread_local std::string g_err;
+
+is_status_t fail(is_status_t s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_err = buf;
+  return s;
+}
+
+#define CUDA_TRY(expr)                                                                  \
+  do {                                                                                  \
+    cudaError_t e_ = (expr);                                                            \
+    if (e_ != cudaSuccess)                                                              \
+      return fail(IS_ERR_CUDA, "%s failed: %s", #expr, cudaGetErrorString(e_));         \
+  } while (0)
+
+int dtype_bytes(int dt) { return dt == IS_F32 ? 4 : 2; }
+bool valid_kv_dtype(int dt) { return dt == IS_F32 || dt == IS_BF16 || dt == IS_F16; }
+bool is_pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
+
+class DeviceGuard {
+ public:
+  explicit DeviceGuard(int dev) {
+    cudaGetDevice(&prev_);
+    if (prev_ != dev) cudaSetDevice(dev);
+  }
+  ~DeviceGuard() {
+    int cur = -1;
+    cudaGetDevice(&cur);
+    if (cur != prev_) cudaSetDevice(prev_);
+  }
+
+ private:
+  int prev_ = 0;
+};
+
+struct EventPair {
+  cudaEvent_t a, b;
+};
+
+}  // namespace
+
+struct is_store {
+  is_store_config_t cfg{};
+  int device = 0;
+  int num_sms = 0;
+  int elt = 0;
+  int emb_elt = 0;
+  int64_t row_bytes = 0;          // H * D * elt
+  int64_t tok_bytes = 0;          // L * 2 * row_bytes
+  int64_t max_tiles = 0;
+  int64_t score_stride = 0;
+  int32_t seg_stride = 0;
+  int inject_ctas = 0;
+
+  uint8_t* kv = nullptr;
+  int64_t* fact_tok = nullptr;
+  int32_t* fact_len = nullptr;
+  int32_t* fact_user = nullptr;
+  uint8_t* emb = nullptr;
+  float* emb_inv_norm = nullptr;
+  int32_t* tile_fact = nullptr;
+  int32_t* user_nfacts = nullptr;
+  int32_t* user_tile_off = nullptr;
+  int32_t* user_tiles = nullptr;
+  float* scores = nullptr;
+  int64_t* ids_tmp = nullptr;
+  float* scores_tmp = nullptr;
+  int32_t* fact_seg_off = nullptr;
+  int32_t* n_ids = nullptr;
+  int32_t* seg_len_tmp = nullptr;
+  int32_t* rows_tmp = nullptr;
+  uint32_t* status = nullptr;
+  int64_t scratch_bytes = 0;
+
+  int64_t n_facts = 0, n_tokens = 0;
+  int32_t n_tiles = 0;
+  int32_t max_len = 0;
+  std::vector<std::vector<int32_t>> user_tiles_h;
+  std::vector<int32_t> user_nfacts_h;
+  std::vector<int32_t> tile_rows_h;
+  int32_t max_user_tiles = 0;
+  int64_t max_user_facts = 0;
+
+  bool timing = false;
+  std::vector<EventPair> pending[IS_NUM_STAGES];
+  std::vector<cudaEvent_t> event_pool;
+  double total_ms[IS_NUM_STAGES] = {};
+  int64_t launches[IS_NUM_STAGES] = {};
+};
+
+namespace {
+
+template <typename P>
+is_status_t dev_alloc(P** p, size_t bytes, is_store_t* s, const char* what) {
+  void* v = nullptr;
+  cudaError_t e = cudaMalloc(&v, bytes > 0 ? bytes : 16);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return fail(IS_ERR_OOM, "cudaMalloc(%zu bytes) for %s failed: %s", bytes, what,
+                cudaGetErrorString(e));
+  }
+  *p = static_cast<P*>(v);
+  if (s) s->scratch_bytes += 0;
+  return IS_OK;
+}
+
+void free_store(is_store_t* s) {
+  void* ptrs[] = {s->kv, s->fact_tok, s->fact_len, s->fact_user, s->emb, s->emb_inv_norm,
+                  s->tile_fact, s->user_nfacts, s->user_tile_off, s->user_tiles, s->scores,
+                  s->ids_tmp, s->scores_tmp, s->fact_seg_off, s->n_ids, s->seg_len_tmp,
+                  s->rows_tmp, s->status};
+  for (void* p : ptrs)
+    if (p) cudaFree(p);
+  for (int st = 0; st < IS_NUM_STAGES; ++st)
+    for (auto& ev : s->pending[st]) {
+      cudaEventDestroy(ev.a);
+      cudaEventDestroy(ev.b);
+    }
+  for (auto ev : s->event_pool) cudaEventDestroy(ev);
+  delete s;
+}
+
+cudaEvent_t take_event(is_store_t* s) {
+  if (!s->event_pool.empty()) {
+    cudaEvent_t e = s->event_pool.back();
+    s->event_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  cudaEventCreate(&e);
+  return e;
+}
+
+// Brackets one launch with events when timing is enabled.
+struct StageTimer {
+  StageTimer(is_store_t* s, int stage, cudaStream_t st) : s_(s), stage_(stage), st_(st) {
+    if (s_->timing) {
+      ev_.a = take_event(s_);
+      ev_.b = take_event(s_);
+      cudaEventRecord(ev_.a, st_);
+    }
+  }
+  ~StageTimer() {
+    if (s_->timing) {
+      cudaEventRecord(ev_.b, st_);
+      s_->pending[stage_].push_back(ev_);
+    }
+  }
+  is_store_t* s_;
+  int stage_;
+  cudaStream_t st_;
+  EventPair ev_{};
+};
+
+void rope_inv_freq(const is_rope_params_t& r, int D, double* out) {
+  const double two_pi = 6.283185307179586476925286766559;
+  for (int i = 0; i < D / 2; ++i) {
+    double w = std::pow(r.theta, -(2.0 * i) / D);
+    if (r.scaling == 1) {
+      const double lam = two_pi / w;
+      const double high_wavelen = r.original_max_pos / r.high_freq_factor;
+      const double low_wavelen = r.original_max_pos / r.low_freq_factor;
+      if (lam > low_wavelen) {
+        w = w / r.factor;
+      } else if (lam >= high_wavelen) {
+        const double s = (r.original_max_pos / lam - r.low_freq_factor) /
+                         (r.high_freq_factor - r.low_freq_factor);
+        w = (1.0 - s) * w / r.factor + s * w;
+      }
+    }
+    out[i] = w;
+  }
+}
+
+is_status_t check_rope(const is_rope_params_t* r, int D, int kv_dtype) {
+  if (!r) return fail(IS_ERR_INVALID_ARG, "rope params are NULL");
+  if (!(r->theta > 1.0) || !std::isfinite(r->theta))
+    return fail(IS_ERR_INVALID_ARG, "rope theta must be finite and > 1");
+  if (r->style != 0 && r->style != 1) return fail(IS_ERR_INVALID_ARG, "rope style must be 0 or 1");
+  if (r->scaling == 1) {
+    if (!(r->factor > 0) || !(r->low_freq_factor > 0) ||
+        !(r->high_freq_factor > r->low_freq_factor) || r->original_max_pos <= 0)
+      return fail(IS_ERR_INVALID_ARG, "bad Llama-3.1 scaling parameters");
+  } else if (r->scaling != 0) {
+    return fail(IS_ERR_INVALID_ARG, "rope scaling must be 0 or 1");
+  }
+  const int ve = 16 / dtype_bytes(kv_dtype);
+  const int vecs = r->style == 0 ? D / 2 / ve : D / ve;
+  if (vecs < 1 || vecs > 32)
+    return fail(IS_ERR_UNSUPPORTED, "head_dim %d with this dtype/style needs %d vectors per %s", D,
+                vecs, r->style == 0 ? "half head (max 32)" : "head (max 32)");
+  return IS_OK;
+}
+
+RopeTurns make_turns(const is_rope_params_t& r, int D) {
+  RopeTurns t;
+  std::memset(&t, 0, sizeof t);
+  double w[kMaxHalfDim];
+  rope_inv_freq(r, D, w);
+  const double two_pi = 6.283185307179586476925286766559;
+  for (int i = 0; i < D / 2; ++i) {
+    const double turns = w[i] / two_pi;
+    t.hi[i] = (float)turns;
+    t.lo[i] = (float)(turns - (double)t.hi[i]);
+  }
+  return t;
+}
+
+is_status_t check_cache(const is_store_t* s, const is_cache_desc_t* c, const void* kv_cache) {
+  if (!c || !kv_cache) return fail(IS_ERR_INVALID_ARG, "cache descriptor or kv_cache is NULL");
+  if (c->block_size <= 0 || c->num_blocks <= 0)
+    return fail(IS_ERR_INVALID_ARG, "block_size and num_blocks must be > 0");
+  if (c->dtype != s->cfg.kv_dtype)
+    return fail(IS_ERR_INVALID_ARG, "cache dtype %d differs from the store's kv dtype %d", c->dtype,
+                s->cfg.kv_dtype);
+  if (((uintptr_t)kv_cache & 15) != 0) return fail(IS_ERR_INVALID_ARG, "kv_cache must be 16-byte aligned");
+  return IS_OK;
+}
+
+is_status_t upload_user_index(is_store_t* s, cudaStream_t st) {
+  const int U = s->cfg.max_users;
+  std::vector<int32_t> off(U + 1, 0), tiles;
+  tiles.reserve(s->n_tiles);
+  for (int u = 0; u < U; ++u) {
+    off[u] = (int32_t)tiles.size();
+    tiles.insert(tiles.end(), s->user_tiles_h[u].begin(), s->user_tiles_h[u].end());
+  }
+  off[U] = (int32_t)tiles.size();
+  CUDA_TRY(cudaMemcpyAsync(s->user_tile_off, off.data(), off.size() * 4, cudaMemcpyHostToDevice, st));
+  if (!tiles.empty())
+    CUDA_TRY(cudaMemcpyAsync(s->user_tiles, tiles.data(), tiles.size() * 4, cudaMemcpyHostToDevice, st));
+  CUDA_TRY(cudaMemcpyAsync(s->user_nfacts, s->user_nfacts_h.data(), (size_t)U * 4,
+                           cudaMemcpyHostToDevice, st));
+  CUDA_TRY(cudaStreamSynchronize(st));   // host vectors die on return
+  return IS_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* is_last_error_message(void) { return g_err.c_str(); }
+
+const char* is_status_string(is_status_t s) {
+  switch (s) {
+    case IS_OK: return "IS_OK";
+    case IS_ERR_INVALID_ARG: return "IS_ERR_INVALID_ARG";
+    case IS_ERR_OOM: return "IS_ERR_OOM";
+    case IS_ERR_CAPACITY: return "IS_ERR_CAPACITY";
+    case IS_ERR_OUT_OF_RANGE: return "IS_ERR_OUT_OF_RANGE";
+    case IS_ERR_CUDA: return "IS_ERR_CUDA";
+    case IS_ERR_TIMEOUT: return "IS_ERR_TIMEOUT";
+    case IS_ERR_DEVICE: return "IS_ERR_DEVICE";
+    case IS_ERR_UNSUPPORTED: return "IS_ERR_UNSUPPORTED";
+  }
+  return "IS_ERR_UNKNOWN";
+}
+
+is_status_t is_rope_frequencies(const is_rope_params_t* rope, int32_t head_dim, double* out) {
+  if (!rope || !out) return fail(IS_ERR_INVALID_ARG, "NULL argument");
+  if (head_dim < 2 || head_dim > IS_MAX_HEAD_DIM || head_dim % 2)
+    return fail(IS_ERR_INVALID_ARG, "head_dim must be even and <= %d", IS_MAX_HEAD_DIM);
+  is_status_t st = check_rope(rope, head_dim, IS_BF16);
+  if (st != IS_OK && st != IS_ERR_UNSUPPORTED) return st;
+  rope_inv_freq(*rope, head_dim, out);
+  return IS_OK;
+}
+
+is_status_t is_store_create(const is_store_config_t* config, int device, cudaStream_t stream,
+                            is_store_t** out) {
+  if (!config || !out) return fail(IS_ERR_INVALID_ARG, "NULL config or out");
+  *out = nullptr;
+  is_store_config_t c = *config;
+  if (c.num_layers <= 0 || c.num_kv_heads <= 0 || c.head_dim <= 0 || c.emb_dim <= 0)
+    return fail(IS_ERR_INVALID_ARG, "layers, kv heads, head_dim and emb_dim must be > 0");
+  if (!valid_kv_dtype(c.kv_dtype)) return fail(IS_ERR_INVALID_ARG, "bad kv_dtype %d", c.kv_dtype);
+  if (c.emb_dtype != IS_F16 && c.emb_dtype != IS_F32)
+    return fail(IS_ERR_INVALID_ARG, "emb_dtype must be IS_F16 or IS_F32");
+  if (c.max_facts <= 0 || c.max_tokens <= 0 || c.max_users <= 0)
+    return fail(IS_ERR_INVALID_ARG, "max_facts, max_tokens and max_users must be > 0");
+  if (c.max_facts >= (int64_t)INT32_MAX)
+    return fail(IS_ERR_INVALID_ARG, "max_facts must be < 2^31");
+  if (c.max_queries == 0) c.max_queries = 64;
+  if (c.max_k == 0) c.max_k = 256;
+  if (c.max_requests == 0) c.max_requests = c.max_queries;
+  if (c.max_facts_per_user <= 0 || c.max_facts_per_user > c.max_facts) c.max_facts_per_user = c.max_facts;
+  if (c.max_queries < 1 || c.max_queries > IS_MAX_QUERIES)
+    return fail(IS_ERR_INVALID_ARG, "max_queries must be in [1, %d]", IS_MAX_QUERIES);
+  if (c.max_k < 1 || c.max_k > IS_MAX_K) return fail(IS_ERR_INVALID_ARG, "max_k must be in [1, %d]", IS_MAX_K);
+  if (c.max_requests < 1 || c.max_requests > IS_MAX_REQUESTS)
+    return fail(IS_ERR_INVALID_ARG, "max_requests must be in [1, %d]", IS_MAX_REQUESTS);
+  if (c.emb_dim % 8 != 0) return fail(IS_ERR_UNSUPPORTED, "emb_dim must be a multiple of 8");
+  const int D = c.head_dim;
+  if (!is_pow2(D) || D < 16 || D > IS_MAX_HEAD_DIM)
+    return fail(IS_ERR_UNSUPPORTED, "head_dim must be a power of two in [16, %d]", IS_MAX_HEAD_DIM);
+  const int elt = dtype_bytes(c.kv_dtype);
+  const int64_t row_bytes = (int64_t)c.num_kv_heads * D * elt;
+  if (row_bytes % 512 != 0)
+    return fail(IS_ERR_UNSUPPORTED, "num_kv_heads * head_dim * elt (%lld B) must be a multiple of 512",
+                (long long)row_bytes);
+
+  int ndev = 0;
+  if (cudaGetDeviceCount(&ndev) != cudaSuccess || ndev == 0) {
+    cudaGetLastError();
+    return fail(IS_ERR_CUDA, "no CUDA device");
+  }
+  if (device < 0 || device >= ndev) return fail(IS_ERR_INVALID_ARG, "device %d out of range", device);
+  DeviceGuard g(device);
+
+  is_store_t* s = new is_store_t();
+  s->cfg = c;
+  s->device = device;
+  cudaDeviceGetAttribute(&s->num_sms, cudaDevAttrMultiProcessorCount, device);
+  s->elt = elt;
+  s->emb_elt = dtype_bytes(c.emb_dtype);
+  s->row_bytes = row_bytes;
+  s->tok_bytes = (int64_t)c.num_layers * 2 * row_bytes;
+  s->max_tiles = (c.max_facts + kTile - 1) / kTile + c.max_users;
+  s->score_stride = (c.max_facts_per_user + kTile - 1) / kTile * kTile;
+  s->seg_stride = c.max_k + 1;
+  s->user_tiles_h.assign(c.max_users, {});
+  s->user_nfacts_h.assign(c.max_users, 0);
+
+  is_status_t st = IS_OK;
+  const size_t Q = c.max_queries, R = std::max(c.max_requests, c.max_queries);
+#define ALLOC(ptr, bytes, what)                              \
+  if ((st = dev_alloc(&s->ptr, (bytes), s, what)) != IS_OK) { \
+    free_store(s);                                           \
+    return st;                                               \
+  }
+  ALLOC(kv, (size_t)c.max_tokens * s->tok_bytes, "K/V arena");
+  ALLOC(fact_tok, (size_t)c.max_facts * 8, "fact offsets");
+  ALLOC(fact_len, (size_t)c.max_facts * 4, "fact lengths");
+  ALLOC(fact_user, (size_t)c.max_facts * 4, "fact users");
+  ALLOC(emb, (size_t)s->max_tiles * kTile * c.emb_dim * s->emb_elt, "embedding tiles");
+  ALLOC(emb_inv_norm, (size_t)s->max_tiles * kTile * 4, "embedding norms");
+  ALLOC(tile_fact, (size_t)s->max_tiles * kTile * 4, "tile fact ids");
+  ALLOC(user_nfacts, (size_t)c.max_users * 4, "user counts");
+  ALLOC(user_tile_off, (size_t)(c.max_users + 1) * 4, "user tile offsets");
+  ALLOC(user_tiles, (size_t)s->max_tiles * 4, "user tiles");
+  ALLOC(scores, Q * s->score_stride * 4, "score scratch");
+  ALLOC(ids_tmp, Q * c.max_k * 8, "id scratch");
+  ALLOC(scores_tmp, Q * c.max_k * 4, "top-k score scratch");
+  ALLOC(fact_seg_off, R * s->seg_stride * 4, "segment plan");
+  ALLOC(n_ids, R * 4, "fact counts");
+  ALLOC(seg_len_tmp, R * 4, "segment lengths");
+  ALLOC(rows_tmp, (size_t)c.max_facts * 4, "row list");
+  ALLOC(status, 4, "status word");
+#undef ALLOC
+  s->scratch_bytes = (int64_t)(Q * s->score_stride * 4 + Q * c.max_k * 12 +
+                               R * (s->seg_stride * 4 + 8) + (size_t)c.max_facts * 4 + 4);
+  cudaError_t e = cudaMemsetAsync(s->status, 0, 4, stream);
+  if (e == cudaSuccess) e = cudaMemsetAsync(s->user_tile_off, 0, (size_t)(c.max_users + 1) * 4, stream);
+  if (e == cudaSuccess) e = cudaMemsetAsync(s->user_nfacts, 0, (size_t)c.max_users * 4, stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) {
+    free_store(s);
+    return fail(IS_ERR_CUDA, "store initialisation failed: %s", cudaGetErrorString(e));
+  }
+  s->inject_ctas = inject_ctas_per_sm(c.kv_dtype, 0, (int)(row_bytes >> 9));
+  *out = s;
+  return IS_OK;
+}
+
+is_status_t is_store_destroy(is_store_t* s) {
+  if (!s) return fail(IS_ERR_INVALID_ARG, "NULL store");
+  DeviceGuard g(s->device);
+  cudaDeviceSynchronize();
+  free_store(s);
+  return IS_OK;
+}
+
+is_status_t is_store_info(const is_store_t* s, is_store_info_t* out) {
+  if (!s || !out) return fail(IS_ERR_INVALID_ARG, "NULL argument");
+  out->n_facts = s->n_facts;
+  out->n_tokens = s->n_tokens;
+  out->n_tiles = s->n_tiles;
+  out->max_user_tiles = s->max_user_tiles;
+  out->max_user_facts = s->max_user_facts;
+  out->kv_bytes = s->cfg.max_tokens * s->tok_bytes;
+  out->emb_bytes = s->max_tiles * kTile * s->cfg.emb_dim * s->emb_elt;
+  out->scratch_bytes = s->scratch_bytes;
+  out->num_sms = s->num_sms;
+  return IS_OK;
+}
+
+is_status_t is_store_add_facts(is_store_t* s, int32_t user, int32_t n, const int32_t* lengths,
+                               const void* k, const void* v, const void* emb, int64_t* ids_out,
+                               cudaStream_t stream) {
+  if (!s) return fail(IS_ERR_INVALID_ARG, "NULL store");
+  if (n <= 0 || !lengths || !k || !v || !emb)
+    return fail(IS_ERR_INVALID_ARG, "n must be > 0 and lengths, k, v, emb non-NULL");
+  if (user < 0 || user >= s->cfg.max_users)
+    return fail(IS_ERR_OUT_OF_RANGE, "user %d outside [0, %d)", user, s->cfg.max_users);
+  int64_t tokens = 0;
+  int32_t max_len = 0;
+  for (int i = 0; i < n; ++i) {
+    if (lengths[i] <= 0) return fail(IS_ERR_INVALID_ARG, "fact %d has length %d", i, lengths[i]);
+    tokens += lengths[i];
+    max_len = std::max(max_len, lengths[i]);
+  }
+  if (s->n_facts + n > s->cfg.max_facts)
+    return fail(IS_ERR_CAPACITY, "store holds %lld of %lld facts; %d more do not fit",
+                (long long)s->n_facts, (long long)s->cfg.max_facts, n);
+  if (s->n_tokens + tokens > s->cfg.max_tokens)
+    return fail(IS_ERR_CAPACITY, "store holds %lld of %lld tokens; %lld more do not fit",
+                (long long)s->n_tokens, (long long)s->cfg.max_tokens, (long long)tokens);
+  if ((int64_t)s->user_nfacts_h[user] + n > s->cfg.max_facts_per_user)
+    return fail(IS_ERR_CAPACITY, "user %d would exceed max_facts_per_user", user);
+
+  // Embedding rows: fill the user's last tile, then fresh tiles.
+  std::vector<int32_t> rows(n);
+  int32_t tiles_used = s->n_tiles;
+  std::vector<int32_t> new_tiles;
+  {
+    int32_t last = s->user_tiles_h[user].empty() ? -1 : s->user_tiles_h[user].back();
+    int32_t fill = last >= 0 ? s->tile_rows_h[last] : kTile;
+    for (int i = 0; i < n; ++i) {
+      if (fill == kTile) {
+        if (tiles_used >= s->max_tiles) return fail(IS_ERR_CAPACITY, "embedding tiles exhausted");
+        last = tiles_used++;
+        new_tiles.push_back(last);
+        fill = 0;
+      }
+      rows[i] = last * kTile + fill++;
+    }
+  }
+  DeviceGuard g(s->device);
+  const int L = s->cfg.num_layers;
+  // K and V into the token-major arena [T][L][2][H][D].
+  uint8_t* dst = s->kv + (size_t)s->n_tokens * s->tok_bytes;
+  CUDA_TRY(cudaMemcpy2DAsync(dst, 2 * s->row_bytes, k, s->row_bytes, s->row_bytes,
+                             (size_t)tokens * L, cudaMemcpyDefault, stream));
+  CUDA_TRY(cudaMemcpy2DAsync(dst + s->row_bytes, 2 * s->row_bytes, v, s->row_bytes, s->row_bytes,
+                             (size_t)tokens * L, cudaMemcpyDefault, stream));
+  // Embeddings, one copy per run of consecutive rows.
+  const size_t erow = (size_t)s->cfg.emb_dim * s->emb_elt;
+  for (int i = 0; i < n;) {
+    int j = i + 1;
+    while (j < n && rows[j] == rows[j - 1] + 1) ++j;
+    CUDA_TRY(cudaMemcpyAsync(s->emb + (size_t)rows[i] * erow, (const uint8_t*)emb + (size_t)i * erow,
+                             (size_t)(j - i) * erow, cudaMemcpyDefault, stream));
+    i = j;
+  }
+  // Per-fact metadata and the row -> fact map.
+  std::vector<int64_t> tok(n);
+  std::vector<int32_t> users(n, user), fids(n);
+  int64_t acc = s->n_tokens;
+  for (int i = 0; i < n; ++i) {
+    tok[i] = acc;
+    acc += lengths[i];
+    fids[i] = (int32_t)(s->n_facts + i);
+  }
+  const int64_t f0 = s->n_facts;
+  CUDA_TRY(cudaMemcpyAsync(s->fact_tok + f0, tok.data(), (size_t)n * 8, cudaMemcpyHostToDevice, stream));
+  CUDA_TRY(cudaMemcpyAsync(s->fact_len + f0, lengths, (size_t)n * 4, cudaMemcpyHostToDevice, stream));
+  CUDA_TRY(cudaMemcpyAsync(s->fact_user + f0, users.data(), (size_t)n * 4, cudaMemcpyHostToDevice, stream));
+  for (int i = 0; i < n;) {
+    int j = i + 1;
+    while (j < n && rows[j] == rows[j - 1] + 1) ++j;
+    CUDA_TRY(cudaMemcpyAsync(s->tile_fact + rows[i], fids.data() + i, (size_t)(j - i) * 4,
+                             cudaMemcpyHostToDevice, stream));
+    i = j;
+  }
+  CUDA_TRY(cudaMemcpyAsync(s->rows_tmp, rows.data(), (size_t)n * 4, cudaMemcpyHostToDevice, stream));
+  CUDA_TRY(launch_emb_norms(s->emb, s->cfg.emb_dtype, s->cfg.emb_dim, s->rows_tmp, n,
+                            s->emb_inv_norm, stream));
+  CUDA_TRY(cudaStreamSynchronize(stream));
+
+  // Commit the host mirror only once every copy succeeded.
+  for (int32_t t : new_tiles) {
+    s->user_tiles_h[user].push_back(t);
+    s->tile_rows_h.push_back(0);
+  }
+  for (int i = 0; i < n; ++i) s->tile_rows_h[rows[i] / kTile] = rows[i] % kTile + 1;
+  s->n_tiles = tiles_used;
+  s->user_nfacts_h[user] += n;
+  s->max_user_tiles = std::max<int32_t>(s->max_user_tiles, (int32_t)s->user_tiles_h[user].size());
+  s->max_user_facts = std::max<int64_t>(s->max_user_facts, s->user_nfacts_h[user]);
+  s->max_len = std::max(s->max_len, max_len);
+  s->n_facts += n;
+  s->n_tokens += tokens;
+  if (ids_out)
+    for (int i = 0; i < n; ++i) ids_out[i] = f0 + i;
+  return upload_user_index(s, stream);
+}
+
+// ---------------------------------------------------------------------------
+
+static is_status_t check_retrieve(is_store_t* s, int32_t Q, const int32_t* users, const void* q_emb,
+                                  int32_t k) {
+  if (!s) return fail(IS_ERR_INVALID_ARG, "NULL store");
+  if (Q < 1 || Q > s->cfg.max_queries)
+    return fail(IS_ERR_INVALID_ARG, "Q=%d outside [1, %d]", Q, s->cfg.max_queries);
+  if (k < 1 || k > s->cfg.max_k) return fail(IS_ERR_OUT_OF_RANGE, "k=%d outside [1, %d]", k, s->cfg.max_k);
+  if (!users || !q_emb) return fail(IS_ERR_INVALID_ARG, "users or q_emb is NULL");
+  if (((uintptr_t)q_emb & 15) != 0) return fail(IS_ERR_INVALID_ARG, "q_emb must be 16-byte aligned");
+  return IS_OK;
+}
+
+static is_status_t run_retrieval(is_store_t* s, int32_t Q, const int32_t* users, const void* q_emb,
+                                 int32_t k, int64_t* ids, float* scores, const int32_t* seg_start,
+                                 int32_t* seg_len, cudaStream_t stream) {
+  const LaunchCfg cfg{stream, s->num_sms, false};
+  SimArgs sa{};
+  sa.emb = s->emb;
+  sa.emb_inv_norm = s->emb_inv_norm;
+  sa.user_nfacts = s->user_nfacts;
+  sa.user_tile_off = s->user_tile_off;
+  sa.user_tiles = s->user_tiles;
+  sa.users = users;
+  sa.q_emb = q_emb;
+  sa.scores = s->scores;
+  sa.score_stride = s->score_stride;
+  sa.status = s->status;
+  sa.Q = Q;
+  sa.E = s->cfg.emb_dim;
+  sa.max_users = s->cfg.max_users;
+  {
+    StageTimer tm(s, IS_STAGE_SIMILARITY, stream);
+    CUDA_TRY(launch_similarity(sa, s->cfg.emb_dtype, s->max_user_tiles, cfg));
+  }
+  TopkArgs ta{};
+  ta.scores = s->scores;
+  ta.score_stride = s->score_stride;
+  ta.users = users;
+  ta.user_nfacts = s->user_nfacts;
+  ta.user_tile_off = s->user_tile_off;
+  ta.user_tiles = s->user_tiles;
+  ta.tile_fact = s->tile_fact;
+  ta.fact_len = s->fact_len;
+  ta.seg_start = seg_start;
+  ta.ids_out = ids;
+  ta.scores_out = scores;
+  ta.n_ids_out = seg_start ? s->n_ids : nullptr;
+  ta.fact_seg_off = seg_start ? s->fact_seg_off : nullptr;
+  ta.seg_stride = s->seg_stride;
+  ta.seg_len = seg_start ? seg_len : nullptr;
+  ta.status = s->status;
+  ta.Q = Q;
+  ta.k = k;
+  ta.max_users = s->cfg.max_users;
+  {
+    StageTimer tm(s, IS_STAGE_TOPK, stream);
+    CUDA_TRY(launch_topk(ta, cfg));
+  }
+  return IS_OK;
+}
+
+is_status_t is_retrieve_topk(is_store_t* s, int32_t Q, const int32_t* users, const void* q_emb,
+                             int32_t k, int64_t* ids_out, float* scores_out, cudaStream_t stream) {
+  is_status_t st = check_retrieve(s, Q, users, q_emb, k);
+  if (st != IS_OK) return st;
+  if (!ids_out || !scores_out) return fail(IS_ERR_INVALID_ARG, "ids_out or scores_out is NULL");
+  DeviceGuard g(s->device);
+  return run_retrieval(s, Q, users, q_emb, k, ids_out, scores_out, nullptr, nullptr, stream);
+}
+
+static is_status_t check_inject_common(is_store_t* s, int32_t R, const int32_t* seg_start,
+                                       const is_rope_params_t* rope, const int32_t* block_table,
+                                       int32_t max_blocks, const is_cache_desc_t* cache,
+                                       void* kv_cache, int32_t facts_per_request) {
+  if (!seg_start || !block_table) return fail(IS_ERR_INVALID_ARG, "seg_start or block_table is NULL");
+  if (max_blocks < 1) return fail(IS_ERR_INVALID_ARG, "max_blocks_per_seq must be >= 1");
+  is_status_t st = check_cache(s, cache, kv_cache);
+  if (st != IS_OK) return st;
+  st = check_rope(rope, s->cfg.head_dim, s->cfg.kv_dtype);
+  if (st != IS_OK) return st;
+  const int64_t bound = (int64_t)R * facts_per_request * std::max(1, s->max_len);
+  if (bound >= (int64_t)INT32_MAX)
+    return fail(IS_ERR_UNSUPPORTED, "a call may inject up to %lld tokens; the limit is 2^31-1",
+                (long long)bound);
+  return IS_OK;
+}
+
+static is_status_t launch_injection(is_store_t* s, int32_t R, const int64_t* ids, int32_t ids_stride,
+                                    const int32_t* seg_len, const int32_t* seg_start,
+                                    const is_rope_params_t* rope, const int32_t* block_table,
+                                    int32_t max_blocks, const is_cache_desc_t* cache, void* kv_cache,
+                                    int64_t* slot_mapping, cudaStream_t stream) {
+  InjectArgs a{};
+  a.kv = s->kv;
+  a.fact_tok = s->fact_tok;
+  a.fact_len = s->fact_len;
+  a.fact_user = s->fact_user;
+  a.n_facts = s->n_facts;
+  a.ids = ids;
+  a.ids_stride = ids_stride;
+  a.n_ids = s->n_ids;
+  a.fact_seg_off = s->fact_seg_off;
+  a.seg_stride = s->seg_stride;
+  a.seg_len = seg_len;
+  a.seg_start = seg_start;
+  a.block_table = block_table;
+  a.max_blocks = max_blocks;
+  a.cache = static_cast<uint8_t*>(kv_cache);
+  a.block_size = cache->block_size;
+  a.num_blocks = cache->num_blocks;
+  a.slot_mapping = slot_mapping;
+  a.status = s->status;
+  a.R = R;
+  a.L = s->cfg.num_layers;
+  a.row_bytes = (int32_t)s->row_bytes;
+  const int ve = 16 / s->elt;
+  a.half_vecs = s->cfg.head_dim / 2 / ve;
+  a.head_vecs = s->cfg.head_dim / ve;
+  const RopeTurns rt = make_turns(*rope, s->cfg.head_dim);
+  const LaunchCfg cfg{stream, s->num_sms, false};
+  const int grid = s->num_sms * std::max(1, s->inject_ctas);
+  StageTimer tm(s, IS_STAGE_INJECT, stream);
+  CUDA_TRY(launch_inject(a, rt, s->cfg.kv_dtype, rope->style, grid, cfg));
+  return IS_OK;
+}
+
+is_status_t is_inject(is_store_t* s, int32_t R, const int64_t* fact_ids, const int32_t* n_ids,
+                      int32_t ids_stride, const int32_t* users, const int32_t* seg_start,
+                      const is_rope_params_t* rope, const int32_t* block_table, int32_t max_blocks,
+                      const is_cache_desc_t* cache, void* kv_cache, int32_t* seg_len_out,
+                      int64_t* slot_mapping_out, cudaStream_t stream) {
+  if (!s) return fail(IS_ERR_INVALID_ARG, "NULL store");
+  if (R < 1 || R > s->cfg.max_requests)
+    return fail(IS_ERR_INVALID_ARG, "R=%d outside [1, %d]", R, s->cfg.max_requests);
+  if (ids_stride < 1 || ids_stride > s->cfg.max_k)
+    return fail(IS_ERR_OUT_OF_RANGE, "ids_stride=%d outside [1, %d]", ids_stride, s->cfg.max_k);
+  if (!fact_ids || !n_ids) return fail(IS_ERR_INVALID_ARG, "fact_ids or n_ids is NULL");
+  is_status_t st = check_inject_common(s, R, seg_start, rope, block_table, max_blocks, cache, kv_cache,
+                                       ids_stride);
+  if (st != IS_OK) return st;
+  DeviceGuard g(s->device);
+  int32_t* seg_len = seg_len_out ? seg_len_out : s->seg_len_tmp;
+  PlanArgs p{};
+  p.ids = fact_ids;
+  p.ids_stride = ids_stride;
+  p.n_ids_in = n_ids;
+  p.users = users;
+  p.seg_start = seg_start;
+  p.fact_len = s->fact_len;
+  p.fact_user = s->fact_user;
+  p.n_facts = s->n_facts;
+  p.n_ids_out = s->n_ids;
+  p.fact_seg_off = s->fact_seg_off;
+  p.seg_stride = s->seg_stride;
+  p.seg_len = seg_len;
+  p.status = s->status;
+  p.R = R;
+  {
+    StageTimer tm(s, IS_STAGE_PLAN, stream);
+    CUDA_TRY(launch_plan(p, LaunchCfg{stream, s->num_sms, false}));
+  }
+  return launch_injection(s, R, fact_ids, ids_stride, seg_len, seg_start, rope, block_table, max_blocks,
+                          cache, kv_cache, slot_mapping_out, stream);
+}
+
+is_status_t is_retrieve_and_inject(is_store_t* s, int32_t Q, const int32_t* users, const void* q_emb,
+                                   int32_t k, const int32_t* seg_start, const is_rope_params_t* rope,
+                                   const int32_t* block_table, int32_t max_blocks,
+                                   const is_cache_desc_t* cache, void* kv_cache, int64_t* ids_out,
+                                   float* scores_out, int32_t* seg_len_out, int64_t* slot_mapping_out,
+                                   cudaStream_t stream) {
+  is_status_t st = check_retrieve(s, Q, users, q_emb, k);
+  if (st != IS_OK) return st;
+  if (Q > s->cfg.max_requests && Q > s->cfg.max_queries)
+    return fail(IS_ERR_INVALID_ARG, "Q exceeds the store's request capacity");
+  st = check_inject_common(s, Q, seg_start, rope, block_table, max_blocks, cache, kv_cache, k);
+  if (st != IS_OK) return st;
+  DeviceGuard g(s->device);
+  int64_t* ids = ids_out ? ids_out : s->ids_tmp;
+  float* scores = scores_out ? scores_out : s->scores_tmp;
+  int32_t* seg_len = seg_len_out ? seg_len_out : s->seg_len_tmp;
+  st = run_retrieval(s, Q, users, q_emb, k, ids, scores, seg_start, seg_len, stream);
+  if (st != IS_OK) return st;
+  return launch_injection(s, Q, ids, k, seg_len, seg_start, rope, block_table, max_blocks, cache,
+                          kv_cache, slot_mapping_out, stream);
+}
+
+is_status_t is_get_status(is_store_t* s, cudaStream_t stream, uint32_t* bits_out) {
+  if (!s || !bits_out) return fail(IS_ERR_INVALID_ARG, "NULL argument");
+  DeviceGuard g(s->device);
+  uint32_t bits = 0;
+  CUDA_TRY(cudaMemcpyAsync(&bits, s->status, 4, cudaMemcpyDeviceToHost, stream));
+  CUDA_TRY(cudaMemsetAsync(s->status, 0, 4, stream));
+  CUDA_TRY(cudaStreamSynchronize(stream));
+  *bits_out = bits;
+  if (bits & IS_ST_TIMEOUT) return fail(IS_ERR_TIMEOUT, "a device wait timed out (bits 0x%x)", bits);
+  if (bits) return fail(IS_ERR_DEVICE, "device status bits 0x%x", bits);
+  return IS_OK;
+}
+
+is_status_t is_set_timing(is_store_t* s, int32_t enable) {
+  if (!s) return fail(IS_ERR_INVALID_ARG, "NULL store");
+  s->timing = enable != 0;
+  return IS_OK;
+}
+
+static is_status_t collect_timing(is_store_t* s) {
+  for (int st = 0; st < IS_NUM_STAGES; ++st) {
+    for (auto& ev : s->pending[st]) {
+      CUDA_TRY(cudaEventSynchronize(ev.b));
+      float ms = 0.f;
+      CUDA_TRY(cudaEventElapsedTime(&ms, ev.a, ev.b));
+      s->total_ms[st] += ms;
+      s->launches[st] += 1;
+      s->event_pool.push_back(ev.a);
+      s->event_pool.push_back(ev.b);
+    }
+    s->pending[st].clear();
+  }
+  return IS_OK;
+}
+
+is_status_t is_get_timing(is_store_t* s, int32_t stage, double* total_ms, int64_t* launches) {
+  if (!s || !total_ms || !launches) return fail(IS_ERR_INVALID_ARG, "NULL argument");
+  if (stage < 0 || stage >= IS_NUM_STAGES) return fail(IS_ERR_INVALID_ARG, "bad stage %d", stage);
+  DeviceGuard g(s->device);
+  is_status_t st = collect_timing(s);
+  if (st != IS_OK) return st;
+  *total_ms = s->total_ms[stage];
+  *launches = s->launches[stage];
+  return IS_OK;
+}
+
+is_status_t is_reset_timing(is_store_t* s) {
+  if (!s) return fail(IS_ERR_INVALID_ARG, "NULL store");
+  DeviceGuard g(s->device);
+  is_status_t st = collect_timing(s);
+  for (int i = 0; i < IS_NUM_STAGES; ++i) {
+    s->total_ms[i] = 0;
+    s->launches[i] = 0;
+  }
+  return st;
+}
+
+}  // extern "C"

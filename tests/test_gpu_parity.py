@@ -1,0 +1,221 @@
+"""Parity of the CUDA path (through the C ABI) with the fp64 oracle, small cases.
+
+Sizes here finish on the oracle in seconds yet span several warps' work
+items, several embedding tiles, ragged fact lists and partial cache blocks.
+"""
+import numpy as np
+import pytest
+
+from oracle import inject as oinject
+from synth import kvgen, staging, workloads
+from tests import gpu_helpers as gh
+from tests import parity
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def api():
+    gh.ensure_built()
+    from kv_cache_injection_gb300 import api as a
+    return a
+
+
+@pytest.fixture(scope="module")
+def tiny(api):
+    wl = workloads.get("tiny")
+    store = staging.load_store(wl, api)
+    yield wl, store
+    store.destroy()
+
+
+def _full_compare(wl, cache, ids_rows, seg_len, slot_map, style):
+    plans, lens = parity.oracle_plans(wl, ids_rows)
+    assert np.array_equal(seg_len, lens)
+    want_slots = np.concatenate([[e[3] for e in pl] for pl in plans]).astype(np.int64)
+    assert np.array_equal(slot_map[: len(want_slots)], want_slots)
+    facts = parity.FactCache(wl)
+    freqs = parity.oracle_freqs(wl)
+    entries = [e for pl in plans for e in pl]
+    gk, gv = gh.gather_rows(cache, [e[3] for e in entries])
+    stats = parity.compare_tokens(wl, gk, gv, entries, freqs, style, facts)
+    gh.assert_only_slots_changed(cache, wl.spec.kv_dtype, want_slots)
+    return stats
+
+
+def test_device_generator_matches_host(api):
+    import torch
+    for dtype in ("f32", "bf16", "f16"):
+        for first, n in [(0, 1000), (123456789, 4097), (2 ** 34 + 5, 333)]:
+            t = torch.empty(n, dtype=staging.torch_dtype(dtype), device="cuda")
+            staging.fill_kv(t, dtype, 9, 1, first)
+            host = kvgen.kv_elements(9, 1, first, n, dtype)
+            dev = staging.cache_bits(t)
+            assert np.array_equal(dev.view(np.uint8), host.view(np.uint8)), dtype
+
+
+@pytest.mark.parametrize("style", [0, 1])
+def test_tiny_fused_full_cache(api, tiny, style):
+    wl, store = tiny
+    inp = staging.device_inputs(wl)
+    cache = staging.canary_cache(wl)
+    out = gh.run_fused(api, store, wl, inp, cache, style=style)
+    assert out["status"] == 0
+    o_ids, o_sc, score_of = parity.oracle_retrieve(wl, 0, wl.spec.k)
+    parity.check_topk(out["ids"][0], out["scores"][0], o_ids, o_sc, score_of, wl.spec.k)
+    _full_compare(wl, cache, out["ids"], out["seg_len"], out["slot_map"], style)
+
+
+def test_tiny_topk_then_inject_equals_fused(api, tiny):
+    import torch
+    wl, store = tiny
+    inp = staging.device_inputs(wl)
+    k = wl.spec.k
+    ids = torch.empty((1, k), dtype=torch.int64, device="cuda")
+    sc = torch.empty((1, k), dtype=torch.float32, device="cuda")
+    api.is_retrieve_topk(store, inp["users"], inp["q_emb"], k, ids, sc)
+    n_ids = (ids >= 0).sum(1).to(torch.int32)
+    cache_a = staging.canary_cache(wl)
+    rope = staging.rope_params(wl, api)
+    cdesc = api.make_cache_desc(wl.spec.block_size, wl.num_blocks, wl.spec.kv_dtype)
+    seg_len = torch.empty(1, dtype=torch.int32, device="cuda")
+    api.is_inject(store, ids, n_ids, inp["seg_start"], rope, inp["block_table"], cdesc, cache_a,
+                  users=inp["users"], seg_len_out=seg_len)
+    assert api.is_get_status(store) == 0
+    cache_b = staging.canary_cache(wl)
+    out = gh.run_fused(api, store, wl, inp, cache_b)
+    assert np.array_equal(out["ids"], ids.cpu().numpy())
+    assert torch.equal(cache_a.view(torch.int32), cache_b.view(torch.int32))
+    assert int(seg_len.item()) == int(out["seg_len"][0])
+
+
+SMALL_BF16 = workloads.WorkloadSpec(
+    name="small_bf16", num_layers=3, num_kv_heads=4, head_dim=64, kv_dtype="bf16",
+    rope=workloads.RopeSpec(theta=1.0e4), n_users=5, facts_per_user=300,
+    length_dist=("uniform", 1, 21), emb_dim=128, emb_dtype="f16", n_queries=5, k=9,
+    query_kind="planted", start=("uniform", 0, 700), block_size=16, tokens_cap=9 * 21,
+    block_layout="free_list", seed=11)
+
+
+@pytest.mark.parametrize("dtype,style,scaled", [("bf16", 0, False), ("bf16", 1, False),
+                                                ("f16", 0, True), ("f32", 0, False),
+                                                ("f32", 1, True)])
+def test_small_multi_user_fused(api, dtype, style, scaled):
+    spec = SMALL_BF16.with_(kv_dtype=dtype, num_kv_heads=8 if dtype == "f32" else 4,
+                            rope=workloads.RopeSpec(theta=5e5, style=style, scaling=1, factor=8.0,
+                                                    low_freq_factor=1.0, high_freq_factor=4.0,
+                                                    original_max_pos=64)
+                            if scaled else workloads.RopeSpec(theta=1e4, style=style))
+    wl = workloads.generate(spec)
+    store = staging.load_store(wl, api)
+    try:
+        inp = staging.device_inputs(wl)
+        cache = staging.canary_cache(wl)
+        out = gh.run_fused(api, store, wl, inp, cache)
+        assert out["status"] == 0
+        for q in range(spec.n_queries):
+            o_ids, o_sc, score_of = parity.oracle_retrieve(wl, q, spec.k)
+            parity.check_topk(out["ids"][q], out["scores"][q], o_ids, o_sc, score_of, spec.k)
+        _full_compare(wl, cache, out["ids"], out["seg_len"], out["slot_map"], style)
+    finally:
+        store.destroy()
+
+
+def test_ragged_explicit_lists(api):
+    """is_inject with ragged per-request fact lists (including an empty one),
+    requests of different users, facts in arbitrary order."""
+    import torch
+    wl = workloads.generate(SMALL_BF16.with_(n_queries=5, seed=12))
+    store = staging.load_store(wl, api)
+    try:
+        rng = np.random.default_rng(0)
+        R, stride = 5, 9
+        n_ids = np.array([9, 0, 1, 5, 7], dtype=np.int32)
+        ids = np.full((R, stride), -5, dtype=np.int64)
+        for r in range(R):
+            facts = wl.user_facts(int(wl.users[r]))
+            ids[r, :n_ids[r]] = rng.choice(facts, size=n_ids[r], replace=False)
+        inp = staging.device_inputs(wl)
+        cache = staging.canary_cache(wl)
+        seg_len = torch.empty(R, dtype=torch.int32, device="cuda")
+        slot_map = torch.full((int(R * stride * 21),), -9, dtype=torch.int64, device="cuda")
+        rope = staging.rope_params(wl, api)
+        cdesc = api.make_cache_desc(16, wl.num_blocks, "bf16")
+        api.is_inject(store, torch.from_numpy(ids).cuda(), torch.from_numpy(n_ids).cuda(),
+                      inp["seg_start"], rope, inp["block_table"], cdesc, cache, users=inp["users"],
+                      seg_len_out=seg_len, slot_mapping_out=slot_map)
+        assert api.is_get_status(store) == 0
+        rows = [ids[r, :n_ids[r]] for r in range(R)]
+        _full_compare(wl, cache, rows, seg_len.cpu().numpy(), slot_map.cpu().numpy(), 0)
+    finally:
+        store.destroy()
+
+
+def test_ties_go_to_lower_fact_id(api):
+    """Exactly tied scores (duplicated embeddings): lower fact ids win, including
+    across the k-th boundary, and k up to the hard limit."""
+    import torch
+    spec = SMALL_BF16.with_(n_users=1, facts_per_user=1500, n_queries=3, k=1024, seed=13,
+                            tokens_cap=1024 * 21, length_dist=("uniform", 1, 3))
+    wl = workloads.generate(spec)
+    base = wl.emb[:50].copy()
+    wl.emb[:] = base[np.arange(1500) % 50]            # every embedding appears 30 times
+    wl.queries[:] = base[[3, 17, 42]]
+    store = staging.load_store(wl, api)
+    try:
+        inp = staging.device_inputs(wl)
+        for k in (1, 29, 30, 31, 1024):
+            ids = torch.empty((3, k), dtype=torch.int64, device="cuda")
+            sc = torch.empty((3, k), dtype=torch.float32, device="cuda")
+            api.is_retrieve_topk(store, inp["users"], inp["q_emb"], k, ids, sc)
+            g = ids.cpu().numpy()
+            for q in range(3):
+                o_ids, o_sc, score_of = parity.oracle_retrieve(wl, q, k)
+                # every fact shares its score with 29 others: check the exact tie-break
+                head = g[q][: min(k, 30)]
+                assert np.array_equal(head, o_ids[: min(k, 30)]), (k, q)
+                parity.check_topk(g[q], sc.cpu().numpy()[q], o_ids, o_sc, score_of, k)
+        assert api.is_get_status(store) == 0
+    finally:
+        store.destroy()
+
+
+def test_user_with_fewer_than_k_facts(api):
+    import torch
+    spec = SMALL_BF16.with_(n_users=2, facts_per_user=6, n_queries=2, k=9, seed=14)
+    wl = workloads.generate(spec)
+    store = staging.load_store(wl, api)
+    try:
+        inp = staging.device_inputs(wl)
+        cache = staging.canary_cache(wl)
+        out = gh.run_fused(api, store, wl, inp, cache)
+        assert out["status"] == 0
+        for q in range(2):
+            o_ids, o_sc, score_of = parity.oracle_retrieve(wl, q, 9)
+            assert len(o_ids) == 6
+            parity.check_topk(out["ids"][q], out["scores"][q], o_ids, o_sc, score_of, 9)
+        _full_compare(wl, cache, out["ids"], out["seg_len"], out["slot_map"], 0)
+    finally:
+        store.destroy()
+
+
+def test_repeat_is_bit_identical(api, tiny):
+    import torch
+    wl, store = tiny
+    inp = staging.device_inputs(wl)
+    a = staging.canary_cache(wl)
+    b = staging.canary_cache(wl)
+    gh.run_fused(api, store, wl, inp, a)
+    gh.run_fused(api, store, wl, inp, b)
+    assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+
+
+def test_rope_frequencies_match_oracle(api):
+    from oracle import rope
+    r = workloads.LLAMA31_ROPE
+    p = api.make_rope(r.theta, 0, 1, r.factor, r.low_freq_factor, r.high_freq_factor,
+                      r.original_max_pos)
+    got = api.is_rope_frequencies(p, 128)
+    want = rope.inv_freq(128, r.theta, 1, r.factor, r.low_freq_factor, r.high_freq_factor,
+                         r.original_max_pos)
+    assert np.allclose(got, want, rtol=1e-14, atol=0)
