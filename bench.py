@@ -115,7 +115,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except (FileNotFoundError, OSError):
             self.proc = None
@@ -190,6 +190,8 @@ def run_ours(args, rank, world, local_rank):
                                    inp["block_table"], cdesc, cache, ids, scores, seg_len, None,
                                    stream=stream)
 
+    # The clock sampler runs from the warm-up through the end of the timed region.
+    clocks = ClockSampler(local_rank).__enter__()
     for _ in range(args.warmup):
         flush.zero_()
         step()
@@ -206,13 +208,13 @@ def run_ours(args, rank, world, local_rank):
     api.is_set_timing(store, True)
     barrier()
     torch.cuda.synchronize()
-    with ClockSampler(local_rank) as clocks:
-        for i in range(args.steps):
-            flush.zero_()
-            starts[i].record(stream)
-            step()
-            ends[i].record(stream)
-        torch.cuda.synchronize()
+    for i in range(args.steps):
+        flush.zero_()
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    clocks.__exit__(None, None, None)
     barrier()
     api.is_set_timing(store, False)
     step_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
@@ -440,8 +442,8 @@ def run_reference(args, rank, world):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="llama31_8b")
     ap.add_argument("--k", type=int, default=0)
