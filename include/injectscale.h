@@ -224,6 +224,42 @@ is_status_t is_retrieve_and_inject(is_store_t* store, int32_t Q, const int32_t* 
                                    int32_t* seg_len_out, int64_t* slot_mapping_out,
                                    cudaStream_t stream);
 
+/* ---- is_inject_noalloc ------------------------------------------------------
+ * The paper has no counterpart to this call; it exists for callers that
+ * cannot allocate device memory: code whose device memory is all owned by
+ * another allocator (a serving engine that reserves HBM for its own pools at
+ * start-up) or that runs where cudaMalloc is not allowed.  Such a caller
+ * keeps facts in its own buffers and still wants the gather + Chunked RoPE +
+ * paged scatter.  This call creates no store and allocates nothing: the
+ * per-request segment plan lives in a static device array of the library
+ * (about 265 KB, held on every device that loads the library until exit).
+ *   kv_arena             device, token-major [tokens][L][2][H][D] in kv_dtype
+ *                        (per token and layer: K row then V row, K before RoPE)
+ *   fact_tok, fact_len   device int64[n_facts] first arena token, int32[n_facts]
+ *                        length (each in [1, max_fact_len])
+ *   R                    1 <= R <= IS_NOALLOC_MAX_REQUESTS
+ *   ids_stride           1 <= ids_stride <= IS_NOALLOC_MAX_FACTS
+ *   status_out           device uint32, caller-owned: IS_ST_* bits are OR-ed in
+ *                        (the caller clears it)
+ * Other arguments as in is_inject (no user check).  Sizes beyond the limits
+ * return IS_ERR_UNSUPPORTED before anything is enqueued.  The first call on a
+ * device looks up the static array's device address (once per device, under
+ * a lock); make that first call before any stream capture.  Every call uses
+ * the same static array and overwrites the entries it reads, so nothing has
+ * to start at zero, but two calls whose kernels overlap on the GPU (different
+ * streams, no ordering between them) race on it. */
+#define IS_NOALLOC_MAX_REQUESTS 256
+#define IS_NOALLOC_MAX_FACTS    256
+is_status_t is_inject_noalloc(const void* kv_arena, const int64_t* fact_tok,
+                              const int32_t* fact_len, int64_t n_facts, int32_t max_fact_len,
+                              int32_t num_layers, int32_t num_kv_heads, int32_t head_dim,
+                              int32_t kv_dtype, int32_t R, const int64_t* fact_ids,
+                              const int32_t* n_ids, int32_t ids_stride, const int32_t* seg_start,
+                              const is_rope_params_t* rope, const int32_t* block_table,
+                              int32_t max_blocks_per_seq, const is_cache_desc_t* cache,
+                              void* kv_cache, int32_t* seg_len_out, int64_t* slot_mapping_out,
+                              uint32_t* status_out, cudaStream_t stream);
+
 /* ---- status / diagnostics ---------------------------------------------------
  * is_get_status: synchronise `stream`, read the device status word into
  * *bits_out and clear it.  Returns IS_ERR_DEVICE if any bit was set,

@@ -17,6 +17,7 @@ IS_ST_FACT_RANGE, IS_ST_FACT_USER, IS_ST_BLOCK_TABLE, IS_ST_BLOCK_ID = 0x01, 0x0
 IS_ST_USER_RANGE, IS_ST_POSITION, IS_ST_COUNT, IS_ST_TIMEOUT = 0x10, 0x20, 0x40, 0x80
 IS_STAGE_SIMILARITY, IS_STAGE_TOPK, IS_STAGE_PLAN, IS_STAGE_INJECT = 0, 1, 2, 3
 IS_MAX_K, IS_MAX_QUERIES, IS_MAX_REQUESTS, IS_EMB_TILE = 1024, 1024, 4096, 128
+IS_NOALLOC_MAX_REQUESTS, IS_NOALLOC_MAX_FACTS = 256, 256
 
 
 class StoreConfig(ctypes.Structure):
@@ -58,6 +59,10 @@ SIGNATURES = {
     "is_retrieve_and_inject": [c_void_p, c_int32, c_void_p, c_void_p, c_int32, c_void_p,
                                POINTER(RopeParams), c_void_p, c_int32, POINTER(CacheDesc),
                                c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p],
+    "is_inject_noalloc": [c_void_p, c_void_p, c_void_p, c_int64, c_int32, c_int32, c_int32,
+                          c_int32, c_int32, c_int32, c_void_p, c_void_p, c_int32, c_void_p,
+                          POINTER(RopeParams), c_void_p, c_int32, POINTER(CacheDesc), c_void_p,
+                          c_void_p, c_void_p, c_void_p, c_void_p],
     "is_get_status": [c_void_p, c_void_p, POINTER(c_uint32)],
     "is_last_error_message": [],
     "is_status_string": [c_int],

@@ -6,6 +6,10 @@
 // scatter-copied into vLLM's paged KV cache.  One pass over the data: each
 // (token, layer) row pair is read once from the store and written once to the
 // cache, the rotation done in registers on the way.
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
 #include "block_scan.cuh"
 #include "common.cuh"
 #include "internal.h"
@@ -292,3 +296,162 @@ int inject_ctas_per_sm(int kv_dtype, int style, int vpl) {
 }
 
 }  // namespace isk
+
+// ---------------------------------------------------------------------------
+// Allocation-free injection (is_inject_noalloc).
+//
+// For callers that cannot allocate device memory, the segment plan that
+// is_inject keeps in store-owned scratch lives here in one file-scope device
+// array of fixed size.  The host never dereferences the array's name: it
+// looks up the device address once per device and passes that to the kernels.
+
+namespace {
+
+constexpr int kNaRequests = IS_NOALLOC_MAX_REQUESTS;
+constexpr int kNaSegStride = IS_NOALLOC_MAX_FACTS + 1;
+constexpr size_t kNaWords = (size_t)kNaRequests * kNaSegStride + 2 * kNaRequests;
+constexpr int kNaMaxDevices = 64;
+
+// [0, R*stride): per-request prefix of fact lengths; then n_ids[R]; then seg_len[R].
+static __device__ __align__(256) int32_t g_noalloc_scratch[kNaWords];
+
+struct NoAllocDevice {
+  bool ready = false;
+  int32_t* scratch = nullptr;   // device address of g_noalloc_scratch on this device
+  int num_sms = 0;
+  int ctas[3][2][3] = {};       // [dtype][style][vpl class], 0 = not yet queried
+};
+NoAllocDevice g_na_dev[kNaMaxDevices];
+std::mutex g_na_mu;
+
+is_status_t na_fail(is_status_t st, const char* msg) {
+  isk::set_last_error_message(msg);
+  return st;
+}
+
+}  // namespace
+
+extern "C" is_status_t is_inject_noalloc(
+    const void* kv_arena, const int64_t* fact_tok, const int32_t* fact_len, int64_t n_facts,
+    int32_t max_fact_len, int32_t num_layers, int32_t num_kv_heads, int32_t head_dim,
+    int32_t kv_dtype, int32_t R, const int64_t* fact_ids, const int32_t* n_ids, int32_t ids_stride,
+    const int32_t* seg_start, const is_rope_params_t* rope, const int32_t* block_table,
+    int32_t max_blocks_per_seq, const is_cache_desc_t* cache, void* kv_cache, int32_t* seg_len_out,
+    int64_t* slot_mapping_out, uint32_t* status_out, cudaStream_t stream) {
+  using namespace isk;
+  if (!kv_arena || !fact_tok || !fact_len || !fact_ids || !n_ids || !seg_start || !rope ||
+      !block_table || !cache || !kv_cache || !status_out)
+    return na_fail(IS_ERR_INVALID_ARG, "a required pointer is NULL");
+  if (R < 1 || R > kNaRequests)
+    return na_fail(IS_ERR_UNSUPPORTED, "R must be in [1, IS_NOALLOC_MAX_REQUESTS]");
+  if (ids_stride < 1 || ids_stride > IS_NOALLOC_MAX_FACTS)
+    return na_fail(IS_ERR_UNSUPPORTED, "ids_stride must be in [1, IS_NOALLOC_MAX_FACTS]");
+  if (n_facts < 1 || max_fact_len < 1 || max_blocks_per_seq < 1)
+    return na_fail(IS_ERR_INVALID_ARG, "n_facts, max_fact_len, max_blocks_per_seq must be >= 1");
+  if ((int64_t)R * ids_stride * max_fact_len >= (int64_t)INT32_MAX)
+    return na_fail(IS_ERR_UNSUPPORTED, "R * ids_stride * max_fact_len must stay below 2^31");
+  if (kv_dtype != IS_F32 && kv_dtype != IS_BF16 && kv_dtype != IS_F16)
+    return na_fail(IS_ERR_INVALID_ARG, "bad kv_dtype");
+  if (num_layers < 1 || num_kv_heads < 1 || head_dim < 16 || head_dim > IS_MAX_HEAD_DIM ||
+      (head_dim & (head_dim - 1)) != 0)
+    return na_fail(IS_ERR_UNSUPPORTED, "head_dim must be a power of two in [16, IS_MAX_HEAD_DIM]");
+  const int elt = kv_dtype == IS_F32 ? 4 : 2;
+  const int64_t row_bytes = (int64_t)num_kv_heads * head_dim * elt;
+  if (row_bytes % 512 != 0)
+    return na_fail(IS_ERR_UNSUPPORTED, "num_kv_heads * head_dim * elt must be a multiple of 512");
+  if (cache->block_size < 1 || cache->num_blocks < 1 || cache->dtype != kv_dtype)
+    return na_fail(IS_ERR_INVALID_ARG, "bad cache descriptor");
+  if ((((uintptr_t)kv_cache) | ((uintptr_t)kv_arena)) & 15)
+    return na_fail(IS_ERR_INVALID_ARG, "kv_cache and kv_arena must be 16-byte aligned");
+  double w[kMaxHalfDim];
+  if (is_rope_frequencies(rope, head_dim, w) != IS_OK)
+    return na_fail(IS_ERR_INVALID_ARG, "bad rope parameters");
+  const int ve = 16 / elt;
+  const int vecs = rope->style == 0 ? head_dim / 2 / ve : head_dim / ve;
+  if (vecs < 1 || vecs > 32)
+    return na_fail(IS_ERR_UNSUPPORTED, "head_dim not supported for this dtype and rope style");
+
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNaMaxDevices)
+    return na_fail(IS_ERR_CUDA, "cudaGetDevice failed");
+  const int vpl = (int)(row_bytes >> 9);
+  const int vclass = vpl % 4 == 0 ? 0 : (vpl % 2 == 0 ? 1 : 2);
+  NoAllocDevice& d = g_na_dev[dev];
+  {
+    std::lock_guard<std::mutex> lock(g_na_mu);
+    if (!d.ready) {
+      void* ptr = nullptr;
+      cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+      if (e != cudaSuccess || ptr == nullptr) {
+        cudaGetLastError();
+        return na_fail(IS_ERR_CUDA, "cudaGetSymbolAddress of the static scratch failed");
+      }
+      if (cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return na_fail(IS_ERR_CUDA, "cudaDeviceGetAttribute failed");
+      d.scratch = static_cast<int32_t*>(ptr);
+      d.ready = true;
+    }
+    if (d.ctas[kv_dtype][rope->style][vclass] == 0)
+      d.ctas[kv_dtype][rope->style][vclass] = inject_ctas_per_sm(kv_dtype, rope->style, vpl);
+  }
+  int32_t* seg_off = d.scratch;
+  int32_t* na_n_ids = d.scratch + (size_t)kNaRequests * kNaSegStride;
+  int32_t* seg_len = seg_len_out ? seg_len_out : na_n_ids + kNaRequests;
+
+  PlanArgs p{};
+  p.ids = fact_ids;
+  p.ids_stride = ids_stride;
+  p.n_ids_in = n_ids;
+  p.users = nullptr;
+  p.seg_start = seg_start;
+  p.fact_len = fact_len;
+  p.fact_user = nullptr;
+  p.n_facts = n_facts;
+  p.n_ids_out = na_n_ids;
+  p.fact_seg_off = seg_off;
+  p.seg_stride = kNaSegStride;
+  p.seg_len = seg_len;
+  p.status = status_out;
+  p.R = R;
+  const LaunchCfg cfg{stream, d.num_sms, false};
+  if (launch_plan(p, cfg) != cudaSuccess) return na_fail(IS_ERR_CUDA, "plan launch failed");
+
+  InjectArgs a{};
+  a.kv = static_cast<const uint8_t*>(kv_arena);
+  a.fact_tok = fact_tok;
+  a.fact_len = fact_len;
+  a.fact_user = nullptr;
+  a.n_facts = n_facts;
+  a.ids = fact_ids;
+  a.ids_stride = ids_stride;
+  a.n_ids = na_n_ids;
+  a.fact_seg_off = seg_off;
+  a.seg_stride = kNaSegStride;
+  a.seg_len = seg_len;
+  a.seg_start = seg_start;
+  a.block_table = block_table;
+  a.max_blocks = max_blocks_per_seq;
+  a.cache = static_cast<uint8_t*>(kv_cache);
+  a.block_size = cache->block_size;
+  a.num_blocks = cache->num_blocks;
+  a.slot_mapping = slot_mapping_out;
+  a.status = status_out;
+  a.R = R;
+  a.L = num_layers;
+  a.row_bytes = (int32_t)row_bytes;
+  a.half_vecs = head_dim / 2 / ve;
+  a.head_vecs = head_dim / ve;
+  RopeTurns rt;
+  memset(&rt, 0, sizeof rt);
+  const double two_pi = 6.283185307179586476925286766559;
+  for (int i = 0; i < head_dim / 2; ++i) {
+    const double turns = w[i] / two_pi;
+    rt.hi[i] = (float)turns;
+    rt.lo[i] = (float)(turns - (double)rt.hi[i]);
+  }
+  const int grid = d.num_sms * (d.ctas[kv_dtype][rope->style][vclass] > 0
+                                    ? d.ctas[kv_dtype][rope->style][vclass] : 1);
+  if (launch_inject(a, rt, kv_dtype, rope->style, grid, cfg) != cudaSuccess)
+    return na_fail(IS_ERR_CUDA, "inject launch failed");
+  return IS_OK;
+}

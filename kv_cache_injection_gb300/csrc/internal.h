@@ -27,6 +27,9 @@ cudaError_t launch_plan(const PlanArgs& a, const LaunchCfg& cfg);
 cudaError_t launch_inject(const InjectArgs& a, const RopeTurns& turns, int kv_dtype, int style,
                           int grid_ctas, const LaunchCfg& cfg);
 
+// Sets the message is_last_error_message() returns on this thread.
+void set_last_error_message(const char* msg);
+
 // CTAs per SM the inject kernel reaches for this dtype/style/row shape.
 int inject_ctas_per_sm(int kv_dtype, int style, int vecs_per_lane);
 

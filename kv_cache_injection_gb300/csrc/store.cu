@@ -258,6 +258,8 @@ is_status_t upload_user_index(is_store_t* s, cudaStream_t st) {
 
 }  // namespace
 
+void isk::set_last_error_message(const char* msg) { g_err = msg ? msg : ""; }
+
 extern "C" {
 
 const char* is_last_error_message(void) { return g_err.c_str(); }
