@@ -167,6 +167,8 @@ def run_ours(args, rank, world, local_rank):
     dev = f"cuda:{local_rank}"
     spec = workloads.SPECS[args.workload]
     overrides = {"seed": rank_seed(spec.seed, rank)}
+    if args.facts:
+        overrides["facts_per_user"] = args.facts
     if args.k:
         overrides["k"] = args.k
         overrides["tokens_cap"] = args.k * int(spec.length_dist[2] if spec.length_dist[0] == "uniform"
@@ -447,6 +449,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="llama31_8b")
     ap.add_argument("--k", type=int, default=0)
+    ap.add_argument("--facts", type=int, default=0,
+                    help="facts per user (smaller store for profiling captures)")
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     args = ap.parse_args(argv)
