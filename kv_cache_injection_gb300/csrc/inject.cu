@@ -6,6 +6,7 @@
 // scatter-copied into vLLM's paged KV cache.  One pass over the data: each
 // (token, layer) row pair is read once from the store and written once to the
 // cache, the rotation done in registers on the way.
+#include <algorithm>
 #include <cmath>
 #include <cstring>
 #include <mutex>
@@ -64,21 +65,34 @@ __global__ void __launch_bounds__(256) plan_kernel(const PlanArgs a) {
 // ---------------------------------------------------------------------------
 // Gather + Chunked RoPE + paged scatter.
 //
-// Work item = (segment token t, layer l): one K row and one V row of H*D
-// elements, contiguous in the token-major store.  Items are numbered t*L + l
-// over all requests back to back; each warp takes one contiguous run of
-// items, so consecutive items usually share a token and its position, slot
-// and rotation angles, which the warp keeps in registers.
+// Work item = (segment token t, layer l): the K row and the V row of one layer,
+// H*D elements each, adjacent in the token-major store, so one bulk copy of
+// 2 * row_bytes brings both into shared memory.  Items are numbered t*L + l
+// over all requests back to back and each warp takes one contiguous run.
 //
-// Lane mapping: lane handles 16-byte vectors v = lane + 32*m of each row.
-// NeoX pairs (i, i + D/2) lie in vectors v and v ^ half_vecs: the partner
-// vector comes from lane ^ half_vecs by shuffle (or from the lane's own next
-// vector when half_vecs == 32).  Interleaved pairs lie inside one vector.
-// Either way the frequencies a lane needs depend only on its lane index, so it
-// computes VE (or VE/2) sin/cos once per position.
-template <typename T, int VC, int STYLE>
-__global__ void __launch_bounds__(256) inject_kernel(const InjectArgs a, const RopeTurns rt) {
-  extern __shared__ int32_t s_off[];            // [R + 1] token offset of each request
+// Each warp runs its own pipeline over a ring of P shared-memory stages: lane
+// 0 issues the bulk load of item i + P - 1 while the warp works on item i, so
+// the bytes in flight are set by shared memory (P stages per warp), not by
+// registers.  On the way out, V leaves shared memory by a bulk store; K is
+// read from shared memory, rotated in fp32 and stored with 16-byte vector
+// stores.  NeoX pairs (i, i + D/2) lie in vectors v and v ^ half_vecs of the
+// row, interleaved pairs inside one vector; either way the frequencies a lane
+// needs depend only on its lane index, so it computes VE (or VE/2) sin/cos
+// once per position.  Every mbarrier wait is bounded: on time-out the warp
+// latches IS_ST_TIMEOUT, stops issuing, drains its copies and returns.
+constexpr int kInjectWarpsMax = 4;
+constexpr uint64_t kWaitBudgetNs = 2000000000ull;   // 2 s per wait
+
+struct StageMeta {
+  int64_t slot;     // destination slot, -1 = nothing to do
+  int32_t p;        // position (rotation angle)
+  int32_t l;        // layer
+};
+
+template <typename T, int STYLE>
+__global__ void __launch_bounds__(kInjectWarpsMax * 32) inject_kernel(const InjectArgs a,
+                                                                      const RopeTurns rt, int P) {
+  extern __shared__ __align__(128) uint8_t smem[];
   __shared__ int32_t scratch[33];
   constexpr int VE = Vec<T>::N;
   constexpr int NF = STYLE == 0 ? VE : VE / 2;
@@ -86,6 +100,18 @@ __global__ void __launch_bounds__(256) inject_kernel(const InjectArgs a, const R
 #if defined(__CUDA_ARCH__)
   asm volatile("griddepcontrol.wait;" ::: "memory");   // inputs of the previous kernel
 #endif
+
+  const int nwarps = blockDim.x >> 5;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t item_bytes = 2u * (uint32_t)a.row_bytes;
+  int32_t* s_off = reinterpret_cast<int32_t*>(smem);                 // [R + 1]
+  const size_t off_bytes = ((size_t)(a.R + 1) * 4 + 127) & ~(size_t)127;
+  uint8_t* stages = smem + off_bytes + (size_t)warp * P * item_bytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + off_bytes + (size_t)nwarps * P * item_bytes) +
+                   (size_t)warp * P;
+  StageMeta* meta = reinterpret_cast<StageMeta*>(smem + off_bytes + (size_t)nwarps * P * item_bytes +
+                                                 (size_t)nwarps * P * 8) + (size_t)warp * P;
 
   // Exclusive prefix of seg_len over requests.
   int32_t total = 0;
@@ -104,32 +130,37 @@ __global__ void __launch_bounds__(256) inject_kernel(const InjectArgs a, const R
     __syncthreads();
   }
 
-  const int lane = threadIdx.x & 31;
   const int64_t n_items = (int64_t)total * a.L;
-  const int64_t warp_id = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int64_t n_warps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  const int64_t warp_id = (int64_t)blockIdx.x * nwarps + warp;
+  const int64_t n_warps = (int64_t)gridDim.x * nwarps;
   const int64_t chunk = (n_items + n_warps - 1) / n_warps;
-  int64_t it = warp_id * chunk;
-  const int64_t it_end = min(n_items, it + chunk);
-  if (it >= it_end) return;
+  const int64_t it0 = warp_id * chunk;
+  const int64_t it_end = min(n_items, it0 + chunk);
+  if (it0 >= it_end) return;
 
-  const uint64_t pol = policy_evict_first();
-  const int vpl = a.row_bytes >> 9;             // vectors per lane per row (row_bytes / 512)
+  if (lane == 0) {
+    for (int s = 0; s < P; ++s) mbar_init(smem_addr(&bars[s]), 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+
+  const uint32_t stage0 = smem_addr(stages);
+  const int vpl = a.row_bytes >> 9;             // 16-byte vectors per lane per row
   const int hv = a.half_vecs;
   const int fbase = STYLE == 0 ? (lane % hv) * VE : (lane % a.head_vecs) * (VE / 2);
-  const bool lane_first_half = (lane & hv) == 0;  // NeoX, half_vecs < 32
 
-  float cs[NF], sn[NF];
-  int32_t cur_t = -1, cur_r = -1, cur_j = 0, seg_lo = 0, seg_hi = 0, cur_p = -1;
-  const uint8_t* src = nullptr;
-  int64_t slot = -1;
+  // Issue-side token cache.
+  int32_t cur_t = -1, cur_r = -1, cur_j = 0, seg_lo = 0, seg_hi = 0;
+  int64_t tok_src = 0, tok_slot = -1;
+  int32_t tok_p = 0;
 
-  for (; it < it_end; ++it) {
-    const int32_t t = (int32_t)(it / a.L);
-    const int32_t l = (int32_t)(it - (int64_t)t * a.L);
+  // Warp-uniform: resolve item j's token (request, fact, position, slot) and
+  // have lane 0 start its bulk load into stage s.  Returns true if a load was issued.
+  auto issue = [&](int64_t j, int s) -> bool {
+    const int32_t t = (int32_t)(j / a.L);
+    const int32_t l = (int32_t)(j - (int64_t)t * a.L);
     if (t != cur_t) {
       cur_t = t;
-      // Request: the last r with s_off[r] <= t (zero-length requests repeat offsets).
       int lo = 0, hi = a.R;
       while (hi - lo > 1) {
         const int mid = (lo + hi) >> 1;
@@ -138,8 +169,6 @@ __global__ void __launch_bounds__(256) inject_kernel(const InjectArgs a, const R
       const int r = lo;
       const int32_t ts = t - s_off[r];
       if (r != cur_r || ts < seg_lo || ts >= seg_hi) {
-        // Fact: the last j with off[j] <= ts, by a warp-wide search over
-        // off[0 .. n] (n + 1 ascending entries, off[n] = segment length).
         const int32_t* off = a.fact_seg_off + (size_t)r * a.seg_stride;
         int jlo = 0, jhi = a.n_ids[r];
         while (jhi - jlo > 1) {
@@ -156,9 +185,10 @@ __global__ void __launch_bounds__(256) inject_kernel(const InjectArgs a, const R
         seg_hi = off[jlo + 1];
       }
       const int64_t f = a.ids[(size_t)cur_r * a.ids_stride + cur_j];
-      const int32_t p = a.seg_start[cur_r] + ts;
-      const int32_t lb = p / a.block_size;
-      slot = -1;
+      tok_src = a.fact_tok[f] + (ts - seg_lo);
+      tok_p = a.seg_start[cur_r] + ts;
+      const int32_t lb = tok_p / a.block_size;
+      tok_slot = -1;
       if (lb >= a.max_blocks) {
         if (lane == 0) latch(a.status, IS_ST_BLOCK_TABLE);
       } else {
@@ -166,55 +196,74 @@ __global__ void __launch_bounds__(256) inject_kernel(const InjectArgs a, const R
         if (blk < 0 || blk >= a.num_blocks) {
           if (lane == 0) latch(a.status, IS_ST_BLOCK_ID);
         } else {
-          slot = (int64_t)blk * a.block_size + (p - lb * a.block_size);
+          tok_slot = (int64_t)blk * a.block_size + (tok_p - lb * a.block_size);
         }
       }
-      src = a.kv + (size_t)(a.fact_tok[f] + (ts - seg_lo)) * a.L * 2 * a.row_bytes;
-      if (p != cur_p) {
-        cur_p = p;
-        const float pf = (float)p;
+    }
+    if (lane == 0) {
+      if (l == 0 && a.slot_mapping) a.slot_mapping[t] = tok_slot;
+      meta[s].slot = tok_slot;
+      meta[s].p = tok_p;
+      meta[s].l = l;
+      if (tok_slot >= 0) {
+        const uint32_t bar = smem_addr(&bars[s]);
+        mbar_expect_tx(bar, item_bytes);
+        bulk_load(stage0 + (uint32_t)s * item_bytes,
+                  a.kv + ((size_t)tok_src * a.L + l) * 2 * (size_t)a.row_bytes, item_bytes, bar);
+      }
+    }
+    return tok_slot >= 0;
+  };
+
+  uint32_t phase = 0;        // expected parity of each stage's next completion
+  uint32_t pending = 0;      // stages with a bulk load in flight
+  for (int s = 0; s < P && it0 + s < it_end; ++s)
+    if (issue(it0 + s, s)) pending |= 1u << s;
+  __syncwarp();
+
+  float cs[NF], sn[NF];
+  int32_t cur_p = -1;
+  bool aborted = false;
+  int s = 0;
+  for (int64_t i = it0; i < it_end; ++i) {
+    const StageMeta m = meta[s];
+    if (m.slot >= 0) {
+      const uint32_t bar = smem_addr(&bars[s]);
+      const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar, (phase >> s) & 1u, kWaitBudgetNs));
+      if (!ok) {
+        if (lane == 0) latch(a.status, IS_ST_TIMEOUT);
+        aborted = true;
+        break;
+      }
+      phase ^= 1u << s;
+      pending &= ~(1u << s);
+      if (m.p != cur_p) {
+        cur_p = m.p;
+        const float pf = (float)m.p;
 #pragma unroll
         for (int e = 0; e < NF; ++e) {
           const float fr = angle_turns(pf, rt.hi[fbase + e], rt.lo[fbase + e]);
           sincospif(2.0f * fr, &sn[e], &cs[e]);
         }
       }
-    }
-    if (l == 0 && lane == 0 && a.slot_mapping) a.slot_mapping[t] = slot;
-    if (slot < 0) continue;
-
-    const uint8_t* sk = src + (size_t)l * 2 * a.row_bytes;
-    const uint8_t* sv = sk + a.row_bytes;
-    uint8_t* dk = a.cache + ((size_t)(2 * l) * a.num_blocks * a.block_size + slot) * a.row_bytes;
-    uint8_t* dv = a.cache + ((size_t)(2 * l + 1) * a.num_blocks * a.block_size + slot) * a.row_bytes;
-
-    for (int c = 0; c < vpl; c += VC) {
-      uint4 kx[VC], vx[VC];
-#pragma unroll
-      for (int m = 0; m < VC; ++m) {
-        const size_t o = ((size_t)(c + m) * 32 + lane) * 16;
-        kx[m] = ld_once(sk + o, pol);
-        vx[m] = ld_once(sv + o, pol);
-      }
-#pragma unroll
-      for (int m = 0; m < VC; ++m) st_v4(dv + ((size_t)(c + m) * 32 + lane) * 16, vx[m]);
-#pragma unroll
-      for (int m = 0; m < VC; ++m) {
+      const uint32_t kst = stage0 + (uint32_t)s * item_bytes;
+      uint8_t* dk = a.cache + ((size_t)(2 * m.l) * a.num_blocks * a.block_size + m.slot) * a.row_bytes;
+      uint8_t* dv = a.cache + ((size_t)(2 * m.l + 1) * a.num_blocks * a.block_size + m.slot) * a.row_bytes;
+      if (lane == 0) bulk_store(dv, kst + a.row_bytes, a.row_bytes);
+      for (int c = 0; c < vpl; ++c) {
+        const int v = c * 32 + lane;
         float x[VE], y[VE];
-        Vec<T>::unpack(kx[m], x);
+        Vec<T>::unpack(ld_shared_v4(kst + v * 16), x);
         if (STYLE == 0) {
           float z[VE];
-          bool first;
-          if (hv < 32) {
-            Vec<T>::unpack(shfl_xor4(kx[m], hv), z);
-            first = lane_first_half;
-          } else {                                    // partner is the lane's next/previous vector
-            Vec<T>::unpack(kx[m ^ 1], z);
-            first = ((c + m) & 1) == 0;
-          }
+          Vec<T>::unpack(ld_shared_v4(kst + (v ^ hv) * 16), z);
+          if ((v & hv) == 0) {
 #pragma unroll
-          for (int e = 0; e < VE; ++e)
-            y[e] = first ? fmaf(x[e], cs[e], -z[e] * sn[e]) : fmaf(x[e], cs[e], z[e] * sn[e]);
+            for (int e = 0; e < VE; ++e) y[e] = fmaf(x[e], cs[e], -z[e] * sn[e]);
+          } else {
+#pragma unroll
+            for (int e = 0; e < VE; ++e) y[e] = fmaf(x[e], cs[e], z[e] * sn[e]);
+          }
         } else {
 #pragma unroll
           for (int e = 0; e < VE / 2; ++e) {
@@ -223,10 +272,35 @@ __global__ void __launch_bounds__(256) inject_kernel(const InjectArgs a, const R
             y[2 * e + 1] = fmaf(w, cs[e], u * sn[e]);
           }
         }
-        st_v4(dk + ((size_t)(c + m) * 32 + lane) * 16, Vec<T>::pack(y));
+        st_v4(dk + (size_t)v * 16, Vec<T>::pack(y));
       }
     }
+    if (lane == 0) bulk_commit();                 // one bulk group per item (maybe empty)
+    // Refill the stage of item i - 1 with item i - 1 + P once its V store has
+    // finished reading shared memory (all groups but the newest).
+    const int sp = s == 0 ? P - 1 : s - 1;
+    if (i > it0 && i - 1 + P < it_end) {
+      if (lane == 0) {
+        bulk_wait_read<1>();
+        fence_proxy_async_smem();
+      }
+      __syncwarp();
+      if (issue(i - 1 + P, sp)) pending |= 1u << sp;
+    }
+    __syncwarp();
+    s = s + 1 == P ? 0 : s + 1;
   }
+
+  if (aborted) {
+    // Let loads already in flight land before shared memory goes away.
+    for (int q = 0; q < P; ++q)
+      if (pending & (1u << q)) {
+        const uint32_t bar = smem_addr(&bars[q]);
+        __all_sync(0xffffffffu, mbar_wait_bounded(bar, (phase >> q) & 1u, kWaitBudgetNs));
+      }
+  }
+  if (lane == 0) bulk_wait_all();
+  __syncwarp();
 }
 
 // ---------------------------------------------------------------------------
@@ -236,63 +310,100 @@ cudaError_t launch_plan(const PlanArgs& a, const LaunchCfg& cfg) {
   return cudaGetLastError();
 }
 
-template <typename T, int VC, int STYLE>
-static cudaError_t launch_inject_t(const InjectArgs& a, const RopeTurns& rt, int grid,
-                                   const LaunchCfg& cfg) {
-  const size_t smem = (size_t)(a.R + 1) * sizeof(int32_t);
+// Shared memory plan of one inject launch: warps per CTA and stages per warp.
+struct InjectShape {
+  int warps;
+  int stages;
+  size_t smem;
+};
+
+static InjectShape inject_shape(const InjectArgs& a) {
+  const size_t item = 2 * (size_t)a.row_bytes;
+  const size_t off_bytes = ((size_t)(a.R + 1) * 4 + 127) & ~(size_t)127;
+  const size_t per_stage = item + 8 + sizeof(StageMeta);
+  const size_t stage_budget = 96 * 1024;        // two CTAs per SM
+  const size_t smem_max = 227 * 1024 - 1024;
+  for (int w = kInjectWarpsMax; w >= 1; w >>= 1) {
+    int p = (int)std::min<size_t>(16, std::max<size_t>(2, stage_budget / (w * item)));
+    size_t need = off_bytes + (size_t)w * p * per_stage;
+    while (p > 2 && need > smem_max) {
+      --p;
+      need = off_bytes + (size_t)w * p * per_stage;
+    }
+    if (need <= smem_max) return {w, p, need};
+  }
+  return {0, 0, 0};
+}
+
+// Per device and kernel instance: the dynamic shared memory limit already set
+// and the occupancy of the last shape queried.
+struct LaunchMemo {
+  size_t smem_set = 0;
+  size_t occ_smem = 0;
+  int occ_warps = 0;
+  int occ_blocks = 0;
+};
+static std::mutex g_launch_mu;
+
+template <typename T, int STYLE>
+static LaunchMemo& launch_memo(int dev) {
+  static LaunchMemo memo[64];
+  return memo[dev & 63];
+}
+
+template <typename T, int STYLE>
+static cudaError_t launch_inject_t(const InjectArgs& a, const RopeTurns& rt, const LaunchCfg& cfg) {
+  const InjectShape sh = inject_shape(a);
+  if (sh.warps == 0) return cudaErrorInvalidValue;
+  auto kern = inject_kernel<T, STYLE>;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  int per_sm = 0;
+  {
+    std::lock_guard<std::mutex> lock(g_launch_mu);
+    LaunchMemo& m = launch_memo<T, STYLE>(dev);
+    if (sh.smem > m.smem_set) {
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sh.smem);
+      if (e != cudaSuccess) return e;
+      m.smem_set = sh.smem;
+    }
+    if (m.occ_smem != sh.smem || m.occ_warps != sh.warps) {
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&m.occ_blocks, kern, sh.warps * 32, sh.smem);
+      if (e != cudaSuccess) return e;
+      m.occ_smem = sh.smem;
+      m.occ_warps = sh.warps;
+    }
+    per_sm = m.occ_blocks;
+  }
   cudaLaunchConfig_t lc = {};
-  lc.gridDim = dim3(grid);
-  lc.blockDim = dim3(256);
-  lc.dynamicSmemBytes = smem;
+  lc.gridDim = dim3(cfg.num_sms * std::max(1, per_sm));
+  lc.blockDim = dim3(sh.warps * 32);
+  lc.dynamicSmemBytes = sh.smem;
   lc.stream = cfg.stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = cfg.pdl ? 1 : 0;
   lc.attrs = attr;
   lc.numAttrs = 1;
-  return cudaLaunchKernelEx(&lc, inject_kernel<T, VC, STYLE>, a, rt);
-}
-
-template <typename T, int STYLE>
-static cudaError_t dispatch_vc(const InjectArgs& a, const RopeTurns& rt, int grid,
-                               const LaunchCfg& cfg) {
-  const int vpl = a.row_bytes >> 9;
-  if (vpl % 4 == 0) return launch_inject_t<T, 4, STYLE>(a, rt, grid, cfg);
-  if (vpl % 2 == 0) return launch_inject_t<T, 2, STYLE>(a, rt, grid, cfg);
-  return launch_inject_t<T, 1, STYLE>(a, rt, grid, cfg);
+  return cudaLaunchKernelEx(&lc, kern, a, rt, sh.stages);
 }
 
 cudaError_t launch_inject(const InjectArgs& a, const RopeTurns& rt, int kv_dtype, int style,
-                          int grid, const LaunchCfg& cfg) {
+                          const LaunchCfg& cfg) {
   if (kv_dtype == IS_BF16)
-    return style == 0 ? dispatch_vc<__nv_bfloat16, 0>(a, rt, grid, cfg)
-                      : dispatch_vc<__nv_bfloat16, 1>(a, rt, grid, cfg);
+    return style == 0 ? launch_inject_t<__nv_bfloat16, 0>(a, rt, cfg)
+                      : launch_inject_t<__nv_bfloat16, 1>(a, rt, cfg);
   if (kv_dtype == IS_F16)
-    return style == 0 ? dispatch_vc<__half, 0>(a, rt, grid, cfg)
-                      : dispatch_vc<__half, 1>(a, rt, grid, cfg);
-  return style == 0 ? dispatch_vc<float, 0>(a, rt, grid, cfg)
-                    : dispatch_vc<float, 1>(a, rt, grid, cfg);
+    return style == 0 ? launch_inject_t<__half, 0>(a, rt, cfg) : launch_inject_t<__half, 1>(a, rt, cfg);
+  return style == 0 ? launch_inject_t<float, 0>(a, rt, cfg) : launch_inject_t<float, 1>(a, rt, cfg);
 }
 
-template <typename T, int STYLE>
-static int occupancy_t(int vpl) {
-  int n = 0;
-  const size_t smem = (size_t)(IS_MAX_REQUESTS + 1) * sizeof(int32_t);
-  if (vpl % 4 == 0)
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, inject_kernel<T, 4, STYLE>, 256, smem);
-  else if (vpl % 2 == 0)
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, inject_kernel<T, 2, STYLE>, 256, smem);
-  else
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, inject_kernel<T, 1, STYLE>, 256, smem);
-  return n > 0 ? n : 1;
-}
-
-int inject_ctas_per_sm(int kv_dtype, int style, int vpl) {
-  if (kv_dtype == IS_BF16)
-    return style == 0 ? occupancy_t<__nv_bfloat16, 0>(vpl) : occupancy_t<__nv_bfloat16, 1>(vpl);
-  if (kv_dtype == IS_F16)
-    return style == 0 ? occupancy_t<__half, 0>(vpl) : occupancy_t<__half, 1>(vpl);
-  return style == 0 ? occupancy_t<float, 0>(vpl) : occupancy_t<float, 1>(vpl);
+bool inject_shape_ok(int row_bytes, int R) {
+  InjectArgs a{};
+  a.row_bytes = row_bytes;
+  a.R = R;
+  return inject_shape(a).warps > 0;
 }
 
 }  // namespace isk
@@ -319,7 +430,6 @@ struct NoAllocDevice {
   bool ready = false;
   int32_t* scratch = nullptr;   // device address of g_noalloc_scratch on this device
   int num_sms = 0;
-  int ctas[3][2][3] = {};       // [dtype][style][vpl class], 0 = not yet queried
 };
 NoAllocDevice g_na_dev[kNaMaxDevices];
 std::mutex g_na_mu;
@@ -357,8 +467,9 @@ extern "C" is_status_t is_inject_noalloc(
     return na_fail(IS_ERR_UNSUPPORTED, "head_dim must be a power of two in [16, IS_MAX_HEAD_DIM]");
   const int elt = kv_dtype == IS_F32 ? 4 : 2;
   const int64_t row_bytes = (int64_t)num_kv_heads * head_dim * elt;
-  if (row_bytes % 512 != 0)
-    return na_fail(IS_ERR_UNSUPPORTED, "num_kv_heads * head_dim * elt must be a multiple of 512");
+  if (row_bytes % 512 != 0 || !inject_shape_ok((int)row_bytes, R))
+    return na_fail(IS_ERR_UNSUPPORTED,
+                   "num_kv_heads * head_dim * elt must be a multiple of 512 and at most 32 KiB");
   if (cache->block_size < 1 || cache->num_blocks < 1 || cache->dtype != kv_dtype)
     return na_fail(IS_ERR_INVALID_ARG, "bad cache descriptor");
   if ((((uintptr_t)kv_cache) | ((uintptr_t)kv_arena)) & 15)
@@ -374,8 +485,6 @@ extern "C" is_status_t is_inject_noalloc(
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNaMaxDevices)
     return na_fail(IS_ERR_CUDA, "cudaGetDevice failed");
-  const int vpl = (int)(row_bytes >> 9);
-  const int vclass = vpl % 4 == 0 ? 0 : (vpl % 2 == 0 ? 1 : 2);
   NoAllocDevice& d = g_na_dev[dev];
   {
     std::lock_guard<std::mutex> lock(g_na_mu);
@@ -391,8 +500,6 @@ extern "C" is_status_t is_inject_noalloc(
       d.scratch = static_cast<int32_t*>(ptr);
       d.ready = true;
     }
-    if (d.ctas[kv_dtype][rope->style][vclass] == 0)
-      d.ctas[kv_dtype][rope->style][vclass] = inject_ctas_per_sm(kv_dtype, rope->style, vpl);
   }
   int32_t* seg_off = d.scratch;
   int32_t* na_n_ids = d.scratch + (size_t)kNaRequests * kNaSegStride;
@@ -449,9 +556,7 @@ extern "C" is_status_t is_inject_noalloc(
     rt.hi[i] = (float)turns;
     rt.lo[i] = (float)(turns - (double)rt.hi[i]);
   }
-  const int grid = d.num_sms * (d.ctas[kv_dtype][rope->style][vclass] > 0
-                                    ? d.ctas[kv_dtype][rope->style][vclass] : 1);
-  if (launch_inject(a, rt, kv_dtype, rope->style, grid, cfg) != cudaSuccess)
+  if (launch_inject(a, rt, kv_dtype, rope->style, cfg) != cudaSuccess)
     return na_fail(IS_ERR_CUDA, "inject launch failed");
   return IS_OK;
 }

@@ -24,13 +24,17 @@ cudaError_t launch_topk(const TopkArgs& a, const LaunchCfg& cfg);
 
 cudaError_t launch_plan(const PlanArgs& a, const LaunchCfg& cfg);
 
+// Persistent launch: one CTA per SM times the occupancy its shared-memory
+// plan allows.
 cudaError_t launch_inject(const InjectArgs& a, const RopeTurns& turns, int kv_dtype, int style,
-                          int grid_ctas, const LaunchCfg& cfg);
+                          const LaunchCfg& cfg);
+
+// Whether a row of row_bytes (K or V of one layer) and R requests fit the
+// inject kernel's shared-memory plan.
+bool inject_shape_ok(int row_bytes, int R);
 
 // Sets the message is_last_error_message() returns on this thread.
 void set_last_error_message(const char* msg);
 
-// CTAs per SM the inject kernel reaches for this dtype/style/row shape.
-int inject_ctas_per_sm(int kv_dtype, int style, int vecs_per_lane);
 
 }  // namespace isk

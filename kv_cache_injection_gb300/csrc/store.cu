@@ -71,7 +71,6 @@ struct is_store {
   int64_t max_tiles = 0;
   int64_t score_stride = 0;
   int32_t seg_stride = 0;
-  int inject_ctas = 0;
 
   uint8_t* kv = nullptr;
   int64_t* fact_tok = nullptr;
@@ -318,8 +317,9 @@ is_status_t is_store_create(const is_store_config_t* config, int device, cudaStr
     return fail(IS_ERR_UNSUPPORTED, "head_dim must be a power of two in [16, %d]", IS_MAX_HEAD_DIM);
   const int elt = dtype_bytes(c.kv_dtype);
   const int64_t row_bytes = (int64_t)c.num_kv_heads * D * elt;
-  if (row_bytes % 512 != 0)
-    return fail(IS_ERR_UNSUPPORTED, "num_kv_heads * head_dim * elt (%lld B) must be a multiple of 512",
+  if (row_bytes % 512 != 0 || !inject_shape_ok((int)row_bytes, std::max(c.max_requests, c.max_queries)))
+    return fail(IS_ERR_UNSUPPORTED,
+                "num_kv_heads * head_dim * elt (%lld B) must be a multiple of 512 and at most 32 KiB",
                 (long long)row_bytes);
 
   int ndev = 0;
@@ -380,7 +380,6 @@ is_status_t is_store_create(const is_store_config_t* config, int device, cudaStr
     free_store(s);
     return fail(IS_ERR_CUDA, "store initialisation failed: %s", cudaGetErrorString(e));
   }
-  s->inject_ctas = inject_ctas_per_sm(c.kv_dtype, 0, (int)(row_bytes >> 9));
   *out = s;
   return IS_OK;
 }
@@ -629,9 +628,8 @@ static is_status_t launch_injection(is_store_t* s, int32_t R, const int64_t* ids
   a.head_vecs = s->cfg.head_dim / ve;
   const RopeTurns rt = make_turns(*rope, s->cfg.head_dim);
   const LaunchCfg cfg{stream, s->num_sms, false};
-  const int grid = s->num_sms * std::max(1, s->inject_ctas);
   StageTimer tm(s, IS_STAGE_INJECT, stream);
-  CUDA_TRY(launch_inject(a, rt, s->cfg.kv_dtype, rope->style, grid, cfg));
+  CUDA_TRY(launch_inject(a, rt, s->cfg.kv_dtype, rope->style, cfg));
   return IS_OK;
 }
 
