@@ -53,6 +53,7 @@ extern "C" {
 #define IS_MAX_HEAD_DIM   512
 #define IS_MAX_POSITION   (1 << 24)  /* positions must stay below 2^24 */
 #define IS_EMB_TILE       128    /* embedding rows per store tile (one user per tile) */
+#define IS_MAX_FACTS_PER_USER (1 << 20)  /* facts of one user (retrieval row index width) */
 
 typedef enum {
   IS_OK = 0,
@@ -94,7 +95,7 @@ typedef struct {
   int32_t max_queries;       /* per retrieval call, <= IS_MAX_QUERIES (0: 64) */
   int32_t max_k;             /* retrieval budget / facts per request, <= IS_MAX_K (0: 256) */
   int32_t max_requests;      /* per injection call, <= IS_MAX_REQUESTS (0: max_queries) */
-  int64_t max_facts_per_user;/* sizes the score scratch (0: max_facts) */
+  int64_t max_facts_per_user;/* sizes the score scratch (0: max_facts), <= IS_MAX_FACTS_PER_USER */
 } is_store_config_t;
 
 /* Rotary embedding of the model the facts were encoded with. */

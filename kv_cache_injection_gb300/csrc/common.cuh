@@ -92,6 +92,7 @@ struct TopkArgs {
   const int32_t* user_tile_off;
   const int32_t* user_tiles;
   const int32_t* tile_fact;     // [n_tiles * kTile] fact id per embedding row
+  const int32_t* tile_len;      // [n_tiles * kTile] length of that fact
   const int32_t* fact_len;
   const int32_t* seg_start;     // [Q] or null (retrieval only)
   int64_t* ids_out;             // [Q][k]
@@ -139,6 +140,22 @@ __device__ __forceinline__ uint4 shfl_xor4(const uint4& v, int mask) {
   r.z = __shfl_xor_sync(0xffffffffu, v.z, mask);
   r.w = __shfl_xor_sync(0xffffffffu, v.w, mask);
   return r;
+}
+
+// ---- programmatic dependent launch ------------------------------------------------
+// A kernel launched with programmatic stream serialisation may start while the
+// previous kernel in the stream still runs; it must call pdl_wait() before
+// reading that kernel's outputs.  pdl_trigger() lets the next kernel launch
+// once every CTA of this one has been scheduled.
+__device__ __forceinline__ void pdl_wait() {
+#if defined(__CUDA_ARCH__)
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+#endif
+}
+__device__ __forceinline__ void pdl_trigger() {
+#if defined(__CUDA_ARCH__)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+#endif
 }
 
 // ---- shared memory, mbarrier and bulk-copy (TMA engine) primitives -------------

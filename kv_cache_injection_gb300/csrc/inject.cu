@@ -22,6 +22,7 @@ namespace isk {
 // One CTA per request.
 __global__ void __launch_bounds__(256) plan_kernel(const PlanArgs a) {
   __shared__ int32_t scratch[33];
+  pdl_trigger();
   const int r = blockIdx.x;
   int n = a.n_ids_in[r];
   if (n < 0 || n > a.ids_stride) {
@@ -97,9 +98,7 @@ __global__ void __launch_bounds__(kInjectWarpsMax * 32) inject_kernel(const Inje
   constexpr int VE = Vec<T>::N;
   constexpr int NF = STYLE == 0 ? VE : VE / 2;
 
-#if defined(__CUDA_ARCH__)
-  asm volatile("griddepcontrol.wait;" ::: "memory");   // inputs of the previous kernel
-#endif
+  pdl_wait();                                   // outputs of the planning kernel
 
   const int nwarps = blockDim.x >> 5;
   const int warp = threadIdx.x >> 5;
@@ -306,8 +305,26 @@ __global__ void __launch_bounds__(kInjectWarpsMax * 32) inject_kernel(const Inje
 // ---------------------------------------------------------------------------
 
 cudaError_t launch_plan(const PlanArgs& a, const LaunchCfg& cfg) {
-  plan_kernel<<<a.R, 256, 0, cfg.stream>>>(a);
-  return cudaGetLastError();
+  return launch_ex(plan_kernel, dim3(a.R), dim3(256), 0, cfg.stream, cfg.pdl, a);
+}
+
+void prefer_max_shared(const void* kern) {
+  static std::mutex mu;
+  static const void* done_kern[64];
+  static int done_dev[64];
+  static int n_done = 0;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return;
+  std::lock_guard<std::mutex> lock(mu);
+  for (int i = 0; i < n_done; ++i)
+    if (done_kern[i] == kern && done_dev[i] == dev) return;
+  cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                       (int)cudaSharedmemCarveoutMaxShared);
+  if (n_done < 64) {
+    done_kern[n_done] = kern;
+    done_dev[n_done] = dev;
+    ++n_done;
+  }
 }
 
 // Shared memory plan of one inject launch: warps per CTA and stages per warp.
@@ -376,17 +393,8 @@ static cudaError_t launch_inject_t(const InjectArgs& a, const RopeTurns& rt, con
     }
     per_sm = m.occ_blocks;
   }
-  cudaLaunchConfig_t lc = {};
-  lc.gridDim = dim3(cfg.num_sms * std::max(1, per_sm));
-  lc.blockDim = dim3(sh.warps * 32);
-  lc.dynamicSmemBytes = sh.smem;
-  lc.stream = cfg.stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = cfg.pdl ? 1 : 0;
-  lc.attrs = attr;
-  lc.numAttrs = 1;
-  return cudaLaunchKernelEx(&lc, kern, a, rt, sh.stages);
+  return launch_ex(kern, dim3(cfg.num_sms * std::max(1, per_sm)), dim3(sh.warps * 32), sh.smem,
+                   cfg.stream, cfg.pdl, a, rt, sh.stages);
 }
 
 cudaError_t launch_inject(const InjectArgs& a, const RopeTurns& rt, int kv_dtype, int style,
@@ -556,7 +564,8 @@ extern "C" is_status_t is_inject_noalloc(
     rt.hi[i] = (float)turns;
     rt.lo[i] = (float)(turns - (double)rt.hi[i]);
   }
-  if (launch_inject(a, rt, kv_dtype, rope->style, cfg) != cudaSuccess)
+  const LaunchCfg cfg_dep{stream, d.num_sms, true};
+  if (launch_inject(a, rt, kv_dtype, rope->style, cfg_dep) != cudaSuccess)
     return na_fail(IS_ERR_CUDA, "inject launch failed");
   return IS_OK;
 }

@@ -14,13 +14,36 @@ struct LaunchCfg {
   bool pdl;   // launch with programmatic stream serialisation
 };
 
+// cudaLaunchKernelEx with optional programmatic stream serialisation; on the
+// first launch of a kernel on a device it also asks for the largest shared
+// memory carve-out, so consecutive kernels do not reconfigure L1/shared.
+void prefer_max_shared(const void* kern);   // once per (kernel, device)
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_ex(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                      bool pdl, Args... args) {
+  prefer_max_shared(reinterpret_cast<const void*>(kern));
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = grid;
+  lc.blockDim = block;
+  lc.dynamicSmemBytes = smem;
+  lc.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+  lc.attrs = attr;
+  lc.numAttrs = 1;
+  return cudaLaunchKernelEx(&lc, kern, args...);
+}
+
 cudaError_t launch_emb_norms(const void* emb, int emb_dtype, int E, const int32_t* rows, int n,
                              float* inv_norm, cudaStream_t stream);
 
-cudaError_t launch_similarity(const SimArgs& a, int emb_dtype, int max_user_tiles,
-                              const LaunchCfg& cfg);
+// Fused retrieval (cosine similarity, then top-k by the last CTA of each
+// query).  `arrive` holds one zeroed counter per query; the kernel leaves it zeroed.
+cudaError_t launch_retrieve(const SimArgs& sa, const TopkArgs& ta, int emb_dtype, int max_user_tiles,
+                            int64_t max_user_facts, int32_t* arrive, const LaunchCfg& cfg);
 
-cudaError_t launch_topk(const TopkArgs& a, const LaunchCfg& cfg);
 
 cudaError_t launch_plan(const PlanArgs& a, const LaunchCfg& cfg);
 

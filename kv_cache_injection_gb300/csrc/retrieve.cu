@@ -5,6 +5,8 @@
 // retrieved text never crosses PCIe ("Conception de Système Native au GPU"),
 // and retrieves a relevant subset of k facts per request ("Problématique").
 // The index it names is not described; retrieval here is exact cosine top-k.
+#include <algorithm>
+
 #include "block_scan.cuh"
 #include "common.cuh"
 #include "internal.h"
@@ -49,237 +51,449 @@ cudaError_t launch_emb_norms(const void* emb, int emb_dtype, int E, const int32_
 }
 
 // ---------------------------------------------------------------------------
-// Similarity: CTA (tile, query) computes the cosine of query q with the up to
-// 128 embedding rows of one tile of q's user; a warp per row, fp32
-// accumulation.  Rows of one user are numbered 0 .. n_u-1 in fill order (tile
-// after tile), which is insertion order.
-template <typename E>
-__global__ void __launch_bounds__(256) similarity_kernel(const SimArgs a) {
-  extern __shared__ float s_q[];                 // [E] query in fp32
-  __shared__ float s_red[8];
-  const int q = blockIdx.y;
-  const int ti = blockIdx.x;
-  const int user = a.users[q];
-  if (user < 0 || user >= a.max_users) {
-    if (ti == 0 && threadIdx.x == 0) latch(a.status, IS_ST_USER_RANGE);
-    return;
-  }
-  const int t0 = a.user_tile_off[user];
-  const int ntiles = a.user_tile_off[user + 1] - t0;
-  if (ti >= ntiles) return;
-  const int tile = a.user_tiles[t0 + ti];
-  const int nrows = min(kTile, a.user_nfacts[user] - ti * kTile);
-  constexpr int VE = EmbT<E>::V::N;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+// Fused retrieval: cosine similarity + exact top-k in one launch.
+//
+// Grid (tiles * n_sub, Q).  CTA (x, q) scores 128 / n_sub embedding rows of
+// one tile of q's user, one warp per row: each lane streams 16-byte chunks of
+// the row and of the query together and accumulates q.e and q.q in fp32, so
+// the warp needs no shared memory and no barrier.  Rows of one user are
+// numbered 0 .. n_u-1 in fill order (tile after tile), which is insertion
+// order, hence ascending fact id.  After its rows, each CTA arrives on q's
+// counter; the last one (the counter reaches tiles * n_sub) resets the counter
+// and runs the top-k of q over the scores, which are then in L2.
+//
+// Top-k: radix select on order-preserving uint32 keys, 8 bits per pass, finds
+// the k-th largest key thr and how many keys equal to thr to take; keys > thr
+// are all taken and keys == thr in ascending row order (ties go to the lower
+// fact id); the picks are sorted by (key desc, row asc); ids, scores and the
+// segment plan (exclusive prefix of the facts' lengths) are written.
+constexpr int kRetThreads = 256;
+constexpr int64_t kSmemKeysMax = 4096;     // keys staged in shared memory up to this n
 
-  const E* qv = reinterpret_cast<const E*>(a.q_emb) + (size_t)q * a.E;
-  float ss = 0.f;
-  for (int c = threadIdx.x * VE; c < a.E; c += blockDim.x * VE) {
-    float x[VE];
-    EmbT<E>::V::unpack(*reinterpret_cast<const uint4*>(qv + c), x);
-#pragma unroll
-    for (int e = 0; e < VE; ++e) {
-      s_q[c + e] = x[e];
-      ss = fmaf(x[e], x[e], ss);
-    }
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-  if (lane == 0) s_red[warp] = ss;
-  __syncthreads();
-  float nq = 0.f;
-#pragma unroll
-  for (int w = 0; w < 8; ++w) nq += s_red[w];
-  const float inv_q = nq > 0.f ? 1.0f / sqrtf(nq) : 0.f;
-
-  const E* base = reinterpret_cast<const E*>(a.emb) + (size_t)tile * kTile * a.E;
-  float* out = a.scores + (size_t)q * a.score_stride + (size_t)ti * kTile;
-  for (int r = warp; r < nrows; r += 8) {
-    const E* row = base + (size_t)r * a.E;
-    float acc = 0.f;
-    for (int c = lane * VE; c < a.E; c += 32 * VE) {
-      float x[VE];
-      EmbT<E>::V::unpack(*reinterpret_cast<const uint4*>(row + c), x);
-#pragma unroll
-      for (int e = 0; e < VE; ++e) acc = fmaf(x[e], s_q[c + e], acc);
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-    if (lane == 0) out[r] = acc * inv_q * a.emb_inv_norm[(size_t)tile * kTile + r];
-  }
+// Warp-aggregated slot claim: lanes with `take` get consecutive positions
+// from one atomic on *counter per warp.  All 32 lanes must call it.
+__device__ __forceinline__ uint32_t warp_claim(bool take, uint32_t* counter, int lane) {
+  const unsigned m = __ballot_sync(0xffffffffu, take);
+  uint32_t base = 0;
+  if (lane == 0 && m) base = atomicAdd(counter, (uint32_t)__popc(m));
+  base = __shfl_sync(0xffffffffu, base, 0);
+  return base + (uint32_t)__popc(m & ((1u << lane) - 1u));
 }
 
-cudaError_t launch_similarity(const SimArgs& a, int emb_dtype, int max_user_tiles,
-                              const LaunchCfg& cfg) {
-  if (max_user_tiles <= 0) return cudaSuccess;
-  const dim3 grid(max_user_tiles, a.Q);
-  const size_t smem = (size_t)a.E * sizeof(float);
-  if (emb_dtype == IS_F16)
-    similarity_kernel<__half><<<grid, 256, smem, cfg.stream>>>(a);
-  else
-    similarity_kernel<float><<<grid, 256, smem, cfg.stream>>>(a);
-  return cudaGetLastError();
+__device__ __forceinline__ uint32_t warp_excl_scan(uint32_t x, int lane, uint32_t* total) {
+  uint32_t inc = x;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += y;
+  }
+  *total = __shfl_sync(0xffffffffu, inc, 31);
+  return inc - x;
 }
 
-// ---------------------------------------------------------------------------
-// Top-k of one query's scores (one CTA per query):
-//  1. radix select on order-preserving uint32 keys, 8 bits per pass, finds
-//     the k-th largest key `thr` and how many keys equal to it to take;
-//  2. keys > thr are all taken; of the keys == thr, the lowest rows (= lowest
-//     fact ids) are taken;
-//  3. the k picks are sorted by (key desc, row asc) with a bitonic sort;
-//  4. ids/scores are written, and the segment plan (prefix of lengths).
-constexpr int kTopkThreads = 256;
+constexpr int kCandMax = IS_MAX_K;          // candidates sorted exactly (10-bit slot index)
+constexpr int kCosBins = 2048;
 
-__global__ void __launch_bounds__(kTopkThreads) topk_kernel(const TopkArgs a) {
-  __shared__ uint32_t hist[256];
-  __shared__ unsigned long long sel[IS_MAX_K];
-  __shared__ int32_t scratch[33];
-  __shared__ uint32_t s_digit, s_above, s_cnt;
+struct TopkShared {
+  uint32_t hist[kCosBins];                  // cosine bins; the radix fallback reuses it as [4][256]
+  unsigned long long sel[kCandMax];         // (key << 32) | ((2^20-1 - row) << 10) | slot
+  unsigned long long cand[kCandMax];        // (length << 32) | fact id, by slot
+  int32_t scratch[33];
+  uint32_t wsum[8];
+  uint32_t bstar, above, eq, digit, cnt;
+};
 
-  const int q = blockIdx.x;
-  const int tid = threadIdx.x;
-  const int user = a.users[q];
-  int n = 0;
-  if (user >= 0 && user < a.max_users) {
-    n = a.user_nfacts[user];
-  } else if (tid == 0) {
-    latch(a.status, IS_ST_USER_RANGE);
+// Bin of a cosine in [-1, 1] on a uniform 2048-bin grid (monotone in s).
+__device__ __forceinline__ int cos_bin(float s) {
+  const int b = (int)((s + 1.0f) * 1024.0f);
+  return min(kCosBins - 1, max(0, b));
+}
+
+__device__ __forceinline__ unsigned long long sel_entry(uint32_t key, uint32_t row, uint32_t slot) {
+  return ((unsigned long long)key << 32) | ((unsigned long long)(0xFFFFFu - row) << 10) | slot;
+}
+
+// Records candidate `slot` = row j of the user: its fact id and length.
+__device__ __forceinline__ void fetch_cand(const TopkArgs& a, TopkShared& sh, int t0, uint32_t j,
+                                           uint32_t slot) {
+  const int tile = a.user_tiles[t0 + (int)(j / kTile)];
+  const size_t row = (size_t)tile * kTile + (j % kTile);
+  sh.cand[slot] = ((unsigned long long)(uint32_t)a.tile_len[row] << 32) | (uint32_t)a.tile_fact[row];
+}
+
+// Writes the segment plan of query q from its facts' lengths (one warp).
+__device__ __forceinline__ void plan_tail(const TopkArgs& a, int q, int nn, int32_t total) {
+  int32_t* off = a.fact_seg_off + (size_t)q * a.seg_stride;
+  const int32_t start = a.seg_start[q];
+  if (start < 0 || (int64_t)start + total > (int64_t)IS_MAX_POSITION) {
+    latch(a.status, IS_ST_POSITION);
+    nn = 0;
+    total = 0;
   }
+  off[nn] = total;
+  a.n_ids_out[q] = nn;
+  a.seg_len[q] = total;
+}
+
+// The top-k of query q by the whole CTA (kRetThreads threads):
+//  A. load the n scores (8 loads in flight per thread), stage their
+//     order-preserving keys, histogram their cosine bins;
+//  B. find the bin b* holding the k-th largest score;
+//  C. candidates = every row in bins >= b* (k plus the rest of bin b*), with
+//     their fact ids and lengths fetched on the way; if more than kCandMax
+//     crowd into b* (heavy ties), an exact 4-pass radix select on the keys
+//     picks exactly k rows instead (ties to the lower row);
+//  D. exact sort of the candidates by (key desc, row asc) and output of the
+//     first k, with the segment plan.
+template <bool SMEM_KEYS>
+__device__ void topk_block(const TopkArgs& a, TopkShared& sh, uint32_t* s_keys, int q, int user, int n) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int kk = min(a.k, n);
   const float* sc = a.scores + (size_t)q * a.score_stride;
+  auto key_at = [&](int j) -> uint32_t { return SMEM_KEYS ? s_keys[j] : score_key(__ldcg(sc + j)); };
+  const int t0 = n > 0 ? a.user_tile_off[user] : 0;
+  int64_t* ids = a.ids_out + (size_t)q * a.k;
+  float* scs = a.scores_out + (size_t)q * a.k;
 
-  uint32_t prefix = 0, rem = (uint32_t)kk, eq_total = 0;
+  for (int i = tid; i < kCosBins; i += kRetThreads) sh.hist[i] = 0;
+  if (tid == 0) sh.cnt = 0;
+  __syncthreads();
   if (kk > 0) {
+    for (int b = 0; b < n; b += 8 * kRetThreads) {
+      float v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int j = b + u * kRetThreads + tid;
+        v[u] = j < n ? __ldcg(sc + j) : 0.f;
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int j = b + u * kRetThreads + tid;
+        if (j < n) {
+          if (SMEM_KEYS) s_keys[j] = score_key(v[u]);
+          atomicAdd(&sh.hist[cos_bin(v[u])], 1u);
+        }
+      }
+    }
+  }
+  for (int r = kk + tid; r < a.k; r += kRetThreads) {
+    ids[r] = -1;
+    scs[r] = -INFINITY;
+  }
+  __syncthreads();
+  if (kk == 0) {
+    if (a.fact_seg_off && tid == 0) plan_tail(a, q, 0, 0);
+    return;
+  }
+
+  // B: warp w scans bins 2047 - 256w downwards, lane l eight of them.
+  {
+    const int hi = kCosBins - 1 - 256 * warp - 8 * lane;
+    uint32_t c[8], sum = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      c[i] = sh.hist[hi - i];
+      sum += c[i];
+    }
+    uint32_t wtot;
+    const uint32_t before_l = warp_excl_scan(sum, lane, &wtot);
+    if (lane == 0) sh.wsum[warp] = wtot;
+    __syncthreads();
+    uint32_t before = before_l;
+    for (int w = 0; w < warp; ++w) before += sh.wsum[w];
+    if (before < (uint32_t)kk && before + sum >= (uint32_t)kk) {
+      uint32_t run = before;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        if (run < (uint32_t)kk && run + c[i] >= (uint32_t)kk) {
+          sh.bstar = hi - i;
+          sh.above = run;
+          sh.eq = c[i];
+        }
+        run += c[i];
+      }
+    }
+    __syncthreads();
+  }
+
+  uint32_t C;                                   // candidates to sort
+  if (sh.above + sh.eq <= (uint32_t)kCandMax) {
+    const int bstar = sh.bstar;
+    C = sh.above + sh.eq;
+    for (int b = 0; b < n; b += kRetThreads) {
+      const int j = b + tid;
+      const uint32_t key = j < n ? key_at(j) : 0u;
+      const bool take = j < n && cos_bin(key_score(key)) >= bstar;
+      const uint32_t slot = warp_claim(take, &sh.cnt, lane);
+      if (take) {
+        sh.sel[slot] = sel_entry(key, (uint32_t)j, slot);
+        fetch_cand(a, sh, t0, (uint32_t)j, slot);
+      }
+    }
+  } else {
+    // Radix select: 8 bits per pass finds the k-th largest key thr and how
+    // many keys equal to it to take.
+    uint32_t* h4 = sh.hist;                    // [4][256]
+    for (int i = tid; i < 1024; i += kRetThreads) h4[i] = 0;
+    __syncthreads();
+    uint32_t prefix = 0, rem = (uint32_t)kk;
     for (int pass = 0; pass < 4; ++pass) {
       const int shift = 24 - 8 * pass;
       const uint32_t hmask = pass == 0 ? 0u : (0xffffffffu << (32 - 8 * pass));
-      hist[tid] = 0;                             // kTopkThreads == 256 bins
-      __syncthreads();
-      for (int j = tid; j < n; j += kTopkThreads) {
-        const uint32_t key = score_key(sc[j]);
-        if ((key & hmask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
-      }
-      __syncthreads();
-      // Thread t holds the count of digit 255 - t; inclusive scan gives the
-      // number of keys whose digit is >= 255 - t.
-      const int32_t c = (int32_t)hist[255 - tid];
-      int32_t tot;
-      const int32_t before = block_exclusive_scan(c, scratch, &tot);
-      if (before < (int32_t)rem && before + c >= (int32_t)rem) {
-        s_digit = 255u - tid;
-        s_above = (uint32_t)before;
-        s_cnt = (uint32_t)c;
-      }
-      __syncthreads();
-      prefix |= s_digit << shift;
-      rem -= s_above;
-      eq_total = s_cnt;                           // after the last pass: keys equal to thr
-      __syncthreads();
-    }
-  }
-  const uint32_t thr = prefix;
-  const uint32_t n_gt = (uint32_t)kk - rem;
-
-  // Collect.
-  if (tid == 0) s_cnt = 0;
-  __syncthreads();
-  if (kk > 0) {
-    if (eq_total == rem) {
-      // every key >= thr is taken: order of collection does not matter
-      for (int j = tid; j < n; j += kTopkThreads) {
-        const uint32_t key = score_key(sc[j]);
-        if (key >= thr) {
-          const uint32_t pos = atomicAdd(&s_cnt, 1u);
-          sel[pos] = ((unsigned long long)key << 32) | (0xffffffffu - (uint32_t)j);
-        }
-      }
-    } else {
-      // ties cross the boundary: keys == thr are taken in ascending row order
-      uint32_t taken = 0;
-      for (int b = 0; b < n; b += kTopkThreads) {
+      for (int b = 0; b < n; b += kRetThreads) {
         const int j = b + tid;
-        const uint32_t key = j < n ? score_key(sc[j]) : 0u;
-        if (j < n && key > thr) {
-          const uint32_t pos = atomicAdd(&s_cnt, 1u);
-          sel[pos] = ((unsigned long long)key << 32) | (0xffffffffu - (uint32_t)j);
+        bool in = false;
+        uint32_t digit = 256u;
+        if (j < n) {
+          const uint32_t key = key_at(j);
+          in = (key & hmask) == prefix;
+          if (in) digit = (key >> shift) & 255u;
         }
-        const int32_t is_eq = (j < n && key == thr) ? 1 : 0;
-        int32_t tot;
-        const int32_t rank = block_exclusive_scan(is_eq, scratch, &tot);
-        if (is_eq && taken + (uint32_t)rank < rem)
-          sel[n_gt + taken + rank] = ((unsigned long long)key << 32) | (0xffffffffu - (uint32_t)j);
-        taken += (uint32_t)tot;
+        const unsigned peers = __match_any_sync(0xffffffffu, digit);
+        if (in && lane == __ffs(peers) - 1) atomicAdd(&h4[pass * 256 + digit], (uint32_t)__popc(peers));
       }
+      __syncthreads();
+      if (warp == 0) {
+        uint32_t c[8], sum = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          c[i] = h4[pass * 256 + 255 - 8 * lane - i];
+          sum += c[i];
+        }
+        uint32_t tot;
+        const uint32_t before = warp_excl_scan(sum, lane, &tot);
+        if (before < rem && before + sum >= rem) {
+          uint32_t run = before;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            if (run < rem && run + c[i] >= rem) {
+              sh.digit = 255u - 8u * lane - i;
+              sh.above = run;
+              sh.eq = c[i];
+            }
+            run += c[i];
+          }
+        }
+      }
+      __syncthreads();
+      prefix |= sh.digit << shift;
+      rem -= sh.above;
+    }
+    const uint32_t thr = prefix;
+    const uint32_t n_gt = (uint32_t)kk - rem;
+    C = (uint32_t)kk;
+    uint32_t taken = 0;
+    for (int b = 0; b < n; b += kRetThreads) {
+      const int j = b + tid;
+      const uint32_t key = j < n ? key_at(j) : 0u;
+      const bool gt = j < n && key > thr;
+      const uint32_t slot = warp_claim(gt, &sh.cnt, lane);
+      if (gt) {
+        sh.sel[slot] = sel_entry(key, (uint32_t)j, slot);
+        fetch_cand(a, sh, t0, (uint32_t)j, slot);
+      }
+      // keys == thr in ascending row order, until rem of them are taken
+      const int32_t is_eq = (j < n && key == thr) ? 1 : 0;
+      int32_t tot;
+      const int32_t rank = block_exclusive_scan(is_eq, sh.scratch, &tot);
+      if (is_eq && taken + (uint32_t)rank < rem) {
+        const uint32_t slot_eq = n_gt + taken + (uint32_t)rank;
+        sh.sel[slot_eq] = sel_entry(key, (uint32_t)j, slot_eq);
+        fetch_cand(a, sh, t0, (uint32_t)j, slot_eq);
+      }
+      taken += (uint32_t)tot;
     }
   }
   __syncthreads();
 
-  // Bitonic sort, descending, over the next power of two >= kk.
+  if (C <= 64) {
+    // One warp: bitonic sort of 64 entries in registers (2 per lane), outputs
+    // and the segment plan by warp scan.
+    if (warp == 0) {
+      unsigned long long v[2];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) v[h] = (uint32_t)(2 * lane + h) < C ? sh.sel[2 * lane + h] : 0ull;
+#pragma unroll
+      for (int size = 2; size <= 64; size <<= 1) {
+#pragma unroll
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+          if (stride == 1) {
+            const bool desc = ((2 * lane) & size) == 0;
+            const unsigned long long hi = v[0] > v[1] ? v[0] : v[1];
+            const unsigned long long lo = v[0] > v[1] ? v[1] : v[0];
+            v[0] = desc ? hi : lo;
+            v[1] = desc ? lo : hi;
+          } else {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const int pos = 2 * lane + h;
+              const unsigned long long o = __shfl_xor_sync(0xffffffffu, v[h], stride >> 1);
+              const bool lower = (pos & stride) == 0;
+              const bool desc = (pos & size) == 0;
+              const unsigned long long hi = v[h] > o ? v[h] : o;
+              const unsigned long long lo = v[h] > o ? o : v[h];
+              v[h] = (lower == desc) ? hi : lo;
+            }
+          }
+        }
+      }
+      int32_t len0 = 0, len1 = 0;
+      if (2 * lane < kk) {
+        const unsigned long long cv = sh.cand[v[0] & 1023u];
+        len0 = (int32_t)(cv >> 32);
+        ids[2 * lane] = (int32_t)(uint32_t)cv;
+        scs[2 * lane] = key_score((uint32_t)(v[0] >> 32));
+      }
+      if (2 * lane + 1 < kk) {
+        const unsigned long long cv = sh.cand[v[1] & 1023u];
+        len1 = (int32_t)(cv >> 32);
+        ids[2 * lane + 1] = (int32_t)(uint32_t)cv;
+        scs[2 * lane + 1] = key_score((uint32_t)(v[1] >> 32));
+      }
+      if (a.fact_seg_off) {
+        uint32_t tot;
+        const uint32_t base = warp_excl_scan((uint32_t)(len0 + len1), lane, &tot);
+        int32_t* off = a.fact_seg_off + (size_t)q * a.seg_stride;
+        if (2 * lane < kk) off[2 * lane] = (int32_t)base;
+        if (2 * lane + 1 < kk) off[2 * lane + 1] = (int32_t)base + len0;
+        if (lane == 0) plan_tail(a, q, kk, (int32_t)tot);
+      }
+    }
+    return;
+  }
+
+  // C > 64: bitonic sort in shared memory over the next power of two.
   int P = 1;
-  while (P < kk) P <<= 1;
-  for (int i = kk + tid; i < P; i += kTopkThreads) sel[i] = 0ull;
+  while ((uint32_t)P < C) P <<= 1;
+  for (int i = (int)C + tid; i < P; i += kRetThreads) sh.sel[i] = 0ull;
   __syncthreads();
   for (int size = 2; size <= P; size <<= 1) {
     for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      for (int i = tid; i < P / 2; i += kTopkThreads) {
+      for (int i = tid; i < P / 2; i += kRetThreads) {
         const int lo = 2 * i - (i & (stride - 1));
         const int hi = lo + stride;
         const bool desc = (lo & size) == 0;
-        const unsigned long long x = sel[lo], y = sel[hi];
+        const unsigned long long x = sh.sel[lo], y = sh.sel[hi];
         if ((x < y) == desc) {
-          sel[lo] = y;
-          sel[hi] = x;
+          sh.sel[lo] = y;
+          sh.sel[hi] = x;
         }
       }
       __syncthreads();
     }
   }
-
-  // Outputs + segment plan.
-  const int t0 = (kk > 0) ? a.user_tile_off[user] : 0;
   int32_t carry = 0;
-  for (int b = 0; b < a.k; b += kTopkThreads) {
+  for (int b = 0; b < kk; b += kRetThreads) {
     const int r = b + tid;
     int32_t len = 0;
-    if (r < a.k) {
-      int64_t id = -1;
-      float s = -INFINITY;
-      if (r < kk) {
-        const unsigned long long v = sel[r];
-        const uint32_t j = 0xffffffffu - (uint32_t)(v & 0xffffffffu);
-        const int tile = a.user_tiles[t0 + (int)(j / kTile)];
-        id = a.tile_fact[(size_t)tile * kTile + (j % kTile)];
-        s = key_score((uint32_t)(v >> 32));
-        len = a.fact_len[id];
-      }
-      a.ids_out[(size_t)q * a.k + r] = id;
-      a.scores_out[(size_t)q * a.k + r] = s;
+    if (r < kk) {
+      const unsigned long long e = sh.sel[r];
+      const unsigned long long cv = sh.cand[e & 1023u];
+      len = (int32_t)(cv >> 32);
+      ids[r] = (int32_t)(uint32_t)cv;
+      scs[r] = key_score((uint32_t)(e >> 32));
     }
     if (a.fact_seg_off) {
       int32_t tot;
-      const int32_t ex = block_exclusive_scan(len, scratch, &tot);
+      const int32_t ex = block_exclusive_scan(len, sh.scratch, &tot);
       if (r < kk) a.fact_seg_off[(size_t)q * a.seg_stride + r] = carry + ex;
       carry += tot;
     }
   }
-  if (a.fact_seg_off && tid == 0) {
-    int nn = kk;
-    const int32_t start = a.seg_start[q];
-    if (start < 0 || (int64_t)start + carry > (int64_t)IS_MAX_POSITION) {
-      latch(a.status, IS_ST_POSITION);
-      nn = 0;
-      carry = 0;
-    }
-    a.fact_seg_off[(size_t)q * a.seg_stride + nn] = carry;
-    a.n_ids_out[q] = nn;
-    a.seg_len[q] = carry;
-  }
+  if (a.fact_seg_off && tid == 0) plan_tail(a, q, kk, carry);
 }
 
-cudaError_t launch_topk(const TopkArgs& a, const LaunchCfg& cfg) {
-  topk_kernel<<<a.Q, kTopkThreads, 0, cfg.stream>>>(a);
-  return cudaGetLastError();
+template <typename E, bool SMEM_KEYS>
+__global__ void __launch_bounds__(kRetThreads) retrieve_kernel(const SimArgs sa, const TopkArgs ta,
+                                                               int n_sub, int32_t* arrive) {
+  extern __shared__ uint32_t s_keys[];         // [n] keys of the top-k phase (SMEM_KEYS)
+  __shared__ TopkShared sh;
+  __shared__ int s_last;
+  pdl_trigger();
+  const int q = blockIdx.y;
+  const int ti = blockIdx.x / n_sub;
+  const int sub = blockIdx.x - ti * n_sub;
+  const int user = sa.users[q];
+  const bool user_ok = user >= 0 && user < sa.max_users;
+  const int t0 = user_ok ? sa.user_tile_off[user] : 0;
+  const int ntiles = user_ok ? sa.user_tile_off[user + 1] - t0 : 0;
+  if (ntiles == 0) {
+    // Unknown user or no facts: CTA x = 0 writes the empty result.
+    if (blockIdx.x == 0) {
+      if (!user_ok && threadIdx.x == 0) latch(sa.status, IS_ST_USER_RANGE);
+      topk_block<SMEM_KEYS>(ta, sh, s_keys, q, user, 0);
+    }
+    return;
+  }
+  if (ti >= ntiles) return;
+  const int n_u = sa.user_nfacts[user];
+  const int tile = sa.user_tiles[t0 + ti];
+  const int rows_per = kTile / n_sub;
+  const int r_begin = sub * rows_per;
+  const int r_end = min(r_begin + rows_per, n_u - ti * kTile);
+  constexpr int VE = EmbT<E>::V::N;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const E* qv = reinterpret_cast<const E*>(sa.q_emb) + (size_t)q * sa.E;
+  const E* base = reinterpret_cast<const E*>(sa.emb) + (size_t)tile * kTile * sa.E;
+  float* out = sa.scores + (size_t)q * sa.score_stride + (size_t)ti * kTile;
+  for (int r = r_begin + warp; r < r_end; r += kRetThreads / 32) {
+    const float inv_e = sa.emb_inv_norm[(size_t)tile * kTile + r];
+    const E* row = base + (size_t)r * sa.E;
+    float dot = 0.f, qq = 0.f;
+#pragma unroll 4
+    for (int c = lane * VE; c < sa.E; c += 32 * VE) {
+      float x[VE], y[VE];
+      EmbT<E>::V::unpack(*reinterpret_cast<const uint4*>(row + c), x);
+      EmbT<E>::V::unpack(*reinterpret_cast<const uint4*>(qv + c), y);
+#pragma unroll
+      for (int e = 0; e < VE; ++e) {
+        dot = fmaf(x[e], y[e], dot);
+        qq = fmaf(y[e], y[e], qq);
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      dot += __shfl_xor_sync(0xffffffffu, dot, o);
+      qq += __shfl_xor_sync(0xffffffffu, qq, o);
+    }
+    if (lane == 0) out[r] = dot * (qq > 0.f ? 1.0f / sqrtf(qq) : 0.f) * inv_e;
+  }
+  // Arrive; the last CTA of query q runs its top-k.
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const int done = atomicAdd(&arrive[q], 1);
+    s_last = done == ntiles * n_sub - 1;
+    if (s_last) arrive[q] = 0;
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  topk_block<SMEM_KEYS>(ta, sh, s_keys, q, user, n_u);
+}
+
+template <typename E>
+static cudaError_t launch_retrieve_t(const SimArgs& sa, const TopkArgs& ta, int n_sub, dim3 grid,
+                                     int64_t max_user_facts, int32_t* arrive, const LaunchCfg& cfg) {
+  if (max_user_facts <= kSmemKeysMax) {
+    const size_t smem = (size_t)std::max<int64_t>(max_user_facts, 1) * sizeof(uint32_t);
+    return launch_ex(retrieve_kernel<E, true>, grid, dim3(kRetThreads), smem, cfg.stream, cfg.pdl, sa,
+                     ta, n_sub, arrive);
+  }
+  return launch_ex(retrieve_kernel<E, false>, grid, dim3(kRetThreads), 0, cfg.stream, cfg.pdl, sa, ta,
+                   n_sub, arrive);
+}
+
+cudaError_t launch_retrieve(const SimArgs& sa, const TopkArgs& ta, int emb_dtype, int max_user_tiles,
+                            int64_t max_user_facts, int32_t* arrive, const LaunchCfg& cfg) {
+  // Split tiles into sub-tiles until the grid covers the SMs a few times over.
+  const int tiles = std::max(1, max_user_tiles);
+  int n_sub = 1;
+  while (n_sub < 16 && (int64_t)tiles * sa.Q * n_sub < 4LL * cfg.num_sms) n_sub *= 2;
+  const dim3 grid(tiles * n_sub, sa.Q);
+  if (emb_dtype == IS_F16)
+    return launch_retrieve_t<__half>(sa, ta, n_sub, grid, max_user_facts, arrive, cfg);
+  return launch_retrieve_t<float>(sa, ta, n_sub, grid, max_user_facts, arrive, cfg);
 }
 
 }  // namespace isk

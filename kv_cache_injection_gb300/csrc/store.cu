@@ -79,6 +79,7 @@ struct is_store {
   uint8_t* emb = nullptr;
   float* emb_inv_norm = nullptr;
   int32_t* tile_fact = nullptr;
+  int32_t* tile_len = nullptr;    // length of the fact of each embedding row
   int32_t* user_nfacts = nullptr;
   int32_t* user_tile_off = nullptr;
   int32_t* user_tiles = nullptr;
@@ -90,6 +91,7 @@ struct is_store {
   int32_t* seg_len_tmp = nullptr;
   int32_t* rows_tmp = nullptr;
   uint32_t* status = nullptr;
+  int32_t* arrive = nullptr;      // per-query arrival counters of the retrieval kernel
   int64_t scratch_bytes = 0;
 
   int64_t n_facts = 0, n_tokens = 0;
@@ -126,9 +128,9 @@ is_status_t dev_alloc(P** p, size_t bytes, is_store_t* s, const char* what) {
 
 void free_store(is_store_t* s) {
   void* ptrs[] = {s->kv, s->fact_tok, s->fact_len, s->fact_user, s->emb, s->emb_inv_norm,
-                  s->tile_fact, s->user_nfacts, s->user_tile_off, s->user_tiles, s->scores,
+                  s->tile_fact, s->tile_len, s->user_nfacts, s->user_tile_off, s->user_tiles, s->scores,
                   s->ids_tmp, s->scores_tmp, s->fact_seg_off, s->n_ids, s->seg_len_tmp,
-                  s->rows_tmp, s->status};
+                  s->rows_tmp, s->status, s->arrive};
   for (void* p : ptrs)
     if (p) cudaFree(p);
   for (int st = 0; st < IS_NUM_STAGES; ++st)
@@ -306,6 +308,7 @@ is_status_t is_store_create(const is_store_config_t* config, int device, cudaStr
   if (c.max_k == 0) c.max_k = 256;
   if (c.max_requests == 0) c.max_requests = c.max_queries;
   if (c.max_facts_per_user <= 0 || c.max_facts_per_user > c.max_facts) c.max_facts_per_user = c.max_facts;
+  if (c.max_facts_per_user > IS_MAX_FACTS_PER_USER) c.max_facts_per_user = IS_MAX_FACTS_PER_USER;
   if (c.max_queries < 1 || c.max_queries > IS_MAX_QUERIES)
     return fail(IS_ERR_INVALID_ARG, "max_queries must be in [1, %d]", IS_MAX_QUERIES);
   if (c.max_k < 1 || c.max_k > IS_MAX_K) return fail(IS_ERR_INVALID_ARG, "max_k must be in [1, %d]", IS_MAX_K);
@@ -358,6 +361,7 @@ is_status_t is_store_create(const is_store_config_t* config, int device, cudaStr
   ALLOC(emb, (size_t)s->max_tiles * kTile * c.emb_dim * s->emb_elt, "embedding tiles");
   ALLOC(emb_inv_norm, (size_t)s->max_tiles * kTile * 4, "embedding norms");
   ALLOC(tile_fact, (size_t)s->max_tiles * kTile * 4, "tile fact ids");
+  ALLOC(tile_len, (size_t)s->max_tiles * kTile * 4, "tile fact lengths");
   ALLOC(user_nfacts, (size_t)c.max_users * 4, "user counts");
   ALLOC(user_tile_off, (size_t)(c.max_users + 1) * 4, "user tile offsets");
   ALLOC(user_tiles, (size_t)s->max_tiles * 4, "user tiles");
@@ -369,12 +373,14 @@ is_status_t is_store_create(const is_store_config_t* config, int device, cudaStr
   ALLOC(seg_len_tmp, R * 4, "segment lengths");
   ALLOC(rows_tmp, (size_t)c.max_facts * 4, "row list");
   ALLOC(status, 4, "status word");
+  ALLOC(arrive, Q * 4, "arrival counters");
 #undef ALLOC
   s->scratch_bytes = (int64_t)(Q * s->score_stride * 4 + Q * c.max_k * 12 +
                                R * (s->seg_stride * 4 + 8) + (size_t)c.max_facts * 4 + 4);
   cudaError_t e = cudaMemsetAsync(s->status, 0, 4, stream);
   if (e == cudaSuccess) e = cudaMemsetAsync(s->user_tile_off, 0, (size_t)(c.max_users + 1) * 4, stream);
   if (e == cudaSuccess) e = cudaMemsetAsync(s->user_nfacts, 0, (size_t)c.max_users * 4, stream);
+  if (e == cudaSuccess) e = cudaMemsetAsync(s->arrive, 0, Q * 4, stream);
   if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
   if (e != cudaSuccess) {
     free_store(s);
@@ -482,6 +488,8 @@ is_status_t is_store_add_facts(is_store_t* s, int32_t user, int32_t n, const int
     while (j < n && rows[j] == rows[j - 1] + 1) ++j;
     CUDA_TRY(cudaMemcpyAsync(s->tile_fact + rows[i], fids.data() + i, (size_t)(j - i) * 4,
                              cudaMemcpyHostToDevice, stream));
+    CUDA_TRY(cudaMemcpyAsync(s->tile_len + rows[i], lengths + i, (size_t)(j - i) * 4,
+                             cudaMemcpyHostToDevice, stream));
     i = j;
   }
   CUDA_TRY(cudaMemcpyAsync(s->rows_tmp, rows.data(), (size_t)n * 4, cudaMemcpyHostToDevice, stream));
@@ -523,7 +531,7 @@ static is_status_t check_retrieve(is_store_t* s, int32_t Q, const int32_t* users
 static is_status_t run_retrieval(is_store_t* s, int32_t Q, const int32_t* users, const void* q_emb,
                                  int32_t k, int64_t* ids, float* scores, const int32_t* seg_start,
                                  int32_t* seg_len, cudaStream_t stream) {
-  const LaunchCfg cfg{stream, s->num_sms, false};
+  const LaunchCfg cfg{stream, s->num_sms, false};     // first kernel: stream order
   SimArgs sa{};
   sa.emb = s->emb;
   sa.emb_inv_norm = s->emb_inv_norm;
@@ -538,10 +546,6 @@ static is_status_t run_retrieval(is_store_t* s, int32_t Q, const int32_t* users,
   sa.Q = Q;
   sa.E = s->cfg.emb_dim;
   sa.max_users = s->cfg.max_users;
-  {
-    StageTimer tm(s, IS_STAGE_SIMILARITY, stream);
-    CUDA_TRY(launch_similarity(sa, s->cfg.emb_dtype, s->max_user_tiles, cfg));
-  }
   TopkArgs ta{};
   ta.scores = s->scores;
   ta.score_stride = s->score_stride;
@@ -550,6 +554,7 @@ static is_status_t run_retrieval(is_store_t* s, int32_t Q, const int32_t* users,
   ta.user_tile_off = s->user_tile_off;
   ta.user_tiles = s->user_tiles;
   ta.tile_fact = s->tile_fact;
+  ta.tile_len = s->tile_len;
   ta.fact_len = s->fact_len;
   ta.seg_start = seg_start;
   ta.ids_out = ids;
@@ -563,8 +568,9 @@ static is_status_t run_retrieval(is_store_t* s, int32_t Q, const int32_t* users,
   ta.k = k;
   ta.max_users = s->cfg.max_users;
   {
-    StageTimer tm(s, IS_STAGE_TOPK, stream);
-    CUDA_TRY(launch_topk(ta, cfg));
+    StageTimer tm(s, IS_STAGE_SIMILARITY, stream);
+    CUDA_TRY(launch_retrieve(sa, ta, s->cfg.emb_dtype, s->max_user_tiles, s->max_user_facts, s->arrive,
+                             cfg));
   }
   return IS_OK;
 }
@@ -627,7 +633,7 @@ static is_status_t launch_injection(is_store_t* s, int32_t R, const int64_t* ids
   a.half_vecs = s->cfg.head_dim / 2 / ve;
   a.head_vecs = s->cfg.head_dim / ve;
   const RopeTurns rt = make_turns(*rope, s->cfg.head_dim);
-  const LaunchCfg cfg{stream, s->num_sms, false};
+  const LaunchCfg cfg{stream, s->num_sms, true};      // follows the planning kernel
   StageTimer tm(s, IS_STAGE_INJECT, stream);
   CUDA_TRY(launch_inject(a, rt, s->cfg.kv_dtype, rope->style, cfg));
   return IS_OK;
