@@ -31,6 +31,7 @@ struct InjectArgs {
   int64_t n_facts;
   const int64_t* ids;           // [R][ids_stride]
   int32_t ids_stride;
+  const int64_t* fact_src;      // [R][seg_stride] arena token of each planned fact, or null
   const int32_t* n_ids;         // [R] facts per request (after planning)
   const int32_t* fact_seg_off;  // [R][seg_stride]: exclusive prefix of fact lengths
   int32_t seg_stride;
@@ -59,9 +60,13 @@ struct PlanArgs {
   const int32_t* seg_start;
   const int32_t* fact_len;
   const int32_t* fact_user;
+  const int64_t* fact_tok;
   int64_t n_facts;
   int32_t* n_ids_out;           // [R]
   int32_t* fact_seg_off;        // [R][seg_stride]
+  int64_t* fact_src;            // [R][seg_stride] arena token of each planned fact, or null
+  const int32_t* block_table;   // [R][max_blocks] (prefetched into L2)
+  int32_t max_blocks;
   int32_t seg_stride;
   int32_t* seg_len;             // [R]
   uint32_t* status;
@@ -71,8 +76,7 @@ struct PlanArgs {
 struct SimArgs {
   const void* emb;              // tiles [n_tiles * kTile][E]
   const float* emb_inv_norm;    // [n_tiles * kTile]
-  const int32_t* user_nfacts;   // [max_users]
-  const int32_t* user_tile_off; // [max_users + 1]
+  const int4* user_meta;        // [max_users] {tile list offset, tiles, facts, first tile or -1}
   const int32_t* user_tiles;    // tiles of each user, in fill order
   const int32_t* users;         // [Q]
   const void* q_emb;            // [Q][E]
@@ -88,19 +92,23 @@ struct TopkArgs {
   const float* scores;
   int64_t score_stride;
   const int32_t* users;
-  const int32_t* user_nfacts;
-  const int32_t* user_tile_off;
+  const int4* user_meta;
   const int32_t* user_tiles;
   const int32_t* tile_fact;     // [n_tiles * kTile] fact id per embedding row
   const int32_t* tile_len;      // [n_tiles * kTile] length of that fact
+  const int64_t* tile_tok;      // [n_tiles * kTile] arena token of that fact
+  const int64_t* fact_tok;
   const int32_t* fact_len;
   const int32_t* seg_start;     // [Q] or null (retrieval only)
   int64_t* ids_out;             // [Q][k]
   float* scores_out;            // [Q][k]
   int32_t* n_ids_out;           // [Q] or null
   int32_t* fact_seg_off;        // [Q][seg_stride] or null
+  int64_t* fact_src;            // [Q][seg_stride] or null
   int32_t seg_stride;
   int32_t* seg_len;             // [Q] or null
+  const int32_t* block_table;   // [Q][max_blocks] or null (prefetched into L2)
+  int32_t max_blocks;
   uint32_t* status;
   int32_t Q;
   int32_t k;
@@ -131,6 +139,20 @@ __device__ __forceinline__ void st_v4(void* ptr, const uint4& v) {
   asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(ptr), "r"(v.x), "r"(v.y),
                "r"(v.z), "r"(v.w)
                : "memory");
+}
+
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
+// Prefetch n int32 entries (one 128-byte line per thread) into L2.
+__device__ __forceinline__ void prefetch_row_l2(const int32_t* p, int n, int tid, int nthreads) {
+  for (int i = tid * 32; i < n; i += nthreads * 32) prefetch_l2(p + i);
+}
+
+// Tile ti of a user: consecutive tiles need no list lookup.
+__device__ __forceinline__ int user_tile(const int32_t* user_tiles, const int4& um, int ti) {
+  return um.w >= 0 ? um.w + ti : user_tiles[um.x + ti];
 }
 
 __device__ __forceinline__ uint4 shfl_xor4(const uint4& v, int mask) {

@@ -31,6 +31,7 @@ __global__ void __launch_bounds__(256) plan_kernel(const PlanArgs a) {
   }
   const int32_t user = a.users ? a.users[r] : -1;
   int32_t* off = a.fact_seg_off + (size_t)r * a.seg_stride;
+  if (a.block_table) prefetch_row_l2(a.block_table + (size_t)r * a.max_blocks, a.max_blocks, threadIdx.x, blockDim.x);
   int32_t carry = 0;
   for (int base = 0; base < n; base += blockDim.x) {
     const int i = base + threadIdx.x;
@@ -43,6 +44,7 @@ __global__ void __launch_bounds__(256) plan_kernel(const PlanArgs a) {
         latch(a.status, IS_ST_FACT_USER);
       } else {
         len = a.fact_len[f];
+        if (a.fact_src) a.fact_src[(size_t)r * a.seg_stride + i] = a.fact_tok[f];
       }
     }
     int32_t tot;
@@ -183,8 +185,9 @@ __global__ void __launch_bounds__(kInjectWarpsMax * 32) inject_kernel(const Inje
         seg_lo = off[jlo];
         seg_hi = off[jlo + 1];
       }
-      const int64_t f = a.ids[(size_t)cur_r * a.ids_stride + cur_j];
-      tok_src = a.fact_tok[f] + (ts - seg_lo);
+      tok_src = (a.fact_src ? a.fact_src[(size_t)cur_r * a.seg_stride + cur_j]
+                            : a.fact_tok[a.ids[(size_t)cur_r * a.ids_stride + cur_j]]) +
+                (ts - seg_lo);
       tok_p = a.seg_start[cur_r] + ts;
       const int32_t lb = tok_p / a.block_size;
       tok_slot = -1;
@@ -521,7 +524,11 @@ extern "C" is_status_t is_inject_noalloc(
   p.seg_start = seg_start;
   p.fact_len = fact_len;
   p.fact_user = nullptr;
+  p.fact_tok = fact_tok;
   p.n_facts = n_facts;
+  p.fact_src = nullptr;
+  p.block_table = block_table;
+  p.max_blocks = max_blocks_per_seq;
   p.n_ids_out = na_n_ids;
   p.fact_seg_off = seg_off;
   p.seg_stride = kNaSegStride;
@@ -539,6 +546,7 @@ extern "C" is_status_t is_inject_noalloc(
   a.n_facts = n_facts;
   a.ids = fact_ids;
   a.ids_stride = ids_stride;
+  a.fact_src = nullptr;
   a.n_ids = na_n_ids;
   a.fact_seg_off = seg_off;
   a.seg_stride = kNaSegStride;

@@ -98,6 +98,7 @@ struct TopkShared {
   uint32_t hist[kCosBins];                  // cosine bins; the radix fallback reuses it as [4][256]
   unsigned long long sel[kCandMax];         // (key << 32) | ((2^20-1 - row) << 10) | slot
   unsigned long long cand[kCandMax];        // (length << 32) | fact id, by slot
+  int32_t len[kCandMax];                    // length by slot (rank path)
   int32_t scratch[33];
   uint32_t wsum[8];
   uint32_t bstar, above, eq, digit, cnt;
@@ -114,9 +115,9 @@ __device__ __forceinline__ unsigned long long sel_entry(uint32_t key, uint32_t r
 }
 
 // Records candidate `slot` = row j of the user: its fact id and length.
-__device__ __forceinline__ void fetch_cand(const TopkArgs& a, TopkShared& sh, int t0, uint32_t j,
+__device__ __forceinline__ void fetch_cand(const TopkArgs& a, TopkShared& sh, const int4& um, uint32_t j,
                                            uint32_t slot) {
-  const int tile = a.user_tiles[t0 + (int)(j / kTile)];
+  const int tile = user_tile(a.user_tiles, um, (int)(j / kTile));
   const size_t row = (size_t)tile * kTile + (j % kTile);
   sh.cand[slot] = ((unsigned long long)(uint32_t)a.tile_len[row] << 32) | (uint32_t)a.tile_fact[row];
 }
@@ -146,12 +147,13 @@ __device__ __forceinline__ void plan_tail(const TopkArgs& a, int q, int nn, int3
 //  D. exact sort of the candidates by (key desc, row asc) and output of the
 //     first k, with the segment plan.
 template <bool SMEM_KEYS>
-__device__ void topk_block(const TopkArgs& a, TopkShared& sh, uint32_t* s_keys, int q, int user, int n) {
+__device__ void topk_block(const TopkArgs& a, TopkShared& sh, uint32_t* s_keys, int q, const int4& um,
+                           int n) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int kk = min(a.k, n);
   const float* sc = a.scores + (size_t)q * a.score_stride;
   auto key_at = [&](int j) -> uint32_t { return SMEM_KEYS ? s_keys[j] : score_key(__ldcg(sc + j)); };
-  const int t0 = n > 0 ? a.user_tile_off[user] : 0;
+  if (a.block_table) prefetch_row_l2(a.block_table + (size_t)q * a.max_blocks, a.max_blocks, tid, kRetThreads);
   int64_t* ids = a.ids_out + (size_t)q * a.k;
   float* scs = a.scores_out + (size_t)q * a.k;
 
@@ -225,10 +227,7 @@ __device__ void topk_block(const TopkArgs& a, TopkShared& sh, uint32_t* s_keys, 
       const uint32_t key = j < n ? key_at(j) : 0u;
       const bool take = j < n && cos_bin(key_score(key)) >= bstar;
       const uint32_t slot = warp_claim(take, &sh.cnt, lane);
-      if (take) {
-        sh.sel[slot] = sel_entry(key, (uint32_t)j, slot);
-        fetch_cand(a, sh, t0, (uint32_t)j, slot);
-      }
+      if (take) sh.sel[slot] = sel_entry(key, (uint32_t)j, slot);
     }
   } else {
     // Radix select: 8 bits per pass finds the k-th largest key thr and how
@@ -288,10 +287,7 @@ __device__ void topk_block(const TopkArgs& a, TopkShared& sh, uint32_t* s_keys, 
       const uint32_t key = j < n ? key_at(j) : 0u;
       const bool gt = j < n && key > thr;
       const uint32_t slot = warp_claim(gt, &sh.cnt, lane);
-      if (gt) {
-        sh.sel[slot] = sel_entry(key, (uint32_t)j, slot);
-        fetch_cand(a, sh, t0, (uint32_t)j, slot);
-      }
+      if (gt) sh.sel[slot] = sel_entry(key, (uint32_t)j, slot);
       // keys == thr in ascending row order, until rem of them are taken
       const int32_t is_eq = (j < n && key == thr) ? 1 : 0;
       int32_t tot;
@@ -299,69 +295,52 @@ __device__ void topk_block(const TopkArgs& a, TopkShared& sh, uint32_t* s_keys, 
       if (is_eq && taken + (uint32_t)rank < rem) {
         const uint32_t slot_eq = n_gt + taken + (uint32_t)rank;
         sh.sel[slot_eq] = sel_entry(key, (uint32_t)j, slot_eq);
-        fetch_cand(a, sh, t0, (uint32_t)j, slot_eq);
       }
       taken += (uint32_t)tot;
     }
   }
   __syncthreads();
 
-  if (C <= 64) {
-    // One warp: bitonic sort of 64 entries in registers (2 per lane), outputs
-    // and the segment plan by warp scan.
-    if (warp == 0) {
-      unsigned long long v[2];
-#pragma unroll
-      for (int h = 0; h < 2; ++h) v[h] = (uint32_t)(2 * lane + h) < C ? sh.sel[2 * lane + h] : 0ull;
-#pragma unroll
-      for (int size = 2; size <= 64; size <<= 1) {
-#pragma unroll
-        for (int stride = size >> 1; stride > 0; stride >>= 1) {
-          if (stride == 1) {
-            const bool desc = ((2 * lane) & size) == 0;
-            const unsigned long long hi = v[0] > v[1] ? v[0] : v[1];
-            const unsigned long long lo = v[0] > v[1] ? v[1] : v[0];
-            v[0] = desc ? hi : lo;
-            v[1] = desc ? lo : hi;
-          } else {
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              const int pos = 2 * lane + h;
-              const unsigned long long o = __shfl_xor_sync(0xffffffffu, v[h], stride >> 1);
-              const bool lower = (pos & stride) == 0;
-              const bool desc = (pos & size) == 0;
-              const unsigned long long hi = v[h] > o ? v[h] : o;
-              const unsigned long long lo = v[h] > o ? o : v[h];
-              v[h] = (lower == desc) ? hi : lo;
-            }
-          }
-        }
-      }
-      int32_t len0 = 0, len1 = 0;
-      if (2 * lane < kk) {
-        const unsigned long long cv = sh.cand[v[0] & 1023u];
-        len0 = (int32_t)(cv >> 32);
-        ids[2 * lane] = (int32_t)(uint32_t)cv;
-        scs[2 * lane] = key_score((uint32_t)(v[0] >> 32));
-      }
-      if (2 * lane + 1 < kk) {
-        const unsigned long long cv = sh.cand[v[1] & 1023u];
-        len1 = (int32_t)(cv >> 32);
-        ids[2 * lane + 1] = (int32_t)(uint32_t)cv;
-        scs[2 * lane + 1] = key_score((uint32_t)(v[1] >> 32));
-      }
+  if (C <= (uint32_t)kRetThreads) {
+    // Rank selection: thread t owns candidate t; its rank is the number of
+    // candidates above it (entries are unique) and its segment offset the sum
+    // of their lengths.  The fact lookup overlaps the first pass.
+    const uint32_t t = (uint32_t)tid;
+    unsigned long long e = 0;
+    int32_t f = 0, len = 0;
+    int64_t tok = 0;
+    uint32_t rank = 0;
+    if (t < C) {
+      e = sh.sel[t];
+      const uint32_t j = 0xFFFFFu - (uint32_t)((e >> 10) & 0xFFFFFu);
+      const int tile = user_tile(a.user_tiles, um, (int)(j / kTile));
+      const size_t row = (size_t)tile * kTile + (j % kTile);
+      f = a.tile_fact[row];
+      len = a.tile_len[row];
+      tok = a.tile_tok[row];
+      for (uint32_t i = 0; i < C; ++i) rank += sh.sel[i] > e ? 1u : 0u;
+      sh.len[t] = len;
+    }
+    __syncthreads();
+    if (t < C && rank < (uint32_t)kk) {
+      int32_t off = 0;
+      for (uint32_t i = 0; i < C; ++i) off += sh.sel[i] > e ? sh.len[i] : 0;
+      ids[rank] = f;
+      scs[rank] = key_score((uint32_t)(e >> 32));
       if (a.fact_seg_off) {
-        uint32_t tot;
-        const uint32_t base = warp_excl_scan((uint32_t)(len0 + len1), lane, &tot);
-        int32_t* off = a.fact_seg_off + (size_t)q * a.seg_stride;
-        if (2 * lane < kk) off[2 * lane] = (int32_t)base;
-        if (2 * lane + 1 < kk) off[2 * lane + 1] = (int32_t)base + len0;
-        if (lane == 0) plan_tail(a, q, kk, (int32_t)tot);
+        a.fact_seg_off[(size_t)q * a.seg_stride + rank] = off;
+        a.fact_src[(size_t)q * a.seg_stride + rank] = tok;
+        if (rank == (uint32_t)kk - 1) plan_tail(a, q, kk, off + len);
       }
     }
     return;
   }
 
+  // More candidates: fetch their fact ids and lengths, then sort.
+  for (uint32_t t = (uint32_t)tid; t < C; t += kRetThreads) {
+    const uint32_t j = 0xFFFFFu - (uint32_t)((sh.sel[t] >> 10) & 0xFFFFFu);
+    fetch_cand(a, sh, um, j, t);
+  }
   // C > 64: bitonic sort in shared memory over the next power of two.
   int P = 1;
   while ((uint32_t)P < C) P <<= 1;
@@ -392,6 +371,7 @@ __device__ void topk_block(const TopkArgs& a, TopkShared& sh, uint32_t* s_keys, 
       len = (int32_t)(cv >> 32);
       ids[r] = (int32_t)(uint32_t)cv;
       scs[r] = key_score((uint32_t)(e >> 32));
+      if (a.fact_src) a.fact_src[(size_t)q * a.seg_stride + r] = a.fact_tok[(int32_t)(uint32_t)cv];
     }
     if (a.fact_seg_off) {
       int32_t tot;
@@ -415,19 +395,19 @@ __global__ void __launch_bounds__(kRetThreads) retrieve_kernel(const SimArgs sa,
   const int sub = blockIdx.x - ti * n_sub;
   const int user = sa.users[q];
   const bool user_ok = user >= 0 && user < sa.max_users;
-  const int t0 = user_ok ? sa.user_tile_off[user] : 0;
-  const int ntiles = user_ok ? sa.user_tile_off[user + 1] - t0 : 0;
+  const int4 um = user_ok ? sa.user_meta[user] : make_int4(0, 0, 0, -1);
+  const int ntiles = um.y;
   if (ntiles == 0) {
     // Unknown user or no facts: CTA x = 0 writes the empty result.
     if (blockIdx.x == 0) {
       if (!user_ok && threadIdx.x == 0) latch(sa.status, IS_ST_USER_RANGE);
-      topk_block<SMEM_KEYS>(ta, sh, s_keys, q, user, 0);
+      topk_block<SMEM_KEYS>(ta, sh, s_keys, q, um, 0);
     }
     return;
   }
   if (ti >= ntiles) return;
-  const int n_u = sa.user_nfacts[user];
-  const int tile = sa.user_tiles[t0 + ti];
+  const int n_u = um.z;
+  const int tile = user_tile(sa.user_tiles, um, ti);
   const int rows_per = kTile / n_sub;
   const int r_begin = sub * rows_per;
   const int r_end = min(r_begin + rows_per, n_u - ti * kTile);
@@ -469,7 +449,7 @@ __global__ void __launch_bounds__(kRetThreads) retrieve_kernel(const SimArgs sa,
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-  topk_block<SMEM_KEYS>(ta, sh, s_keys, q, user, n_u);
+  topk_block<SMEM_KEYS>(ta, sh, s_keys, q, um, n_u);
 }
 
 template <typename E>

@@ -80,9 +80,10 @@ struct is_store {
   float* emb_inv_norm = nullptr;
   int32_t* tile_fact = nullptr;
   int32_t* tile_len = nullptr;    // length of the fact of each embedding row
-  int32_t* user_nfacts = nullptr;
-  int32_t* user_tile_off = nullptr;
+  int4* user_meta = nullptr;      // {tile list offset, tiles, facts, first tile if consecutive else -1}
   int32_t* user_tiles = nullptr;
+  int64_t* tile_tok = nullptr;    // arena token of the fact of each embedding row
+  int64_t* fact_src = nullptr;    // plan: arena token of each planned fact [R][seg_stride]
   float* scores = nullptr;
   int64_t* ids_tmp = nullptr;
   float* scores_tmp = nullptr;
@@ -128,7 +129,7 @@ is_status_t dev_alloc(P** p, size_t bytes, is_store_t* s, const char* what) {
 
 void free_store(is_store_t* s) {
   void* ptrs[] = {s->kv, s->fact_tok, s->fact_len, s->fact_user, s->emb, s->emb_inv_norm,
-                  s->tile_fact, s->tile_len, s->user_nfacts, s->user_tile_off, s->user_tiles, s->scores,
+                  s->tile_fact, s->tile_len, s->user_meta, s->tile_tok, s->fact_src, s->user_tiles, s->scores,
                   s->ids_tmp, s->scores_tmp, s->fact_seg_off, s->n_ids, s->seg_len_tmp,
                   s->rows_tmp, s->status, s->arrive};
   for (void* p : ptrs)
@@ -241,18 +242,20 @@ is_status_t check_cache(const is_store_t* s, const is_cache_desc_t* c, const voi
 
 is_status_t upload_user_index(is_store_t* s, cudaStream_t st) {
   const int U = s->cfg.max_users;
-  std::vector<int32_t> off(U + 1, 0), tiles;
+  std::vector<int4> meta(U);
+  std::vector<int32_t> tiles;
   tiles.reserve(s->n_tiles);
   for (int u = 0; u < U; ++u) {
-    off[u] = (int32_t)tiles.size();
-    tiles.insert(tiles.end(), s->user_tiles_h[u].begin(), s->user_tiles_h[u].end());
+    const std::vector<int32_t>& ut = s->user_tiles_h[u];
+    bool consecutive = !ut.empty();
+    for (size_t i = 1; i < ut.size() && consecutive; ++i) consecutive = ut[i] == ut[i - 1] + 1;
+    meta[u] = make_int4((int32_t)tiles.size(), (int32_t)ut.size(), s->user_nfacts_h[u],
+                        consecutive ? ut[0] : -1);
+    tiles.insert(tiles.end(), ut.begin(), ut.end());
   }
-  off[U] = (int32_t)tiles.size();
-  CUDA_TRY(cudaMemcpyAsync(s->user_tile_off, off.data(), off.size() * 4, cudaMemcpyHostToDevice, st));
+  CUDA_TRY(cudaMemcpyAsync(s->user_meta, meta.data(), meta.size() * sizeof(int4), cudaMemcpyHostToDevice, st));
   if (!tiles.empty())
     CUDA_TRY(cudaMemcpyAsync(s->user_tiles, tiles.data(), tiles.size() * 4, cudaMemcpyHostToDevice, st));
-  CUDA_TRY(cudaMemcpyAsync(s->user_nfacts, s->user_nfacts_h.data(), (size_t)U * 4,
-                           cudaMemcpyHostToDevice, st));
   CUDA_TRY(cudaStreamSynchronize(st));   // host vectors die on return
   return IS_OK;
 }
@@ -362,13 +365,14 @@ is_status_t is_store_create(const is_store_config_t* config, int device, cudaStr
   ALLOC(emb_inv_norm, (size_t)s->max_tiles * kTile * 4, "embedding norms");
   ALLOC(tile_fact, (size_t)s->max_tiles * kTile * 4, "tile fact ids");
   ALLOC(tile_len, (size_t)s->max_tiles * kTile * 4, "tile fact lengths");
-  ALLOC(user_nfacts, (size_t)c.max_users * 4, "user counts");
-  ALLOC(user_tile_off, (size_t)(c.max_users + 1) * 4, "user tile offsets");
+  ALLOC(user_meta, (size_t)c.max_users * sizeof(int4), "user records");
   ALLOC(user_tiles, (size_t)s->max_tiles * 4, "user tiles");
+  ALLOC(tile_tok, (size_t)s->max_tiles * kTile * 8, "tile fact tokens");
   ALLOC(scores, Q * s->score_stride * 4, "score scratch");
   ALLOC(ids_tmp, Q * c.max_k * 8, "id scratch");
   ALLOC(scores_tmp, Q * c.max_k * 4, "top-k score scratch");
   ALLOC(fact_seg_off, R * s->seg_stride * 4, "segment plan");
+  ALLOC(fact_src, R * s->seg_stride * 8, "segment sources");
   ALLOC(n_ids, R * 4, "fact counts");
   ALLOC(seg_len_tmp, R * 4, "segment lengths");
   ALLOC(rows_tmp, (size_t)c.max_facts * 4, "row list");
@@ -378,8 +382,7 @@ is_status_t is_store_create(const is_store_config_t* config, int device, cudaStr
   s->scratch_bytes = (int64_t)(Q * s->score_stride * 4 + Q * c.max_k * 12 +
                                R * (s->seg_stride * 4 + 8) + (size_t)c.max_facts * 4 + 4);
   cudaError_t e = cudaMemsetAsync(s->status, 0, 4, stream);
-  if (e == cudaSuccess) e = cudaMemsetAsync(s->user_tile_off, 0, (size_t)(c.max_users + 1) * 4, stream);
-  if (e == cudaSuccess) e = cudaMemsetAsync(s->user_nfacts, 0, (size_t)c.max_users * 4, stream);
+  if (e == cudaSuccess) e = cudaMemsetAsync(s->user_meta, 0, (size_t)c.max_users * sizeof(int4), stream);
   if (e == cudaSuccess) e = cudaMemsetAsync(s->arrive, 0, Q * 4, stream);
   if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
   if (e != cudaSuccess) {
@@ -490,6 +493,8 @@ is_status_t is_store_add_facts(is_store_t* s, int32_t user, int32_t n, const int
                              cudaMemcpyHostToDevice, stream));
     CUDA_TRY(cudaMemcpyAsync(s->tile_len + rows[i], lengths + i, (size_t)(j - i) * 4,
                              cudaMemcpyHostToDevice, stream));
+    CUDA_TRY(cudaMemcpyAsync(s->tile_tok + rows[i], tok.data() + i, (size_t)(j - i) * 8,
+                             cudaMemcpyHostToDevice, stream));
     i = j;
   }
   CUDA_TRY(cudaMemcpyAsync(s->rows_tmp, rows.data(), (size_t)n * 4, cudaMemcpyHostToDevice, stream));
@@ -530,13 +535,13 @@ static is_status_t check_retrieve(is_store_t* s, int32_t Q, const int32_t* users
 
 static is_status_t run_retrieval(is_store_t* s, int32_t Q, const int32_t* users, const void* q_emb,
                                  int32_t k, int64_t* ids, float* scores, const int32_t* seg_start,
-                                 int32_t* seg_len, cudaStream_t stream) {
+                                 int32_t* seg_len, const int32_t* block_table, int32_t max_blocks,
+                                 cudaStream_t stream) {
   const LaunchCfg cfg{stream, s->num_sms, false};     // first kernel: stream order
   SimArgs sa{};
   sa.emb = s->emb;
   sa.emb_inv_norm = s->emb_inv_norm;
-  sa.user_nfacts = s->user_nfacts;
-  sa.user_tile_off = s->user_tile_off;
+  sa.user_meta = s->user_meta;
   sa.user_tiles = s->user_tiles;
   sa.users = users;
   sa.q_emb = q_emb;
@@ -550,11 +555,15 @@ static is_status_t run_retrieval(is_store_t* s, int32_t Q, const int32_t* users,
   ta.scores = s->scores;
   ta.score_stride = s->score_stride;
   ta.users = users;
-  ta.user_nfacts = s->user_nfacts;
-  ta.user_tile_off = s->user_tile_off;
+  ta.user_meta = s->user_meta;
   ta.user_tiles = s->user_tiles;
   ta.tile_fact = s->tile_fact;
   ta.tile_len = s->tile_len;
+  ta.tile_tok = s->tile_tok;
+  ta.fact_tok = s->fact_tok;
+  ta.fact_src = seg_start ? s->fact_src : nullptr;
+  ta.block_table = block_table;
+  ta.max_blocks = max_blocks;
   ta.fact_len = s->fact_len;
   ta.seg_start = seg_start;
   ta.ids_out = ids;
@@ -581,7 +590,7 @@ is_status_t is_retrieve_topk(is_store_t* s, int32_t Q, const int32_t* users, con
   if (st != IS_OK) return st;
   if (!ids_out || !scores_out) return fail(IS_ERR_INVALID_ARG, "ids_out or scores_out is NULL");
   DeviceGuard g(s->device);
-  return run_retrieval(s, Q, users, q_emb, k, ids_out, scores_out, nullptr, nullptr, stream);
+  return run_retrieval(s, Q, users, q_emb, k, ids_out, scores_out, nullptr, nullptr, nullptr, 0, stream);
 }
 
 static is_status_t check_inject_common(is_store_t* s, int32_t R, const int32_t* seg_start,
@@ -614,6 +623,7 @@ static is_status_t launch_injection(is_store_t* s, int32_t R, const int64_t* ids
   a.n_facts = s->n_facts;
   a.ids = ids;
   a.ids_stride = ids_stride;
+  a.fact_src = s->fact_src;
   a.n_ids = s->n_ids;
   a.fact_seg_off = s->fact_seg_off;
   a.seg_stride = s->seg_stride;
@@ -663,9 +673,13 @@ is_status_t is_inject(is_store_t* s, int32_t R, const int64_t* fact_ids, const i
   p.seg_start = seg_start;
   p.fact_len = s->fact_len;
   p.fact_user = s->fact_user;
+  p.fact_tok = s->fact_tok;
   p.n_facts = s->n_facts;
   p.n_ids_out = s->n_ids;
   p.fact_seg_off = s->fact_seg_off;
+  p.fact_src = s->fact_src;
+  p.block_table = block_table;
+  p.max_blocks = max_blocks;
   p.seg_stride = s->seg_stride;
   p.seg_len = seg_len;
   p.status = s->status;
@@ -694,7 +708,8 @@ is_status_t is_retrieve_and_inject(is_store_t* s, int32_t Q, const int32_t* user
   int64_t* ids = ids_out ? ids_out : s->ids_tmp;
   float* scores = scores_out ? scores_out : s->scores_tmp;
   int32_t* seg_len = seg_len_out ? seg_len_out : s->seg_len_tmp;
-  st = run_retrieval(s, Q, users, q_emb, k, ids, scores, seg_start, seg_len, stream);
+  st = run_retrieval(s, Q, users, q_emb, k, ids, scores, seg_start, seg_len, block_table, max_blocks,
+                     stream);
   if (st != IS_OK) return st;
   return launch_injection(s, Q, ids, k, seg_len, seg_start, rope, block_table, max_blocks, cache,
                           kv_cache, slot_mapping_out, stream);
