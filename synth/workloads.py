@@ -143,6 +143,13 @@ class Workload:
         """Global fact indices of user u, in insertion order."""
         return np.nonzero(self.fact_user == u)[0].astype(np.int64)
 
+    def token_kv(self, f: int, t: int, stream: int) -> np.ndarray:
+        """K (stream 0) or V (stream 1) of token t of fact f: [L][H][D] in storage encoding."""
+        s = self.spec
+        first = (int(self.tok_base[f]) + int(t)) * s.token_elems
+        flat = kvgen.kv_elements(s.seed, stream, first, s.token_elems, s.kv_dtype)
+        return flat.reshape(s.num_layers, s.num_kv_heads, s.head_dim)
+
     def fact_kv(self, f: int, stream: int) -> np.ndarray:
         """K (stream 0) or V (stream 1) of fact f: [len][L][H][D] in storage encoding."""
         s = self.spec

@@ -80,7 +80,8 @@ def check_rotated(g_enc, o_f64, x_f64, style: int, dtype: str) -> dict:
 
 
 class FactCache:
-    """Oracle-side K/V of facts, regenerated from the generator definition."""
+    """Oracle-side K/V, regenerated from the generator definition: whole facts
+    (``cache(f)``) or single tokens (``cache.token(f, t)``)."""
 
     def __init__(self, wl):
         self.wl = wl
@@ -91,6 +92,12 @@ class FactCache:
         if f not in self._m:
             self._m[f] = (self.wl.fact_kv(f, kvgen.STREAM_K), self.wl.fact_kv(f, kvgen.STREAM_V))
         return self._m[f]
+
+    def token(self, f: int, t: int):
+        f, t = int(f), int(t)
+        if f in self._m:
+            return self._m[f][0][t], self._m[f][1][t]
+        return self.wl.token_kv(f, t, kvgen.STREAM_K), self.wl.token_kv(f, t, kvgen.STREAM_V)
 
 
 def oracle_plans(wl, ids_rows):
@@ -110,11 +117,11 @@ def compare_tokens(wl, gathered_k, gathered_v, entries, freqs, style: int, facts
     dtype = wl.spec.kv_dtype
     stats = {"n": 0, "within_1ulp": 0, "floor_only": 0}
     for i, (f, j, p, _) in enumerate(entries):
-        K, V = facts(f)
-        assert np.array_equal(np.asarray(gathered_v[i]).view(np.uint8), V[j].view(np.uint8)), \
+        Kj, Vj = facts.token(f, j)
+        assert np.array_equal(np.asarray(gathered_v[i]).view(np.uint8), Vj.view(np.uint8)), \
             f"V of fact {f} token {j} differs"
-        x = numerics.decode(K[j], dtype)
-        o = oinject.rotated_key_rows(K[j], p, freqs, style, dtype)
+        x = numerics.decode(Kj, dtype)
+        o = oinject.rotated_key_rows(Kj, p, freqs, style, dtype)
         st = check_rotated(gathered_k[i], o, x, style, dtype)
         for key in stats:
             stats[key] += st[key]

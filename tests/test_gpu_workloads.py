@@ -59,7 +59,8 @@ def _check_workload(api, wl, store, k=None, sample_tokens=160, seed=0):
 
 class TestLlama31:
     @pytest.fixture(scope="class")
-    def loaded(self, api):
+    @classmethod
+    def loaded(cls, api):
         wl = workloads.get("llama31_8b")
         store = staging.load_store(wl, api)
         yield wl, store
@@ -82,7 +83,8 @@ class TestLlama31:
 
 class TestMistralKSweep:
     @pytest.fixture(scope="class")
-    def loaded(self, api):
+    @classmethod
+    def loaded(cls, api):
         wl = workloads.get("mistral_7b")
         store = staging.load_store(wl, api)
         yield wl, store
@@ -97,7 +99,8 @@ class TestMistralKSweep:
 
 class TestQwen100Users:
     @pytest.fixture(scope="class")
-    def loaded(self, api):
+    @classmethod
+    def loaded(cls, api):
         wl = workloads.get("qwen25_7b_100u")
         store = staging.load_store(wl, api)
         yield wl, store
@@ -112,7 +115,8 @@ class TestQwen100Users:
 @pytest.mark.slow
 class TestCapacity:
     @pytest.fixture(scope="class")
-    def loaded(self, api):
+    @classmethod
+    def loaded(cls, api):
         wl = workloads.get("capacity")
         store = staging.load_store(wl, api, chunk_bytes=4 << 30)
         yield wl, store
