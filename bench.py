@@ -186,6 +186,8 @@ def run_ours(args, rank, world, local_rank):
     overrides = {"seed": rank_seed(spec.seed, rank)}
     if args.facts:
         overrides["facts_per_user"] = args.facts
+    if args.layers:
+        overrides["num_layers"] = args.layers
     if args.k:
         overrides["k"] = args.k
         overrides["tokens_cap"] = args.k * int(spec.length_dist[2] if spec.length_dist[0] == "uniform"
@@ -483,6 +485,8 @@ def main(argv=None):
     ap.add_argument("--k", type=int, default=0)
     ap.add_argument("--facts", type=int, default=0,
                     help="facts per user (smaller store for profiling captures)")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="model layers (smaller K/V for profiling the retrieval kernels)")
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     args = ap.parse_args(argv)

@@ -261,6 +261,23 @@ is_status_t is_inject_noalloc(const void* kv_arena, const int64_t* fact_tok,
                               void* kv_cache, int32_t* seg_len_out, int64_t* slot_mapping_out,
                               uint32_t* status_out, cudaStream_t stream);
 
+/* ---- is_set_retrieval_mode -----------------------------------------------------
+ * How the similarity is computed.  IS_RETRIEVAL_PER_QUERY: one launch in
+ * which each query's CTAs stream its user's embedding tiles and the last CTA
+ * of the query selects its top-k (best when each user has one query in the
+ * call).  IS_RETRIEVAL_BATCHED: queries are grouped by user (up to 64 per
+ * group) and each (group, 128-row tile) is one tensor-core contraction
+ * (tcgen05, fp16 operands, fp32 accumulation), then one top-k CTA per query
+ * (best when a user has many queries in the call: the tile is read once for
+ * all of them).  IS_RETRIEVAL_AUTO (default): batched when Q >= 32 and the
+ * largest user holds >= 1024 facts.  Results are the same up to the order of
+ * fp32 accumulation.  Errors: IS_ERR_UNSUPPORTED for the batched mode with
+ * fp32 embeddings. */
+#define IS_RETRIEVAL_AUTO      0
+#define IS_RETRIEVAL_PER_QUERY 1
+#define IS_RETRIEVAL_BATCHED   2
+is_status_t is_set_retrieval_mode(is_store_t* store, int32_t mode);
+
 /* ---- status / diagnostics ---------------------------------------------------
  * is_get_status: synchronise `stream`, read the device status word into
  * *bits_out and clear it.  Returns IS_ERR_DEVICE if any bit was set,

@@ -18,6 +18,7 @@ IS_ST_USER_RANGE, IS_ST_POSITION, IS_ST_COUNT, IS_ST_TIMEOUT = 0x10, 0x20, 0x40,
 IS_STAGE_SIMILARITY, IS_STAGE_TOPK, IS_STAGE_PLAN, IS_STAGE_INJECT = 0, 1, 2, 3
 IS_MAX_K, IS_MAX_QUERIES, IS_MAX_REQUESTS, IS_EMB_TILE = 1024, 1024, 4096, 128
 IS_NOALLOC_MAX_REQUESTS, IS_NOALLOC_MAX_FACTS = 256, 256
+IS_RETRIEVAL_AUTO, IS_RETRIEVAL_PER_QUERY, IS_RETRIEVAL_BATCHED = 0, 1, 2
 
 
 class StoreConfig(ctypes.Structure):
@@ -67,6 +68,7 @@ SIGNATURES = {
     "is_last_error_message": [],
     "is_status_string": [c_int],
     "is_rope_frequencies": [POINTER(RopeParams), c_int32, POINTER(c_double)],
+    "is_set_retrieval_mode": [c_void_p, c_int32],
     "is_set_timing": [c_void_p, c_int32],
     "is_get_timing": [c_void_p, c_int32, POINTER(c_double), POINTER(c_int64)],
     "is_reset_timing": [c_void_p],

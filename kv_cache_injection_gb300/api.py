@@ -172,6 +172,10 @@ def is_rope_frequencies(rope: RopeParams, head_dim: int) -> np.ndarray:
     return out
 
 
+def is_set_retrieval_mode(store: Store, mode: int) -> None:
+    _check(_lib.load().is_set_retrieval_mode(c_void_p(store.handle), int(mode)))
+
+
 def is_set_timing(store: Store, enable: bool) -> None:
     _check(_lib.load().is_set_timing(c_void_p(store.handle), 1 if enable else 0))
 

@@ -115,6 +115,37 @@ struct TopkArgs {
   int32_t max_users;
 };
 
+// Grouping of a retrieval call's queries by user (batched path).
+struct GroupArgs {
+  const int32_t* users;         // [Q]
+  const void* q_emb;            // [Q][E] fp16
+  int32_t Q;
+  int32_t E;
+  const int4* user_meta;
+  int32_t max_users;
+  __half* qg;                   // [max_queries][E] queries in group order
+  float* q_inv;                 // [max_queries] their inverse norms
+  int32_t* qperm;               // packed position -> caller's query index
+  int4* groups;                 // [max_queries] {user, first position, count, first work item}
+  int32_t* counts;              // {groups, work items}
+  uint32_t* status;
+};
+
+// The tensor-core contraction of the batched path.
+struct GemmArgs {
+  const int4* groups;
+  const int32_t* counts;
+  const int32_t* qperm;
+  const float* q_inv;
+  const int4* user_meta;
+  const int32_t* user_tiles;
+  const float* emb_inv_norm;
+  float* scores;                // [Q][score_stride], indexed by the caller's query
+  int64_t score_stride;
+  int32_t E;
+  uint32_t* status;
+};
+
 // ------------------------------------------------------------------ device helpers
 
 __device__ __forceinline__ void latch(uint32_t* status, uint32_t bits) { atomicOr(status, bits); }

@@ -47,6 +47,16 @@ cudaError_t launch_retrieve(const SimArgs& sa, const TopkArgs& ta, int emb_dtype
 
 cudaError_t launch_plan(const PlanArgs& a, const LaunchCfg& cfg);
 
+// Batched retrieval (tensor cores): tensor maps of the embedding tiles and of
+// the packed queries, and the three launches (grouping, contraction, top-k).
+size_t operand_map_bytes();
+bool make_operand_map(void* map_out, const void* base, int E, int64_t rows, int box_rows);
+cudaError_t launch_group(const GroupArgs& ga, const LaunchCfg& cfg);
+cudaError_t launch_sim_gemm(const GemmArgs& gg, const void* map_emb, const void* map_q, int Q,
+                            int max_user_tiles, const LaunchCfg& cfg);
+cudaError_t launch_topk_batched(const TopkArgs& ta, int Q, int32_t max_users, int64_t max_user_facts,
+                                const LaunchCfg& cfg);
+
 // Persistent launch: one CTA per SM times the occupancy its shared-memory
 // plan allows.
 cudaError_t launch_inject(const InjectArgs& a, const RopeTurns& turns, int kv_dtype, int style,

@@ -93,6 +93,16 @@ struct is_store {
   int32_t* rows_tmp = nullptr;
   uint32_t* status = nullptr;
   int32_t* arrive = nullptr;      // per-query arrival counters of the retrieval kernel
+  // batched (tensor-core) retrieval
+  __half* qg = nullptr;           // [max_queries][E] queries packed in group order
+  float* q_inv = nullptr;
+  int32_t* qperm = nullptr;
+  int4* groups = nullptr;
+  int32_t* counts = nullptr;
+  alignas(64) unsigned char map_emb[128];
+  alignas(64) unsigned char map_q[128];
+  bool batched_ok = false;
+  int32_t retrieval_mode = IS_RETRIEVAL_AUTO;
   int64_t scratch_bytes = 0;
 
   int64_t n_facts = 0, n_tokens = 0;
@@ -131,7 +141,7 @@ void free_store(is_store_t* s) {
   void* ptrs[] = {s->kv, s->fact_tok, s->fact_len, s->fact_user, s->emb, s->emb_inv_norm,
                   s->tile_fact, s->tile_len, s->user_meta, s->tile_tok, s->fact_src, s->user_tiles, s->scores,
                   s->ids_tmp, s->scores_tmp, s->fact_seg_off, s->n_ids, s->seg_len_tmp,
-                  s->rows_tmp, s->status, s->arrive};
+                  s->rows_tmp, s->status, s->arrive, s->qg, s->q_inv, s->qperm, s->groups, s->counts};
   for (void* p : ptrs)
     if (p) cudaFree(p);
   for (int st = 0; st < IS_NUM_STAGES; ++st)
@@ -378,6 +388,11 @@ is_status_t is_store_create(const is_store_config_t* config, int device, cudaStr
   ALLOC(rows_tmp, (size_t)c.max_facts * 4, "row list");
   ALLOC(status, 4, "status word");
   ALLOC(arrive, Q * 4, "arrival counters");
+  ALLOC(qg, Q * (size_t)c.emb_dim * 2, "packed queries");
+  ALLOC(q_inv, Q * 4, "query norms");
+  ALLOC(qperm, Q * 4, "query order");
+  ALLOC(groups, Q * sizeof(int4), "query groups");
+  ALLOC(counts, 8, "group counts");
 #undef ALLOC
   s->scratch_bytes = (int64_t)(Q * s->score_stride * 4 + Q * c.max_k * 12 +
                                R * (s->seg_stride * 4 + 8) + (size_t)c.max_facts * 4 + 4);
@@ -389,6 +404,10 @@ is_status_t is_store_create(const is_store_config_t* config, int device, cudaStr
     free_store(s);
     return fail(IS_ERR_CUDA, "store initialisation failed: %s", cudaGetErrorString(e));
   }
+  // Tensor maps for the batched path (fp16 embeddings only).
+  if (c.emb_dtype == IS_F16 && operand_map_bytes() <= sizeof(s->map_emb))
+    s->batched_ok = make_operand_map(s->map_emb, s->emb, c.emb_dim, s->max_tiles * kTile, 128) &&
+                    make_operand_map(s->map_q, s->qg, c.emb_dim, (int64_t)Q, 64);
   *out = s;
   return IS_OK;
 }
@@ -551,6 +570,9 @@ static is_status_t run_retrieval(is_store_t* s, int32_t Q, const int32_t* users,
   sa.Q = Q;
   sa.E = s->cfg.emb_dim;
   sa.max_users = s->cfg.max_users;
+  const bool batched = s->batched_ok &&
+                       (s->retrieval_mode == IS_RETRIEVAL_BATCHED ||
+                        (s->retrieval_mode == IS_RETRIEVAL_AUTO && Q >= 32 && s->max_user_facts >= 1024));
   TopkArgs ta{};
   ta.scores = s->scores;
   ta.score_stride = s->score_stride;
@@ -576,10 +598,49 @@ static is_status_t run_retrieval(is_store_t* s, int32_t Q, const int32_t* users,
   ta.Q = Q;
   ta.k = k;
   ta.max_users = s->cfg.max_users;
-  {
+  if (!batched) {
     StageTimer tm(s, IS_STAGE_SIMILARITY, stream);
     CUDA_TRY(launch_retrieve(sa, ta, s->cfg.emb_dtype, s->max_user_tiles, s->max_user_facts, s->arrive,
                              cfg));
+    return IS_OK;
+  }
+  GroupArgs ga{};
+  ga.users = users;
+  ga.q_emb = q_emb;
+  ga.Q = Q;
+  ga.E = s->cfg.emb_dim;
+  ga.user_meta = s->user_meta;
+  ga.max_users = s->cfg.max_users;
+  ga.qg = s->qg;
+  ga.q_inv = s->q_inv;
+  ga.qperm = s->qperm;
+  ga.groups = s->groups;
+  ga.counts = s->counts;
+  ga.status = s->status;
+  GemmArgs gg{};
+  gg.groups = s->groups;
+  gg.counts = s->counts;
+  gg.qperm = s->qperm;
+  gg.q_inv = s->q_inv;
+  gg.user_meta = s->user_meta;
+  gg.user_tiles = s->user_tiles;
+  gg.emb_inv_norm = s->emb_inv_norm;
+  gg.scores = s->scores;
+  gg.score_stride = s->score_stride;
+  gg.E = s->cfg.emb_dim;
+  gg.status = s->status;
+  const LaunchCfg dep{stream, s->num_sms, true};
+  {
+    StageTimer tm(s, IS_STAGE_PLAN, stream);
+    CUDA_TRY(launch_group(ga, cfg));
+  }
+  {
+    StageTimer tm(s, IS_STAGE_SIMILARITY, stream);
+    CUDA_TRY(launch_sim_gemm(gg, s->map_emb, s->map_q, Q, s->max_user_tiles, dep));
+  }
+  {
+    StageTimer tm(s, IS_STAGE_TOPK, stream);
+    CUDA_TRY(launch_topk_batched(ta, Q, s->cfg.max_users, s->max_user_facts, dep));
   }
   return IS_OK;
 }
@@ -725,6 +786,16 @@ is_status_t is_get_status(is_store_t* s, cudaStream_t stream, uint32_t* bits_out
   *bits_out = bits;
   if (bits & IS_ST_TIMEOUT) return fail(IS_ERR_TIMEOUT, "a device wait timed out (bits 0x%x)", bits);
   if (bits) return fail(IS_ERR_DEVICE, "device status bits 0x%x", bits);
+  return IS_OK;
+}
+
+is_status_t is_set_retrieval_mode(is_store_t* s, int32_t mode) {
+  if (!s) return fail(IS_ERR_INVALID_ARG, "NULL store");
+  if (mode != IS_RETRIEVAL_AUTO && mode != IS_RETRIEVAL_PER_QUERY && mode != IS_RETRIEVAL_BATCHED)
+    return fail(IS_ERR_INVALID_ARG, "unknown retrieval mode %d", mode);
+  if (mode == IS_RETRIEVAL_BATCHED && !s->batched_ok)
+    return fail(IS_ERR_UNSUPPORTED, "the batched path needs fp16 embeddings and tensor maps");
+  s->retrieval_mode = mode;
   return IS_OK;
 }
 
