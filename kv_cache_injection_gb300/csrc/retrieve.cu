@@ -78,6 +78,9 @@ __global__ void __launch_bounds__(kRetThreads) retrieve_kernel(const SimArgs sa,
   const int q = blockIdx.y;
   const int ti = blockIdx.x / n_sub;
   const int sub = blockIdx.x - ti * n_sub;
+  // The query row does not depend on the user lookup: start pulling it into L2.
+  if (threadIdx.x * 128 < sa.E * (int)sizeof(E))
+    prefetch_l2(reinterpret_cast<const uint8_t*>(sa.q_emb) + ((size_t)q * sa.E * sizeof(E)) + threadIdx.x * 128);
   const int user = sa.users[q];
   const bool user_ok = user >= 0 && user < sa.max_users;
   const int4 um = user_ok ? sa.user_meta[user] : make_int4(0, 0, 0, -1);
@@ -101,6 +104,14 @@ __global__ void __launch_bounds__(kRetThreads) retrieve_kernel(const SimArgs sa,
   const E* qv = reinterpret_cast<const E*>(sa.q_emb) + (size_t)q * sa.E;
   const E* base = reinterpret_cast<const E*>(sa.emb) + (size_t)tile * kTile * sa.E;
   float* out = sa.scores + (size_t)q * sa.score_stride + (size_t)ti * kTile;
+  // The top-k will look up the fact, length and arena token of its candidate
+  // rows: warm those lines of this CTA's rows now.
+  if (threadIdx.x < 3 && r_begin < r_end) {
+    const size_t row0 = (size_t)tile * kTile + r_begin;
+    const void* p = threadIdx.x == 0 ? (const void*)(ta.tile_fact + row0)
+                  : threadIdx.x == 1 ? (const void*)(ta.tile_len + row0) : (const void*)(ta.tile_tok + row0);
+    prefetch_l2(p);
+  }
   for (int r = r_begin + warp; r < r_end; r += kRetThreads / 32) {
     const float inv_e = sa.emb_inv_norm[(size_t)tile * kTile + r];
     const E* row = base + (size_t)r * sa.E;
@@ -121,10 +132,12 @@ __global__ void __launch_bounds__(kRetThreads) retrieve_kernel(const SimArgs sa,
       dot += __shfl_xor_sync(0xffffffffu, dot, o);
       qq += __shfl_xor_sync(0xffffffffu, qq, o);
     }
-    if (lane == 0) out[r] = dot * (qq > 0.f ? 1.0f / sqrtf(qq) : 0.f) * inv_e;
+    if (lane == 0) {
+      out[r] = dot * (qq > 0.f ? 1.0f / sqrtf(qq) : 0.f) * inv_e;
+      __threadfence();                          // the score before the arrival below
+    }
   }
   // Arrive; the last CTA of query q runs its top-k.
-  __threadfence();
   __syncthreads();
   if (threadIdx.x == 0) {
     const int done = atomicAdd(&arrive[q], 1);
