@@ -211,6 +211,29 @@ is_status_t is_inject(is_store_t* store, int32_t R, const int64_t* fact_ids,
                       const is_cache_desc_t* cache, void* kv_cache, int32_t* seg_len_out,
                       int64_t* slot_mapping_out, cudaStream_t stream);
 
+/* ---- is_inject_layer --------------------------------------------------------
+ * is_inject for one layer, into that layer's own cache tensor
+ * layer_cache [2][num_blocks][block_size][H][D] (K at [0], V at [1]), so an
+ * engine can inject layer l while it works on another layer: the pages
+ * integrate through vLLM's KV-connector interface ("Méthodologie"), which
+ * saves and loads KV layer by layer.
+ *   fact_ids != NULL   plan the segments (as is_inject) and inject `layer`;
+ *   fact_ids == NULL   reuse the segment plan of the store's previous
+ *                      is_inject, is_inject_layer or is_retrieve_and_inject
+ *                      call, which must have had the same R (n_ids, users and
+ *                      ids_stride are then ignored); the plan stays valid
+ *                      until the next planning call on the store.
+ * seg_start and block_table must be the ones the plan was made with.
+ * slot_mapping_out (if given) is written again for this call.  Errors as
+ * is_inject, plus IS_ERR_OUT_OF_RANGE for a bad layer and
+ * IS_ERR_INVALID_ARG when there is no plan of R requests to reuse. */
+is_status_t is_inject_layer(is_store_t* store, int32_t layer, int32_t R, const int64_t* fact_ids,
+                            const int32_t* n_ids, int32_t ids_stride, const int32_t* users,
+                            const int32_t* seg_start, const is_rope_params_t* rope,
+                            const int32_t* block_table, int32_t max_blocks_per_seq,
+                            const is_cache_desc_t* cache, void* layer_cache, int32_t* seg_len_out,
+                            int64_t* slot_mapping_out, cudaStream_t stream);
+
 /* ---- is_retrieve_and_inject -------------------------------------------------
  * is_retrieve_topk followed by is_inject of each query's k facts in
  * descending-score order, with no host synchronisation between the stages

@@ -57,6 +57,9 @@ SIGNATURES = {
     "is_inject": [c_void_p, c_int32, c_void_p, c_void_p, c_int32, c_void_p, c_void_p,
                   POINTER(RopeParams), c_void_p, c_int32, POINTER(CacheDesc), c_void_p, c_void_p,
                   c_void_p, c_void_p],
+    "is_inject_layer": [c_void_p, c_int32, c_int32, c_void_p, c_void_p, c_int32, c_void_p, c_void_p,
+                        POINTER(RopeParams), c_void_p, c_int32, POINTER(CacheDesc), c_void_p,
+                        c_void_p, c_void_p, c_void_p],
     "is_retrieve_and_inject": [c_void_p, c_int32, c_void_p, c_void_p, c_int32, c_void_p,
                                POINTER(RopeParams), c_void_p, c_int32, POINTER(CacheDesc),
                                c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p],

@@ -130,6 +130,17 @@ def is_inject(store: Store, fact_ids, n_ids, seg_start, rope: RopeParams, block_
         _ptr(kv_cache), _ptr(seg_len_out), _ptr(slot_mapping_out), _stream(stream)))
 
 
+def is_inject_layer(store: Store, layer: int, R: int, seg_start, rope: RopeParams, block_table,
+                    cache: CacheDesc, layer_cache, fact_ids=None, n_ids=None, users=None,
+                    seg_len_out=None, slot_mapping_out=None, stream=None) -> None:
+    """One layer into its own cache tensor; fact_ids=None reuses the last plan."""
+    stride = int(fact_ids.shape[1]) if fact_ids is not None else 0
+    _check(_lib.load().is_inject_layer(
+        c_void_p(store.handle), int(layer), int(R), _ptr(fact_ids), _ptr(n_ids), stride, _ptr(users),
+        _ptr(seg_start), byref(rope), _ptr(block_table), int(block_table.shape[1]), byref(cache),
+        _ptr(layer_cache), _ptr(seg_len_out), _ptr(slot_mapping_out), _stream(stream)))
+
+
 def is_retrieve_and_inject(store: Store, users, q_emb, k: int, seg_start, rope: RopeParams,
                            block_table, cache: CacheDesc, kv_cache, ids_out=None, scores_out=None,
                            seg_len_out=None, slot_mapping_out=None, stream=None) -> None:

@@ -45,7 +45,10 @@ struct InjectArgs {
   int64_t* slot_mapping;        // [sum seg_len] or null
   uint32_t* status;
   int32_t R;
-  int32_t L;
+  int32_t L;                    // layers of the store
+  int32_t layer0;               // first layer this call injects
+  int32_t n_layers;             // layers this call injects
+  int64_t layer_stride;         // bytes between consecutive layers of the destination cache
   int32_t row_bytes;            // H * D * elt
   int32_t half_vecs;            // NeoX: 16-byte vectors per half head (D / 2 / VE)
   int32_t head_vecs;            // 16-byte vectors per head (D / VE)

@@ -131,7 +131,7 @@ __global__ void __launch_bounds__(kInjectWarpsMax * 32) inject_kernel(const Inje
     __syncthreads();
   }
 
-  const int64_t n_items = (int64_t)total * a.L;
+  const int64_t n_items = (int64_t)total * a.n_layers;
   const int64_t warp_id = (int64_t)blockIdx.x * nwarps + warp;
   const int64_t n_warps = (int64_t)gridDim.x * nwarps;
   const int64_t chunk = (n_items + n_warps - 1) / n_warps;
@@ -158,8 +158,8 @@ __global__ void __launch_bounds__(kInjectWarpsMax * 32) inject_kernel(const Inje
   // Warp-uniform: resolve item j's token (request, fact, position, slot) and
   // have lane 0 start its bulk load into stage s.  Returns true if a load was issued.
   auto issue = [&](int64_t j, int s) -> bool {
-    const int32_t t = (int32_t)(j / a.L);
-    const int32_t l = (int32_t)(j - (int64_t)t * a.L);
+    const int32_t t = (int32_t)(j / a.n_layers);
+    const int32_t l = (int32_t)(j - (int64_t)t * a.n_layers);   // layer within this call
     if (t != cur_t) {
       cur_t = t;
       int lo = 0, hi = a.R;
@@ -211,7 +211,7 @@ __global__ void __launch_bounds__(kInjectWarpsMax * 32) inject_kernel(const Inje
         const uint32_t bar = smem_addr(&bars[s]);
         mbar_expect_tx(bar, item_bytes);
         bulk_load(stage0 + (uint32_t)s * item_bytes,
-                  a.kv + ((size_t)tok_src * a.L + l) * 2 * (size_t)a.row_bytes, item_bytes, bar);
+                  a.kv + ((size_t)tok_src * a.L + a.layer0 + l) * 2 * (size_t)a.row_bytes, item_bytes, bar);
       }
     }
     return tok_slot >= 0;
@@ -249,8 +249,8 @@ __global__ void __launch_bounds__(kInjectWarpsMax * 32) inject_kernel(const Inje
         }
       }
       const uint32_t kst = stage0 + (uint32_t)s * item_bytes;
-      uint8_t* dk = a.cache + ((size_t)(2 * m.l) * a.num_blocks * a.block_size + m.slot) * a.row_bytes;
-      uint8_t* dv = a.cache + ((size_t)(2 * m.l + 1) * a.num_blocks * a.block_size + m.slot) * a.row_bytes;
+      uint8_t* dk = a.cache + (size_t)m.l * a.layer_stride + (size_t)m.slot * a.row_bytes;
+      uint8_t* dv = dk + (size_t)a.num_blocks * a.block_size * a.row_bytes;
       if (lane == 0) bulk_store(dv, kst + a.row_bytes, a.row_bytes);
       for (int c = 0; c < vpl; ++c) {
         const int v = c * 32 + lane;
@@ -561,6 +561,9 @@ extern "C" is_status_t is_inject_noalloc(
   a.status = status_out;
   a.R = R;
   a.L = num_layers;
+  a.layer0 = 0;
+  a.n_layers = num_layers;
+  a.layer_stride = 2LL * cache->num_blocks * cache->block_size * row_bytes;
   a.row_bytes = (int32_t)row_bytes;
   a.half_vecs = head_dim / 2 / ve;
   a.head_vecs = head_dim / ve;

@@ -103,6 +103,9 @@ struct is_store {
   alignas(64) unsigned char map_q[128];
   bool batched_ok = false;
   int32_t retrieval_mode = IS_RETRIEVAL_AUTO;
+  // segment plan of the last injecting call (reused by is_inject_layer)
+  int32_t plan_R = 0;
+  const int32_t* plan_seg_len = nullptr;
   int64_t scratch_bytes = 0;
 
   int64_t n_facts = 0, n_tokens = 0;
@@ -671,11 +674,14 @@ static is_status_t check_inject_common(is_store_t* s, int32_t R, const int32_t* 
   return IS_OK;
 }
 
+// Layers [layer0, layer0 + n_layers) into a cache whose consecutive layers are
+// layer_stride bytes apart (kv_cache points at layer layer0's K block).
 static is_status_t launch_injection(is_store_t* s, int32_t R, const int64_t* ids, int32_t ids_stride,
                                     const int32_t* seg_len, const int32_t* seg_start,
                                     const is_rope_params_t* rope, const int32_t* block_table,
                                     int32_t max_blocks, const is_cache_desc_t* cache, void* kv_cache,
-                                    int64_t* slot_mapping, cudaStream_t stream) {
+                                    int64_t* slot_mapping, cudaStream_t stream, int32_t layer0,
+                                    int32_t n_layers, int64_t layer_stride) {
   InjectArgs a{};
   a.kv = s->kv;
   a.fact_tok = s->fact_tok;
@@ -699,6 +705,9 @@ static is_status_t launch_injection(is_store_t* s, int32_t R, const int64_t* ids
   a.status = s->status;
   a.R = R;
   a.L = s->cfg.num_layers;
+  a.layer0 = layer0;
+  a.n_layers = n_layers;
+  a.layer_stride = layer_stride;
   a.row_bytes = (int32_t)s->row_bytes;
   const int ve = 16 / s->elt;
   a.half_vecs = s->cfg.head_dim / 2 / ve;
@@ -710,22 +719,10 @@ static is_status_t launch_injection(is_store_t* s, int32_t R, const int64_t* ids
   return IS_OK;
 }
 
-is_status_t is_inject(is_store_t* s, int32_t R, const int64_t* fact_ids, const int32_t* n_ids,
-                      int32_t ids_stride, const int32_t* users, const int32_t* seg_start,
-                      const is_rope_params_t* rope, const int32_t* block_table, int32_t max_blocks,
-                      const is_cache_desc_t* cache, void* kv_cache, int32_t* seg_len_out,
-                      int64_t* slot_mapping_out, cudaStream_t stream) {
-  if (!s) return fail(IS_ERR_INVALID_ARG, "NULL store");
-  if (R < 1 || R > s->cfg.max_requests)
-    return fail(IS_ERR_INVALID_ARG, "R=%d outside [1, %d]", R, s->cfg.max_requests);
-  if (ids_stride < 1 || ids_stride > s->cfg.max_k)
-    return fail(IS_ERR_OUT_OF_RANGE, "ids_stride=%d outside [1, %d]", ids_stride, s->cfg.max_k);
-  if (!fact_ids || !n_ids) return fail(IS_ERR_INVALID_ARG, "fact_ids or n_ids is NULL");
-  is_status_t st = check_inject_common(s, R, seg_start, rope, block_table, max_blocks, cache, kv_cache,
-                                       ids_stride);
-  if (st != IS_OK) return st;
-  DeviceGuard g(s->device);
-  int32_t* seg_len = seg_len_out ? seg_len_out : s->seg_len_tmp;
+// Arguments of the planning kernel for an explicit fact list.
+static PlanArgs make_plan_args(is_store_t* s, int32_t R, const int64_t* fact_ids, const int32_t* n_ids,
+                               int32_t ids_stride, const int32_t* users, const int32_t* seg_start,
+                               const int32_t* block_table, int32_t max_blocks, int32_t* seg_len) {
   PlanArgs p{};
   p.ids = fact_ids;
   p.ids_stride = ids_stride;
@@ -745,12 +742,76 @@ is_status_t is_inject(is_store_t* s, int32_t R, const int64_t* fact_ids, const i
   p.seg_len = seg_len;
   p.status = s->status;
   p.R = R;
+  return p;
+}
+
+is_status_t is_inject(is_store_t* s, int32_t R, const int64_t* fact_ids, const int32_t* n_ids,
+                      int32_t ids_stride, const int32_t* users, const int32_t* seg_start,
+                      const is_rope_params_t* rope, const int32_t* block_table, int32_t max_blocks,
+                      const is_cache_desc_t* cache, void* kv_cache, int32_t* seg_len_out,
+                      int64_t* slot_mapping_out, cudaStream_t stream) {
+  if (!s) return fail(IS_ERR_INVALID_ARG, "NULL store");
+  if (R < 1 || R > s->cfg.max_requests)
+    return fail(IS_ERR_INVALID_ARG, "R=%d outside [1, %d]", R, s->cfg.max_requests);
+  if (ids_stride < 1 || ids_stride > s->cfg.max_k)
+    return fail(IS_ERR_OUT_OF_RANGE, "ids_stride=%d outside [1, %d]", ids_stride, s->cfg.max_k);
+  if (!fact_ids || !n_ids) return fail(IS_ERR_INVALID_ARG, "fact_ids or n_ids is NULL");
+  is_status_t st = check_inject_common(s, R, seg_start, rope, block_table, max_blocks, cache, kv_cache,
+                                       ids_stride);
+  if (st != IS_OK) return st;
+  DeviceGuard g(s->device);
+  int32_t* seg_len = seg_len_out ? seg_len_out : s->seg_len_tmp;
+  const PlanArgs p = make_plan_args(s, R, fact_ids, n_ids, ids_stride, users, seg_start, block_table,
+                                    max_blocks, seg_len);
   {
     StageTimer tm(s, IS_STAGE_PLAN, stream);
     CUDA_TRY(launch_plan(p, LaunchCfg{stream, s->num_sms, false}));
   }
+  s->plan_R = R;
+  s->plan_seg_len = seg_len;
   return launch_injection(s, R, fact_ids, ids_stride, seg_len, seg_start, rope, block_table, max_blocks,
-                          cache, kv_cache, slot_mapping_out, stream);
+                          cache, kv_cache, slot_mapping_out, stream, 0, s->cfg.num_layers,
+                          2LL * cache->num_blocks * cache->block_size * s->row_bytes);
+}
+
+is_status_t is_inject_layer(is_store_t* s, int32_t layer, int32_t R, const int64_t* fact_ids,
+                            const int32_t* n_ids, int32_t ids_stride, const int32_t* users,
+                            const int32_t* seg_start, const is_rope_params_t* rope,
+                            const int32_t* block_table, int32_t max_blocks, const is_cache_desc_t* cache,
+                            void* layer_cache, int32_t* seg_len_out, int64_t* slot_mapping_out,
+                            cudaStream_t stream) {
+  if (!s) return fail(IS_ERR_INVALID_ARG, "NULL store");
+  if (layer < 0 || layer >= s->cfg.num_layers)
+    return fail(IS_ERR_OUT_OF_RANGE, "layer %d outside [0, %d)", layer, s->cfg.num_layers);
+  if (R < 1 || R > s->cfg.max_requests)
+    return fail(IS_ERR_INVALID_ARG, "R=%d outside [1, %d]", R, s->cfg.max_requests);
+  const int32_t stride_for_bound = fact_ids ? ids_stride : s->cfg.max_k;
+  is_status_t st = check_inject_common(s, R, seg_start, rope, block_table, max_blocks, cache, layer_cache,
+                                       stride_for_bound);
+  if (st != IS_OK) return st;
+  DeviceGuard g(s->device);
+  const int32_t* seg_len = nullptr;
+  if (fact_ids) {
+    if (ids_stride < 1 || ids_stride > s->cfg.max_k)
+      return fail(IS_ERR_OUT_OF_RANGE, "ids_stride=%d outside [1, %d]", ids_stride, s->cfg.max_k);
+    if (!n_ids) return fail(IS_ERR_INVALID_ARG, "n_ids is NULL");
+    int32_t* out = seg_len_out ? seg_len_out : s->seg_len_tmp;
+    const PlanArgs p = make_plan_args(s, R, fact_ids, n_ids, ids_stride, users, seg_start, block_table,
+                                      max_blocks, out);
+    {
+      StageTimer tm(s, IS_STAGE_PLAN, stream);
+      CUDA_TRY(launch_plan(p, LaunchCfg{stream, s->num_sms, false}));
+    }
+    s->plan_R = R;
+    s->plan_seg_len = out;
+    seg_len = out;
+  } else {
+    if (s->plan_R != R || !s->plan_seg_len)
+      return fail(IS_ERR_INVALID_ARG, "no segment plan of %d requests to reuse", R);
+    seg_len = s->plan_seg_len;
+  }
+  return launch_injection(s, R, nullptr, 0, seg_len, seg_start, rope, block_table, max_blocks, cache,
+                          layer_cache, slot_mapping_out, stream, layer, 1, 0);
 }
 
 is_status_t is_retrieve_and_inject(is_store_t* s, int32_t Q, const int32_t* users, const void* q_emb,
@@ -772,8 +833,11 @@ is_status_t is_retrieve_and_inject(is_store_t* s, int32_t Q, const int32_t* user
   st = run_retrieval(s, Q, users, q_emb, k, ids, scores, seg_start, seg_len, block_table, max_blocks,
                      stream);
   if (st != IS_OK) return st;
+  s->plan_R = Q;
+  s->plan_seg_len = seg_len;
   return launch_injection(s, Q, ids, k, seg_len, seg_start, rope, block_table, max_blocks, cache,
-                          kv_cache, slot_mapping_out, stream);
+                          kv_cache, slot_mapping_out, stream, 0, s->cfg.num_layers,
+                          2LL * cache->num_blocks * cache->block_size * s->row_bytes);
 }
 
 is_status_t is_get_status(is_store_t* s, cudaStream_t stream, uint32_t* bits_out) {
