@@ -79,6 +79,15 @@ typedef enum {
 
 typedef enum { IS_F32 = 0, IS_BF16 = 1, IS_F16 = 2 } is_dtype_t;
 
+/* Where the store's K/V arena lives (is_store_config_t.kv_placement).
+ * InferScale ("Résultats", Scalabilité) offloads the KV store to host DRAM to go past the
+ * GPU's memory capacity, at a small cost in time to first token; the retrieval
+ * index stays on the GPU.  IS_KV_HOST: the arena is page-locked host memory
+ * mapped into the device's address space; the injection kernel reads the
+ * selected rows over the CPU-GPU link itself, so no call synchronises with the
+ * host and the control flow is unchanged. */
+typedef enum { IS_KV_DEVICE = 0, IS_KV_HOST = 1 } is_kv_placement_t;
+
 typedef struct is_store is_store_t;   /* opaque */
 
 /* Store capacity and model KV shape.  Fields set to 0 take the default noted. */
@@ -96,6 +105,8 @@ typedef struct {
   int32_t max_k;             /* retrieval budget / facts per request, <= IS_MAX_K (0: 256) */
   int32_t max_requests;      /* per injection call, <= IS_MAX_REQUESTS (0: max_queries) */
   int64_t max_facts_per_user;/* sizes the score scratch (0: max_facts), <= IS_MAX_FACTS_PER_USER */
+  int32_t kv_placement;      /* is_kv_placement_t (0: IS_KV_DEVICE) */
+  int32_t reserved;          /* must be 0 */
 } is_store_config_t;
 
 /* Rotary embedding of the model the facts were encoded with. */
@@ -124,6 +135,7 @@ typedef struct {
   int64_t max_user_facts;
   int64_t kv_bytes, emb_bytes, scratch_bytes;
   int32_t num_sms;
+  int32_t kv_placement;      /* is_kv_placement_t of the arena */
 } is_store_info_t;
 
 /* ---- store ------------------------------------------------------------------
@@ -132,10 +144,12 @@ typedef struct {
  * per-fact metadata and all per-call scratch, so that no later call
  * allocates device memory.  InferScale keeps precomputed per-fact KV and a
  * semantic embedding GPU-resident (abstract; "Conception de Système Native
- * au GPU").  Synchronous.  Errors: IS_ERR_INVALID_ARG (bad config),
- * IS_ERR_UNSUPPORTED (head_dim / row size the kernels do not handle),
- * IS_ERR_OOM, IS_ERR_CUDA.  *out is owned by the caller; free with
- * is_store_destroy. */
+ * au GPU").  With kv_placement = IS_KV_HOST the arena alone is page-locked
+ * host memory instead (is_kv_placement_t); everything else stays on the
+ * device.  Synchronous.  Errors: IS_ERR_INVALID_ARG (bad config),
+ * IS_ERR_UNSUPPORTED (head_dim / row size the kernels do not handle, or a
+ * device that cannot map host memory), IS_ERR_OOM, IS_ERR_CUDA.  *out is owned
+ * by the caller; free with is_store_destroy. */
 is_status_t is_store_create(const is_store_config_t* config, int device, cudaStream_t stream,
                             is_store_t** out);
 

@@ -19,6 +19,7 @@ IS_STAGE_SIMILARITY, IS_STAGE_TOPK, IS_STAGE_PLAN, IS_STAGE_INJECT = 0, 1, 2, 3
 IS_MAX_K, IS_MAX_QUERIES, IS_MAX_REQUESTS, IS_EMB_TILE = 1024, 1024, 4096, 128
 IS_NOALLOC_MAX_REQUESTS, IS_NOALLOC_MAX_FACTS = 256, 256
 IS_RETRIEVAL_AUTO, IS_RETRIEVAL_PER_QUERY, IS_RETRIEVAL_BATCHED = 0, 1, 2
+IS_KV_DEVICE, IS_KV_HOST = 0, 1
 
 
 class StoreConfig(ctypes.Structure):
@@ -26,7 +27,7 @@ class StoreConfig(ctypes.Structure):
                 ("emb_dim", c_int32), ("kv_dtype", c_int32), ("emb_dtype", c_int32),
                 ("max_facts", c_int64), ("max_tokens", c_int64), ("max_users", c_int32),
                 ("max_queries", c_int32), ("max_k", c_int32), ("max_requests", c_int32),
-                ("max_facts_per_user", c_int64)]
+                ("max_facts_per_user", c_int64), ("kv_placement", c_int32), ("reserved", c_int32)]
 
 
 class RopeParams(ctypes.Structure):
@@ -42,7 +43,8 @@ class CacheDesc(ctypes.Structure):
 class StoreInfo(ctypes.Structure):
     _fields_ = [("n_facts", c_int64), ("n_tokens", c_int64), ("n_tiles", c_int32),
                 ("max_user_tiles", c_int32), ("max_user_facts", c_int64), ("kv_bytes", c_int64),
-                ("emb_bytes", c_int64), ("scratch_bytes", c_int64), ("num_sms", c_int32)]
+                ("emb_bytes", c_int64), ("scratch_bytes", c_int64), ("num_sms", c_int32),
+                ("kv_placement", c_int32)]
 
 
 # name -> argtypes (restype is is_status_t unless listed in _RESTYPES)

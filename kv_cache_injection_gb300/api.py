@@ -73,6 +73,8 @@ def make_config(**kw) -> StoreConfig:
     for k, v in kw.items():
         if k in ("kv_dtype", "emb_dtype") and isinstance(v, str):
             v = DTYPE_CODES[v]
+        elif k == "kv_placement" and isinstance(v, str):
+            v = {"device": 0, "host": 1}[v]
         setattr(c, k, int(v))
     return c
 

@@ -92,6 +92,78 @@ struct StageMeta {
   int32_t l;        // layer
 };
 
+// Exclusive prefix of seg_len over the R requests into s_off[0..R] (shared
+// memory); returns the total token count.  All threads of the block call it.
+__device__ __forceinline__ int32_t segment_prefix(const InjectArgs& a, int32_t* s_off, int32_t* scratch) {
+  int32_t total = 0;
+  const int per = (a.R + blockDim.x - 1) / blockDim.x;
+  const int b = min(a.R, (int)threadIdx.x * per);
+  const int e = min(a.R, b + per);
+  int32_t sum = 0;
+  for (int i = b; i < e; ++i) sum += a.seg_len[i];
+  int32_t base = block_exclusive_scan(sum, scratch, &total);
+  for (int i = b; i < e; ++i) {
+    s_off[i] = base;
+    base += a.seg_len[i];
+  }
+  if (threadIdx.x == 0) s_off[a.R] = total;
+  __syncthreads();
+  return total;
+}
+
+// Warp-uniform walk from a composed-segment token t (all requests back to
+// back) to its store token, serving position and destination slot.  Tokens a
+// warp visits are consecutive, so the request and fact found last time are
+// kept and searched again only when t leaves them.
+struct TokenCursor {
+  int32_t t = -1, r = -1, j = 0, lo = 0, hi = 0;
+  int64_t src = 0;    // store token
+  int64_t slot = -1;  // cache slot, -1 if the block table rejects the position
+  int32_t p = 0;      // position in the request's sequence
+
+  __device__ __forceinline__ void seek(const InjectArgs& a, const int32_t* s_off, int32_t tt, int lane) {
+    if (tt == t) return;
+    t = tt;
+    int rlo = 0, rhi = a.R;
+    while (rhi - rlo > 1) {
+      const int mid = (rlo + rhi) >> 1;
+      if (s_off[mid] <= tt) rlo = mid; else rhi = mid;
+    }
+    const int32_t ts = tt - s_off[rlo];
+    if (rlo != r || ts < lo || ts >= hi) {
+      const int32_t* off = a.fact_seg_off + (size_t)rlo * a.seg_stride;
+      int jlo = 0, jhi = a.n_ids[rlo];
+      while (jhi - jlo > 1) {
+        const int stride = (jhi - jlo + 31) >> 5;
+        const int idx = jlo + lane * stride;
+        const bool le = idx < jhi && off[idx] <= ts;
+        const unsigned m = __ballot_sync(0xffffffffu, le);
+        jlo += (31 - __clz(m)) * stride;
+        jhi = min(jhi, jlo + stride);
+      }
+      r = rlo;
+      j = jlo;
+      lo = off[jlo];
+      hi = off[jlo + 1];
+    }
+    src = (a.fact_src ? a.fact_src[(size_t)r * a.seg_stride + j]
+                      : a.fact_tok[a.ids[(size_t)r * a.ids_stride + j]]) + (ts - lo);
+    p = a.seg_start[r] + ts;
+    const int32_t lb = p / a.block_size;
+    slot = -1;
+    if (lb >= a.max_blocks) {
+      if (lane == 0) latch(a.status, IS_ST_BLOCK_TABLE);
+    } else {
+      const int32_t blk = a.block_table[(size_t)r * a.max_blocks + lb];
+      if (blk < 0 || blk >= a.num_blocks) {
+        if (lane == 0) latch(a.status, IS_ST_BLOCK_ID);
+      } else {
+        slot = (int64_t)blk * a.block_size + (p - lb * a.block_size);
+      }
+    }
+  }
+};
+
 template <typename T, int STYLE>
 __global__ void __launch_bounds__(kInjectWarpsMax * 32) inject_kernel(const InjectArgs a,
                                                                       const RopeTurns rt, int P) {
@@ -114,22 +186,7 @@ __global__ void __launch_bounds__(kInjectWarpsMax * 32) inject_kernel(const Inje
   StageMeta* meta = reinterpret_cast<StageMeta*>(smem + off_bytes + (size_t)nwarps * P * item_bytes +
                                                  (size_t)nwarps * P * 8) + (size_t)warp * P;
 
-  // Exclusive prefix of seg_len over requests.
-  int32_t total = 0;
-  {
-    const int per = (a.R + blockDim.x - 1) / blockDim.x;
-    const int b = min(a.R, (int)threadIdx.x * per);
-    const int e = min(a.R, b + per);
-    int32_t sum = 0;
-    for (int i = b; i < e; ++i) sum += a.seg_len[i];
-    int32_t base = block_exclusive_scan(sum, scratch, &total);
-    for (int i = b; i < e; ++i) {
-      s_off[i] = base;
-      base += a.seg_len[i];
-    }
-    if (threadIdx.x == 0) s_off[a.R] = total;
-    __syncthreads();
-  }
+  const int32_t total = segment_prefix(a, s_off, scratch);
 
   const int64_t n_items = (int64_t)total * a.n_layers;
   const int64_t warp_id = (int64_t)blockIdx.x * nwarps + warp;
@@ -150,58 +207,17 @@ __global__ void __launch_bounds__(kInjectWarpsMax * 32) inject_kernel(const Inje
   const int hv = a.half_vecs;
   const int fbase = STYLE == 0 ? (lane % hv) * VE : (lane % a.head_vecs) * (VE / 2);
 
-  // Issue-side token cache.
-  int32_t cur_t = -1, cur_r = -1, cur_j = 0, seg_lo = 0, seg_hi = 0;
-  int64_t tok_src = 0, tok_slot = -1;
-  int32_t tok_p = 0;
+  TokenCursor cur;
 
-  // Warp-uniform: resolve item j's token (request, fact, position, slot) and
-  // have lane 0 start its bulk load into stage s.  Returns true if a load was issued.
+  // Warp-uniform: resolve item j's token and have lane 0 start its bulk load
+  // into stage s.  Returns true if a load was issued.
   auto issue = [&](int64_t j, int s) -> bool {
     const int32_t t = (int32_t)(j / a.n_layers);
     const int32_t l = (int32_t)(j - (int64_t)t * a.n_layers);   // layer within this call
-    if (t != cur_t) {
-      cur_t = t;
-      int lo = 0, hi = a.R;
-      while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (s_off[mid] <= t) lo = mid; else hi = mid;
-      }
-      const int r = lo;
-      const int32_t ts = t - s_off[r];
-      if (r != cur_r || ts < seg_lo || ts >= seg_hi) {
-        const int32_t* off = a.fact_seg_off + (size_t)r * a.seg_stride;
-        int jlo = 0, jhi = a.n_ids[r];
-        while (jhi - jlo > 1) {
-          const int stride = (jhi - jlo + 31) >> 5;
-          const int idx = jlo + lane * stride;
-          const bool le = idx < jhi && off[idx] <= ts;
-          const unsigned m = __ballot_sync(0xffffffffu, le);
-          jlo += (31 - __clz(m)) * stride;
-          jhi = min(jhi, jlo + stride);
-        }
-        cur_r = r;
-        cur_j = jlo;
-        seg_lo = off[jlo];
-        seg_hi = off[jlo + 1];
-      }
-      tok_src = (a.fact_src ? a.fact_src[(size_t)cur_r * a.seg_stride + cur_j]
-                            : a.fact_tok[a.ids[(size_t)cur_r * a.ids_stride + cur_j]]) +
-                (ts - seg_lo);
-      tok_p = a.seg_start[cur_r] + ts;
-      const int32_t lb = tok_p / a.block_size;
-      tok_slot = -1;
-      if (lb >= a.max_blocks) {
-        if (lane == 0) latch(a.status, IS_ST_BLOCK_TABLE);
-      } else {
-        const int32_t blk = a.block_table[(size_t)cur_r * a.max_blocks + lb];
-        if (blk < 0 || blk >= a.num_blocks) {
-          if (lane == 0) latch(a.status, IS_ST_BLOCK_ID);
-        } else {
-          tok_slot = (int64_t)blk * a.block_size + (tok_p - lb * a.block_size);
-        }
-      }
-    }
+    cur.seek(a, s_off, t, lane);
+    const int64_t tok_slot = cur.slot;
+    const int32_t tok_p = cur.p;
+    const int64_t tok_src = cur.src;
     if (lane == 0) {
       if (l == 0 && a.slot_mapping) a.slot_mapping[t] = tok_slot;
       meta[s].slot = tok_slot;
@@ -306,6 +322,106 @@ __global__ void __launch_bounds__(kInjectWarpsMax * 32) inject_kernel(const Inje
 }
 
 // ---------------------------------------------------------------------------
+// The same gather + rotation + scatter for a store kept in host memory mapped
+// into the device's address space (InferScale, "Résultats", Scalabilité: the KV store
+// offloaded to host DRAM).  The rows come over the CPU-GPU link through
+// ordinary 16-byte loads straight into registers: each lane issues the loads
+// of up to kHostChunk vectors of the K row and of the V row before using any,
+// and dozens of warps per SM keep enough bytes in flight to cover the link's
+// latency.  A NeoX partner vector v ^ half_vecs sits in lane lane ^ half_vecs
+// (a shuffle) or, when a half head is exactly 32 vectors, in the neighbouring
+// register of the same lane.  No waits: nothing here can stall unboundedly.
+constexpr int kHostWarps = 8;
+constexpr int kHostChunk = 4;
+
+// Plain 16-byte global load: valid for device memory and for mapped host memory.
+__device__ __forceinline__ uint4 ld_plain(const uint8_t* p) { return *reinterpret_cast<const uint4*>(p); }
+
+template <typename T, int STYLE>
+__global__ void __launch_bounds__(kHostWarps * 32) inject_host_kernel(const InjectArgs a,
+                                                                      const RopeTurns rt) {
+  extern __shared__ __align__(16) int32_t s_off[];   // [R + 1]
+  __shared__ int32_t scratch[33];
+  constexpr int VE = Vec<T>::N;
+  constexpr int NF = STYLE == 0 ? VE : VE / 2;
+
+  pdl_wait();                                   // outputs of the planning kernel
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int32_t total = segment_prefix(a, s_off, scratch);
+  const int64_t n_items = (int64_t)total * a.n_layers;
+  const int64_t n_warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+  const int64_t chunk = (n_items + n_warps - 1) / n_warps;
+  const int64_t it0 = ((int64_t)blockIdx.x * (blockDim.x >> 5) + warp) * chunk;
+  const int64_t it_end = min(n_items, it0 + chunk);
+
+  const int vpl = a.row_bytes >> 9;
+  const int hv = a.half_vecs;
+  const int fbase = STYLE == 0 ? (lane % hv) * VE : (lane % a.head_vecs) * (VE / 2);
+  const size_t plane = (size_t)a.num_blocks * a.block_size * a.row_bytes;
+  TokenCursor cur;
+  float cs[NF], sn[NF];
+  int32_t cur_p = -1;
+  for (int64_t i = it0; i < it_end; ++i) {
+    const int32_t t = (int32_t)(i / a.n_layers);
+    const int32_t l = (int32_t)(i - (int64_t)t * a.n_layers);
+    cur.seek(a, s_off, t, lane);
+    if (l == 0 && lane == 0 && a.slot_mapping) a.slot_mapping[t] = cur.slot;
+    if (cur.slot < 0) continue;
+    if (cur.p != cur_p) {
+      cur_p = cur.p;
+      const float pf = (float)cur_p;
+#pragma unroll
+      for (int e = 0; e < NF; ++e) {
+        const float fr = angle_turns(pf, rt.hi[fbase + e], rt.lo[fbase + e]);
+        sincospif(2.0f * fr, &sn[e], &cs[e]);
+      }
+    }
+    const uint8_t* src = a.kv + ((size_t)cur.src * a.L + a.layer0 + l) * 2 * (size_t)a.row_bytes;
+    uint8_t* dk = a.cache + (size_t)l * a.layer_stride + (size_t)cur.slot * a.row_bytes;
+    uint8_t* dv = dk + plane;
+    for (int c0 = 0; c0 < vpl; c0 += kHostChunk) {
+      uint4 kx[kHostChunk], vx[kHostChunk];
+#pragma unroll
+      for (int c = 0; c < kHostChunk; ++c)
+        if (c0 + c < vpl) {
+          const size_t o = (size_t)((c0 + c) * 32 + lane) * 16;
+          kx[c] = ld_plain(src + o);
+          vx[c] = ld_plain(src + a.row_bytes + o);
+        }
+#pragma unroll
+      for (int c = 0; c < kHostChunk; ++c)
+        if (c0 + c < vpl) {                     // warp-uniform
+          const int v = (c0 + c) * 32 + lane;
+          st_v4(dv + (size_t)v * 16, vx[c]);
+          float x[VE], y[VE];
+          Vec<T>::unpack(kx[c], x);
+          if (STYLE == 0) {
+            float z[VE];
+            Vec<T>::unpack(hv < 32 ? shfl_xor4(kx[c], hv) : kx[c ^ 1], z);
+            if ((v & hv) == 0) {
+#pragma unroll
+              for (int e = 0; e < VE; ++e) y[e] = fmaf(x[e], cs[e], -z[e] * sn[e]);
+            } else {
+#pragma unroll
+              for (int e = 0; e < VE; ++e) y[e] = fmaf(x[e], cs[e], z[e] * sn[e]);
+            }
+          } else {
+#pragma unroll
+            for (int e = 0; e < VE / 2; ++e) {
+              const float u = x[2 * e], w = x[2 * e + 1];
+              y[2 * e] = fmaf(u, cs[e], -w * sn[e]);
+              y[2 * e + 1] = fmaf(w, cs[e], u * sn[e]);
+            }
+          }
+          st_v4(dk + (size_t)v * 16, Vec<T>::pack(y));
+        }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
 
 cudaError_t launch_plan(const PlanArgs& a, const LaunchCfg& cfg) {
   return launch_ex(plan_kernel, dim3(a.R), dim3(256), 0, cfg.stream, cfg.pdl, a);
@@ -365,7 +481,7 @@ struct LaunchMemo {
 };
 static std::mutex g_launch_mu;
 
-template <typename T, int STYLE>
+template <typename T, int STYLE, bool HOST>
 static LaunchMemo& launch_memo(int dev) {
   static LaunchMemo memo[64];
   return memo[dev & 63];
@@ -382,7 +498,7 @@ static cudaError_t launch_inject_t(const InjectArgs& a, const RopeTurns& rt, con
   int per_sm = 0;
   {
     std::lock_guard<std::mutex> lock(g_launch_mu);
-    LaunchMemo& m = launch_memo<T, STYLE>(dev);
+    LaunchMemo& m = launch_memo<T, STYLE, false>(dev);
     if (sh.smem > m.smem_set) {
       e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sh.smem);
       if (e != cudaSuccess) return e;
@@ -400,14 +516,45 @@ static cudaError_t launch_inject_t(const InjectArgs& a, const RopeTurns& rt, con
                    cfg.stream, cfg.pdl, a, rt, sh.stages);
 }
 
+template <typename T, int STYLE>
+static cudaError_t launch_inject_host_t(const InjectArgs& a, const RopeTurns& rt, const LaunchCfg& cfg) {
+  auto kern = inject_host_kernel<T, STYLE>;
+  const size_t smem = (size_t)(a.R + 1) * 4;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  int per_sm = 0;
+  {
+    std::lock_guard<std::mutex> lock(g_launch_mu);
+    LaunchMemo& m = launch_memo<T, STYLE, true>(dev);
+    if (m.occ_smem != smem || m.occ_warps != kHostWarps) {
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&m.occ_blocks, kern, kHostWarps * 32, smem);
+      if (e != cudaSuccess) return e;
+      m.occ_smem = smem;
+      m.occ_warps = kHostWarps;
+    }
+    per_sm = m.occ_blocks;
+  }
+  return launch_ex(kern, dim3(cfg.num_sms * std::max(1, per_sm)), dim3(kHostWarps * 32), smem,
+                   cfg.stream, cfg.pdl, a, rt);
+}
+
+template <typename T, int STYLE>
+static cudaError_t launch_inject_any(const InjectArgs& a, const RopeTurns& rt, bool host_src,
+                                     const LaunchCfg& cfg) {
+  return host_src ? launch_inject_host_t<T, STYLE>(a, rt, cfg) : launch_inject_t<T, STYLE>(a, rt, cfg);
+}
+
 cudaError_t launch_inject(const InjectArgs& a, const RopeTurns& rt, int kv_dtype, int style,
-                          const LaunchCfg& cfg) {
+                          bool host_src, const LaunchCfg& cfg) {
   if (kv_dtype == IS_BF16)
-    return style == 0 ? launch_inject_t<__nv_bfloat16, 0>(a, rt, cfg)
-                      : launch_inject_t<__nv_bfloat16, 1>(a, rt, cfg);
+    return style == 0 ? launch_inject_any<__nv_bfloat16, 0>(a, rt, host_src, cfg)
+                      : launch_inject_any<__nv_bfloat16, 1>(a, rt, host_src, cfg);
   if (kv_dtype == IS_F16)
-    return style == 0 ? launch_inject_t<__half, 0>(a, rt, cfg) : launch_inject_t<__half, 1>(a, rt, cfg);
-  return style == 0 ? launch_inject_t<float, 0>(a, rt, cfg) : launch_inject_t<float, 1>(a, rt, cfg);
+    return style == 0 ? launch_inject_any<__half, 0>(a, rt, host_src, cfg)
+                      : launch_inject_any<__half, 1>(a, rt, host_src, cfg);
+  return style == 0 ? launch_inject_any<float, 0>(a, rt, host_src, cfg)
+                    : launch_inject_any<float, 1>(a, rt, host_src, cfg);
 }
 
 bool inject_shape_ok(int row_bytes, int R) {
@@ -576,7 +723,7 @@ extern "C" is_status_t is_inject_noalloc(
     rt.lo[i] = (float)(turns - (double)rt.hi[i]);
   }
   const LaunchCfg cfg_dep{stream, d.num_sms, true};
-  if (launch_inject(a, rt, kv_dtype, rope->style, cfg_dep) != cudaSuccess)
+  if (launch_inject(a, rt, kv_dtype, rope->style, false, cfg_dep) != cudaSuccess)
     return na_fail(IS_ERR_CUDA, "inject launch failed");
   return IS_OK;
 }

@@ -58,9 +58,10 @@ cudaError_t launch_topk_batched(const TopkArgs& ta, int Q, int32_t max_users, in
                                 const LaunchCfg& cfg);
 
 // Persistent launch: one CTA per SM times the occupancy its shared-memory
-// plan allows.
+// plan allows.  host_src: the arena a.kv is mapped host memory, read with
+// plain loads instead of bulk copies.
 cudaError_t launch_inject(const InjectArgs& a, const RopeTurns& turns, int kv_dtype, int style,
-                          const LaunchCfg& cfg);
+                          bool host_src, const LaunchCfg& cfg);
 
 // Whether a row of row_bytes (K or V of one layer) and R requests fit the
 // inject kernel's shared-memory plan.

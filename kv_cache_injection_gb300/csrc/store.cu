@@ -127,7 +127,7 @@ struct is_store {
 namespace {
 
 template <typename P>
-is_status_t dev_alloc(P** p, size_t bytes, is_store_t* s, const char* what) {
+is_status_t dev_alloc(P** p, size_t bytes, const char* what) {
   void* v = nullptr;
   cudaError_t e = cudaMalloc(&v, bytes > 0 ? bytes : 16);
   if (e != cudaSuccess) {
@@ -136,11 +136,35 @@ is_status_t dev_alloc(P** p, size_t bytes, is_store_t* s, const char* what) {
                 cudaGetErrorString(e));
   }
   *p = static_cast<P*>(v);
-  if (s) s->scratch_bytes += 0;
+  return IS_OK;
+}
+
+// Page-locked host memory for the arena, mapped into the device's address
+// space; *p is the device-side address (equal to the host one under UVA).
+is_status_t host_alloc(uint8_t** p, size_t bytes) {
+  void* h = nullptr;
+  cudaError_t e = cudaHostAlloc(&h, bytes > 0 ? bytes : 16, cudaHostAllocMapped | cudaHostAllocPortable);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return fail(IS_ERR_OOM, "cudaHostAlloc(%zu bytes) for the host K/V arena failed: %s", bytes,
+                cudaGetErrorString(e));
+  }
+  void* d = nullptr;
+  e = cudaHostGetDevicePointer(&d, h, 0);
+  if (e != cudaSuccess || d != h) {
+    cudaGetLastError();
+    cudaFreeHost(h);
+    return fail(IS_ERR_UNSUPPORTED, "host K/V arena is not mapped at its host address");
+  }
+  *p = static_cast<uint8_t*>(d);
   return IS_OK;
 }
 
 void free_store(is_store_t* s) {
+  if (s->kv && s->cfg.kv_placement == IS_KV_HOST) {
+    cudaFreeHost(s->kv);
+    s->kv = nullptr;
+  }
   void* ptrs[] = {s->kv, s->fact_tok, s->fact_len, s->fact_user, s->emb, s->emb_inv_norm,
                   s->tile_fact, s->tile_len, s->user_meta, s->tile_tok, s->fact_src, s->user_tiles, s->scores,
                   s->ids_tmp, s->scores_tmp, s->fact_seg_off, s->n_ids, s->seg_len_tmp,
@@ -330,6 +354,9 @@ is_status_t is_store_create(const is_store_config_t* config, int device, cudaStr
   if (c.max_k < 1 || c.max_k > IS_MAX_K) return fail(IS_ERR_INVALID_ARG, "max_k must be in [1, %d]", IS_MAX_K);
   if (c.max_requests < 1 || c.max_requests > IS_MAX_REQUESTS)
     return fail(IS_ERR_INVALID_ARG, "max_requests must be in [1, %d]", IS_MAX_REQUESTS);
+  if (c.kv_placement != IS_KV_DEVICE && c.kv_placement != IS_KV_HOST)
+    return fail(IS_ERR_INVALID_ARG, "kv_placement must be IS_KV_DEVICE or IS_KV_HOST");
+  if (c.reserved != 0) return fail(IS_ERR_INVALID_ARG, "reserved config field must be 0");
   if (c.emb_dim % 8 != 0) return fail(IS_ERR_UNSUPPORTED, "emb_dim must be a multiple of 8");
   const int D = c.head_dim;
   if (!is_pow2(D) || D < 16 || D > IS_MAX_HEAD_DIM)
@@ -348,6 +375,11 @@ is_status_t is_store_create(const is_store_config_t* config, int device, cudaStr
   }
   if (device < 0 || device >= ndev) return fail(IS_ERR_INVALID_ARG, "device %d out of range", device);
   DeviceGuard g(device);
+  if (c.kv_placement == IS_KV_HOST) {
+    int can_map = 0;
+    cudaDeviceGetAttribute(&can_map, cudaDevAttrCanMapHostMemory, device);
+    if (!can_map) return fail(IS_ERR_UNSUPPORTED, "device %d cannot map host memory", device);
+  }
 
   is_store_t* s = new is_store_t();
   s->cfg = c;
@@ -366,11 +398,18 @@ is_status_t is_store_create(const is_store_config_t* config, int device, cudaStr
   is_status_t st = IS_OK;
   const size_t Q = c.max_queries, R = std::max(c.max_requests, c.max_queries);
 #define ALLOC(ptr, bytes, what)                              \
-  if ((st = dev_alloc(&s->ptr, (bytes), s, what)) != IS_OK) { \
+  if ((st = dev_alloc(&s->ptr, (bytes), what)) != IS_OK) {    \
     free_store(s);                                           \
     return st;                                               \
   }
-  ALLOC(kv, (size_t)c.max_tokens * s->tok_bytes, "K/V arena");
+  if (c.kv_placement == IS_KV_HOST) {
+    if ((st = host_alloc(&s->kv, (size_t)c.max_tokens * s->tok_bytes)) != IS_OK) {
+      free_store(s);
+      return st;
+    }
+  } else {
+    ALLOC(kv, (size_t)c.max_tokens * s->tok_bytes, "K/V arena");
+  }
   ALLOC(fact_tok, (size_t)c.max_facts * 8, "fact offsets");
   ALLOC(fact_len, (size_t)c.max_facts * 4, "fact lengths");
   ALLOC(fact_user, (size_t)c.max_facts * 4, "fact users");
@@ -434,6 +473,7 @@ is_status_t is_store_info(const is_store_t* s, is_store_info_t* out) {
   out->emb_bytes = s->max_tiles * kTile * s->cfg.emb_dim * s->emb_elt;
   out->scratch_bytes = s->scratch_bytes;
   out->num_sms = s->num_sms;
+  out->kv_placement = s->cfg.kv_placement;
   return IS_OK;
 }
 
@@ -715,7 +755,7 @@ static is_status_t launch_injection(is_store_t* s, int32_t R, const int64_t* ids
   const RopeTurns rt = make_turns(*rope, s->cfg.head_dim);
   const LaunchCfg cfg{stream, s->num_sms, true};      // follows the planning kernel
   StageTimer tm(s, IS_STAGE_INJECT, stream);
-  CUDA_TRY(launch_inject(a, rt, s->cfg.kv_dtype, rope->style, cfg));
+  CUDA_TRY(launch_inject(a, rt, s->cfg.kv_dtype, rope->style, s->cfg.kv_placement == IS_KV_HOST, cfg));
   return IS_OK;
 }
 

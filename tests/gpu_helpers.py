@@ -5,6 +5,7 @@ import numpy as np
 
 from synth import staging
 from synth.workloads import CANARY_BITS
+from tests import parity
 
 
 def ensure_built():
@@ -65,3 +66,38 @@ def assert_only_slots_changed(cache, dtype: str, slots) -> None:
     exp[np.asarray(slots, dtype=np.int64)] = True
     assert np.array_equal(ch, np.broadcast_to(exp, ch.shape)), \
         f"{int((ch != exp).sum())} cache rows differ from the expected set"
+
+
+def check_fused_workload(api, wl, store, k=None, sample_tokens=160, seed=0):
+    """Fused retrieve + inject of ``wl`` through ``store`` against the oracle:
+    every top-k, segment length and slot; a sample of injected tokens; and
+    that exactly the targeted cache rows changed.  Returns the cache too."""
+    inp = staging.device_inputs(wl)
+    cache = staging.canary_cache(wl)
+    k = wl.spec.k if k is None else k
+    out = run_fused(api, store, wl, inp, cache, k=k)
+    assert out["status"] == 0, hex(out["status"])
+    swapped = 0
+    for q in range(wl.spec.n_queries):
+        o_ids, o_sc, score_of = parity.oracle_retrieve(wl, q, k)
+        swapped += parity.check_topk(out["ids"][q], out["scores"][q], o_ids, o_sc, score_of, k)["swapped"]
+    plans, lens = parity.oracle_plans(wl, out["ids"])
+    assert np.array_equal(out["seg_len"], lens)
+    want_slots = np.concatenate([[e[3] for e in pl] for pl in plans]).astype(np.int64)
+    assert np.array_equal(out["slot_map"][: len(want_slots)], want_slots)
+    assert len(np.unique(want_slots)) == len(want_slots)
+    assert_only_slots_changed(cache, wl.spec.kv_dtype, want_slots)
+    # sampled tokens: first and last token of every segment, plus random ones
+    entries = [e for pl in plans for e in pl]
+    rng = np.random.default_rng(seed)
+    pick = set(rng.choice(len(entries), size=min(sample_tokens, len(entries)), replace=False).tolist())
+    off = 0
+    for pl in plans:
+        if pl:
+            pick.update([off, off + len(pl) - 1])
+        off += len(pl)
+    sample = [entries[i] for i in sorted(pick)]
+    gk, gv = gather_rows(cache, [e[3] for e in sample])
+    stats = parity.compare_tokens(wl, gk, gv, sample, parity.oracle_freqs(wl), wl.spec.rope.style,
+                                  parity.FactCache(wl))
+    return {"tokens": int(lens.sum()), "swapped": swapped, "cache": cache, **stats}

@@ -39,7 +39,7 @@ def test_status_strings(lib):
 
 
 def test_struct_layouts_match_header():
-    assert ctypes.sizeof(_lib.StoreConfig) == 64
+    assert ctypes.sizeof(_lib.StoreConfig) == 72
     assert ctypes.sizeof(_lib.RopeParams) == 48
     assert ctypes.sizeof(_lib.CacheDesc) == 12
     assert ctypes.sizeof(_lib.StoreInfo) == 64
@@ -56,7 +56,7 @@ def _create(**kw):
     (dict(num_layers=0), 1), (dict(emb_dtype="bf16"), 1), (dict(max_facts=0), 1),
     (dict(max_k=2000), 1), (dict(max_queries=5000), 1), (dict(head_dim=96), 8),
     (dict(num_kv_heads=1, head_dim=64), 8), (dict(emb_dim=60), 8), (dict(head_dim=1024), 8),
-    (dict(kv_dtype=7), 1)])
+    (dict(kv_dtype=7), 1), (dict(kv_placement=2), 1), (dict(reserved=3), 1)])
 def test_create_rejects_bad_configs_before_the_device(lib, kw, status):
     with pytest.raises(api.ISError) as e:
         _create(**kw)
