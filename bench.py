@@ -212,6 +212,9 @@ def run_ours(args, rank, world, local_rank):
     wl = workloads.get(args.workload, **overrides)
     s = wl.spec
     store = staging.load_store(wl, api, device=local_rank, kv_placement=args.kv_placement)
+    from kv_cache_injection_gb300 import _lib
+    api.is_set_retrieval_mode(store, {"auto": _lib.IS_RETRIEVAL_AUTO, "per_query": _lib.IS_RETRIEVAL_PER_QUERY,
+                                      "batched": _lib.IS_RETRIEVAL_BATCHED}[args.retrieval])
     inp = staging.device_inputs(wl, local_rank)
     cache = staging.canary_cache(wl, local_rank)
     Q, k = s.n_queries, s.k
@@ -385,6 +388,7 @@ def run_ours(args, rank, world, local_rank):
                        f"then {L2_FLUSH_BYTES >> 20} MiB read (clean, cold L2 at each step)"),
                 "parallelism": f"replicas x{world} (one store per GPU, no collective)",
                 "kv_placement": args.kv_placement,
+                "retrieval": args.retrieval,
             },
             "roofline": roofline,
             "path_roofline": {
@@ -526,6 +530,8 @@ def main(argv=None):
                     help="model layers (smaller K/V for profiling the retrieval kernels)")
     ap.add_argument("--kv-placement", choices=["device", "host"], default="device",
                     help="where the store's K/V arena lives (host: page-locked host DRAM)")
+    ap.add_argument("--retrieval", choices=["auto", "per_query", "batched"], default="auto",
+                    help="similarity path: per-query kernel, tcgen05 batched contraction, or automatic")
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     args = ap.parse_args(argv)

@@ -179,6 +179,18 @@ __device__ __forceinline__ void prefetch_l2(const void* p) {
   asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
 
+// Thread i < 8 prefetches the first line of p_i into L2 (null pointers are
+// skipped).  Used at a kernel's start on arrays a later, dependent step will
+// read or write: the prefetch fills the address translation and L2 off that
+// step's critical path.
+__device__ __forceinline__ void warm8(const void* p0, const void* p1, const void* p2, const void* p3,
+                                      const void* p4, const void* p5, const void* p6, const void* p7) {
+  const int i = threadIdx.x;
+  const void* p = i == 0 ? p0 : i == 1 ? p1 : i == 2 ? p2 : i == 3 ? p3
+                : i == 4 ? p4 : i == 5 ? p5 : i == 6 ? p6 : i == 7 ? p7 : nullptr;
+  if (p) prefetch_l2(p);
+}
+
 // Prefetch n int32 entries (one 128-byte line per thread) into L2.
 __device__ __forceinline__ void prefetch_row_l2(const int32_t* p, int n, int tid, int nthreads) {
   for (int i = tid * 32; i < n; i += nthreads * 32) prefetch_l2(p + i);

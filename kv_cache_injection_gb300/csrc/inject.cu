@@ -92,9 +92,35 @@ struct StageMeta {
   int32_t l;        // layer
 };
 
-// Exclusive prefix of seg_len over the R requests into s_off[0..R] (shared
-// memory); returns the total token count.  All threads of the block call it.
-__device__ __forceinline__ int32_t segment_prefix(const InjectArgs& a, int32_t* s_off, int32_t* scratch) {
+// Shared-memory ints the request prefix needs: R + 1 for the block-wide scan,
+// or a 33-entry slice per warp when every warp scans R <= 32 requests itself.
+__host__ __device__ constexpr int prefix_ints(int R, int warps) { return R <= 32 ? warps * 33 : R + 1; }
+
+// Exclusive prefix of seg_len over the R requests; returns the total token
+// count and points *s_off at the prefix (R + 1 entries, the last = total).
+// Up to 32 requests, each warp loads and scans them with shuffles into its
+// own slice of `region`, so no block-wide barrier sits between the planning
+// kernel's outputs and the warp's first copy; more requests are scanned by the
+// whole block.  All threads of the block call it.
+__device__ __forceinline__ int32_t segment_prefix(const InjectArgs& a, int32_t* region, int32_t* scratch,
+                                                  const int32_t** s_off) {
+  if (a.R <= 32) {
+    const int lane = threadIdx.x & 31;
+    int32_t* mine = region + (threadIdx.x >> 5) * 33;
+    const int32_t v = lane < a.R ? a.seg_len[lane] : 0;
+    int32_t inc = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int32_t y = __shfl_up_sync(0xffffffffu, inc, o);
+      if (lane >= o) inc += y;
+    }
+    const int32_t total = __shfl_sync(0xffffffffu, inc, 31);
+    if (lane < a.R) mine[lane] = inc - v;
+    if (lane == 0) mine[a.R] = total;
+    __syncwarp();
+    *s_off = mine;
+    return total;
+  }
   int32_t total = 0;
   const int per = (a.R + blockDim.x - 1) / blockDim.x;
   const int b = min(a.R, (int)threadIdx.x * per);
@@ -103,23 +129,102 @@ __device__ __forceinline__ int32_t segment_prefix(const InjectArgs& a, int32_t* 
   for (int i = b; i < e; ++i) sum += a.seg_len[i];
   int32_t base = block_exclusive_scan(sum, scratch, &total);
   for (int i = b; i < e; ++i) {
-    s_off[i] = base;
+    region[i] = base;
     base += a.seg_len[i];
   }
-  if (threadIdx.x == 0) s_off[a.R] = total;
+  if (threadIdx.x == 0) region[a.R] = total;
   __syncthreads();
+  *s_off = region;
   return total;
 }
 
 // Warp-uniform walk from a composed-segment token t (all requests back to
 // back) to its store token, serving position and destination slot.  Tokens a
-// warp visits are consecutive, so the request and fact found last time are
-// kept and searched again only when t leaves them.
+// warp visits are consecutive, so the request, fact and block-table entry found
+// last time are kept and looked up again only when t leaves them.
+//
+// Finding the fact of a token is on the critical path of every warp's first
+// item, so it is one round of independent loads: the request's fact count and
+// start position, and the first 128 entries of its plan (segment offset and
+// store token of each fact, four per lane); a ballot then picks the last fact
+// whose offset is <= the token's.  Longer plans continue with a strided search
+// over the rest.
 struct TokenCursor {
   int32_t t = -1, r = -1, j = 0, lo = 0, hi = 0;
-  int64_t src = 0;    // store token
-  int64_t slot = -1;  // cache slot, -1 if the block table rejects the position
-  int32_t p = 0;      // position in the request's sequence
+  int32_t start = 0;    // seg_start of request r
+  int64_t src0 = 0;     // store token of fact j's first token
+  int32_t lb = -1, blk = -1;
+  int64_t src = 0;      // store token
+  int64_t slot = -1;    // cache slot, -1 if the block table rejects the position
+  int32_t p = 0;        // position in the request's sequence
+
+  static constexpr int kPer = 4;    // plan entries per lane in the first round
+
+  __device__ __forceinline__ void find_fact(const InjectArgs& a, int rr, int32_t ts, int lane) {
+    const int32_t* off = a.fact_seg_off + (size_t)rr * a.seg_stride;
+    const int64_t* fsrc = a.fact_src ? a.fact_src + (size_t)rr * a.seg_stride : nullptr;
+    const int n = a.n_ids[rr];
+    start = a.seg_start[rr];
+    int32_t o[kPer];
+    int64_t sv[kPer];
+#pragma unroll
+    for (int e = 0; e < kPer; ++e) {
+      const int idx = lane * kPer + e;
+      const bool in = idx < a.seg_stride;
+      o[e] = in ? off[idx] : 0;
+      sv[e] = (in && fsrc) ? fsrc[idx] : 0;
+    }
+    // Offsets strictly increase, so "offset <= ts" holds for a prefix of the
+    // facts; its last entry is the fact holding ts (off[0] = 0 <= ts).
+    int best = -1;
+#pragma unroll
+    for (int e = 0; e < kPer; ++e) {
+      const int idx = lane * kPer + e;
+      if (idx < n && idx < a.seg_stride && o[e] <= ts) best = idx;
+    }
+    const unsigned m = __ballot_sync(0xffffffffu, best >= 0);
+    const int owner = 31 - __clz(m);
+    int jlo = __shfl_sync(0xffffffffu, best, owner);
+    constexpr int kFan = 32 * kPer;
+    auto pick32 = [&](const int32_t* v, int idx) -> int32_t {
+      const int e = idx % kPer;
+      int32_t x = v[0];
+#pragma unroll
+      for (int q = 1; q < kPer; ++q) x = e == q ? v[q] : x;
+      return __shfl_sync(0xffffffffu, x, idx / kPer);
+    };
+    auto pick64 = [&](const int64_t* v, int idx) -> int64_t {
+      const int e = idx % kPer;
+      int64_t x = v[0];
+#pragma unroll
+      for (int q = 1; q < kPer; ++q) x = e == q ? v[q] : x;
+      return __shfl_sync(0xffffffffu, x, idx / kPer);
+    };
+    if (jlo == kFan - 1 && n > kFan) {
+      // Beyond the first round: strided search over [kFan - 1, n).
+      int jhi = n;
+      while (jhi - jlo > 1) {
+        const int stride = (jhi - jlo + 31) >> 5;
+        const int idx = jlo + lane * stride;
+        const bool le = idx < jhi && off[idx] <= ts;
+        const unsigned mm = __ballot_sync(0xffffffffu, le);
+        jlo += (31 - __clz(mm)) * stride;
+        jhi = min(jhi, jlo + stride);
+      }
+      lo = off[jlo];
+      hi = off[jlo + 1];
+      src0 = fsrc ? fsrc[jlo] : a.fact_tok[a.ids[(size_t)rr * a.ids_stride + jlo]];
+    } else {
+      lo = pick32(o, jlo);
+      const int32_t hnext = pick32(o, min(jlo + 1, kFan - 1));
+      hi = jlo + 1 < kFan ? hnext : off[jlo + 1];
+      const int64_t s_in = pick64(sv, jlo);
+      src0 = fsrc ? s_in : a.fact_tok[a.ids[(size_t)rr * a.ids_stride + jlo]];
+    }
+    r = rr;
+    j = jlo;
+    lb = -1;
+  }
 
   __device__ __forceinline__ void seek(const InjectArgs& a, const int32_t* s_off, int32_t tt, int lane) {
     if (tt == t) return;
@@ -130,36 +235,21 @@ struct TokenCursor {
       if (s_off[mid] <= tt) rlo = mid; else rhi = mid;
     }
     const int32_t ts = tt - s_off[rlo];
-    if (rlo != r || ts < lo || ts >= hi) {
-      const int32_t* off = a.fact_seg_off + (size_t)rlo * a.seg_stride;
-      int jlo = 0, jhi = a.n_ids[rlo];
-      while (jhi - jlo > 1) {
-        const int stride = (jhi - jlo + 31) >> 5;
-        const int idx = jlo + lane * stride;
-        const bool le = idx < jhi && off[idx] <= ts;
-        const unsigned m = __ballot_sync(0xffffffffu, le);
-        jlo += (31 - __clz(m)) * stride;
-        jhi = min(jhi, jlo + stride);
-      }
-      r = rlo;
-      j = jlo;
-      lo = off[jlo];
-      hi = off[jlo + 1];
+    if (rlo != r || ts < lo || ts >= hi) find_fact(a, rlo, ts, lane);
+    src = src0 + (ts - lo);
+    p = start + ts;
+    const int32_t lbn = p / a.block_size;
+    if (lbn != lb) {
+      lb = lbn;
+      blk = lbn < a.max_blocks ? a.block_table[(size_t)r * a.max_blocks + lbn] : -1;
     }
-    src = (a.fact_src ? a.fact_src[(size_t)r * a.seg_stride + j]
-                      : a.fact_tok[a.ids[(size_t)r * a.ids_stride + j]]) + (ts - lo);
-    p = a.seg_start[r] + ts;
-    const int32_t lb = p / a.block_size;
     slot = -1;
     if (lb >= a.max_blocks) {
       if (lane == 0) latch(a.status, IS_ST_BLOCK_TABLE);
+    } else if (blk < 0 || blk >= a.num_blocks) {
+      if (lane == 0) latch(a.status, IS_ST_BLOCK_ID);
     } else {
-      const int32_t blk = a.block_table[(size_t)r * a.max_blocks + lb];
-      if (blk < 0 || blk >= a.num_blocks) {
-        if (lane == 0) latch(a.status, IS_ST_BLOCK_ID);
-      } else {
-        slot = (int64_t)blk * a.block_size + (p - lb * a.block_size);
-      }
+      slot = (int64_t)blk * a.block_size + (p - lb * a.block_size);
     }
   }
 };
@@ -172,21 +262,30 @@ __global__ void __launch_bounds__(kInjectWarpsMax * 32) inject_kernel(const Inje
   constexpr int VE = Vec<T>::N;
   constexpr int NF = STYLE == 0 ? VE : VE / 2;
 
-  pdl_wait();                                   // outputs of the planning kernel
-
   const int nwarps = blockDim.x >> 5;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const uint32_t item_bytes = 2u * (uint32_t)a.row_bytes;
-  int32_t* s_off = reinterpret_cast<int32_t*>(smem);                 // [R + 1]
-  const size_t off_bytes = ((size_t)(a.R + 1) * 4 + 127) & ~(size_t)127;
+  int32_t* off_region = reinterpret_cast<int32_t*>(smem);
+  const size_t off_bytes = ((size_t)prefix_ints(a.R, kInjectWarpsMax) * 4 + 127) & ~(size_t)127;
   uint8_t* stages = smem + off_bytes + (size_t)warp * P * item_bytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + off_bytes + (size_t)nwarps * P * item_bytes) +
                    (size_t)warp * P;
   StageMeta* meta = reinterpret_cast<StageMeta*>(smem + off_bytes + (size_t)nwarps * P * item_bytes +
                                                  (size_t)nwarps * P * 8) + (size_t)warp * P;
 
-  const int32_t total = segment_prefix(a, s_off, scratch);
+  // While the planning kernel still runs: set up this warp's barriers and warm
+  // the pages the first item's lookup reads.
+  if (lane == 0) {
+    for (int s = 0; s < P; ++s) mbar_init(smem_addr(&bars[s]), 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+  warm8(a.seg_len, a.n_ids, a.fact_seg_off, a.fact_src, a.seg_start, a.block_table, a.slot_mapping, a.ids);
+  pdl_wait();                                   // outputs of the planning kernel
+
+  const int32_t* s_off;
+  const int32_t total = segment_prefix(a, off_region, scratch, &s_off);
 
   const int64_t n_items = (int64_t)total * a.n_layers;
   const int64_t warp_id = (int64_t)blockIdx.x * nwarps + warp;
@@ -196,12 +295,6 @@ __global__ void __launch_bounds__(kInjectWarpsMax * 32) inject_kernel(const Inje
   const int64_t it_end = min(n_items, it0 + chunk);
   if (it0 >= it_end) return;
 
-  if (lane == 0) {
-    for (int s = 0; s < P; ++s) mbar_init(smem_addr(&bars[s]), 1);
-    fence_mbar_init();
-  }
-  __syncwarp();
-
   const uint32_t stage0 = smem_addr(stages);
   const int vpl = a.row_bytes >> 9;             // 16-byte vectors per lane per row
   const int hv = a.half_vecs;
@@ -209,11 +302,18 @@ __global__ void __launch_bounds__(kInjectWarpsMax * 32) inject_kernel(const Inje
 
   TokenCursor cur;
 
-  // Warp-uniform: resolve item j's token and have lane 0 start its bulk load
-  // into stage s.  Returns true if a load was issued.
-  auto issue = [&](int64_t j, int s) -> bool {
-    const int32_t t = (int32_t)(j / a.n_layers);
-    const int32_t l = (int32_t)(j - (int64_t)t * a.n_layers);   // layer within this call
+  // Next item to issue, as (segment token, layer within this call).
+  int32_t nt = (int32_t)(it0 / a.n_layers);
+  int32_t nl = (int32_t)(it0 - (int64_t)nt * a.n_layers);
+
+  // Warp-uniform: resolve the next item's token and have lane 0 start its bulk
+  // load into stage s.  Items are issued in order.  Returns true if a load was issued.
+  auto issue = [&](int s) -> bool {
+    const int32_t t = nt, l = nl;
+    if (++nl == a.n_layers) {
+      nl = 0;
+      ++nt;
+    }
     cur.seek(a, s_off, t, lane);
     const int64_t tok_slot = cur.slot;
     const int32_t tok_p = cur.p;
@@ -236,7 +336,7 @@ __global__ void __launch_bounds__(kInjectWarpsMax * 32) inject_kernel(const Inje
   uint32_t phase = 0;        // expected parity of each stage's next completion
   uint32_t pending = 0;      // stages with a bulk load in flight
   for (int s = 0; s < P && it0 + s < it_end; ++s)
-    if (issue(it0 + s, s)) pending |= 1u << s;
+    if (issue(s)) pending |= 1u << s;
   __syncwarp();
 
   float cs[NF], sn[NF];
@@ -303,7 +403,7 @@ __global__ void __launch_bounds__(kInjectWarpsMax * 32) inject_kernel(const Inje
         fence_proxy_async_smem();
       }
       __syncwarp();
-      if (issue(i - 1 + P, sp)) pending |= 1u << sp;
+      if (issue(sp)) pending |= 1u << sp;
     }
     __syncwarp();
     s = s + 1 == P ? 0 : s + 1;
@@ -340,16 +440,18 @@ __device__ __forceinline__ uint4 ld_plain(const uint8_t* p) { return *reinterpre
 template <typename T, int STYLE>
 __global__ void __launch_bounds__(kHostWarps * 32) inject_host_kernel(const InjectArgs a,
                                                                       const RopeTurns rt) {
-  extern __shared__ __align__(16) int32_t s_off[];   // [R + 1]
+  extern __shared__ __align__(16) int32_t off_region[];   // prefix_ints(R, kHostWarps)
   __shared__ int32_t scratch[33];
   constexpr int VE = Vec<T>::N;
   constexpr int NF = STYLE == 0 ? VE : VE / 2;
 
+  warm8(a.seg_len, a.n_ids, a.fact_seg_off, a.fact_src, a.seg_start, a.block_table, a.slot_mapping, a.ids);
   pdl_wait();                                   // outputs of the planning kernel
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int32_t total = segment_prefix(a, s_off, scratch);
+  const int32_t* s_off;
+  const int32_t total = segment_prefix(a, off_region, scratch, &s_off);
   const int64_t n_items = (int64_t)total * a.n_layers;
   const int64_t n_warps = (int64_t)gridDim.x * (blockDim.x >> 5);
   const int64_t chunk = (n_items + n_warps - 1) / n_warps;
@@ -363,9 +465,13 @@ __global__ void __launch_bounds__(kHostWarps * 32) inject_host_kernel(const Inje
   TokenCursor cur;
   float cs[NF], sn[NF];
   int32_t cur_p = -1;
+  int32_t t = (int32_t)(it0 / a.n_layers);
+  int32_t l = (int32_t)(it0 - (int64_t)t * a.n_layers) - 1;
   for (int64_t i = it0; i < it_end; ++i) {
-    const int32_t t = (int32_t)(i / a.n_layers);
-    const int32_t l = (int32_t)(i - (int64_t)t * a.n_layers);
+    if (++l == a.n_layers) {
+      l = 0;
+      ++t;
+    }
     cur.seek(a, s_off, t, lane);
     if (l == 0 && lane == 0 && a.slot_mapping) a.slot_mapping[t] = cur.slot;
     if (cur.slot < 0) continue;
@@ -455,7 +561,7 @@ struct InjectShape {
 
 static InjectShape inject_shape(const InjectArgs& a) {
   const size_t item = 2 * (size_t)a.row_bytes;
-  const size_t off_bytes = ((size_t)(a.R + 1) * 4 + 127) & ~(size_t)127;
+  const size_t off_bytes = ((size_t)prefix_ints(a.R, kInjectWarpsMax) * 4 + 127) & ~(size_t)127;
   const size_t per_stage = item + 8 + sizeof(StageMeta);
   const size_t stage_budget = 96 * 1024;        // two CTAs per SM
   const size_t smem_max = 227 * 1024 - 1024;
@@ -519,7 +625,7 @@ static cudaError_t launch_inject_t(const InjectArgs& a, const RopeTurns& rt, con
 template <typename T, int STYLE>
 static cudaError_t launch_inject_host_t(const InjectArgs& a, const RopeTurns& rt, const LaunchCfg& cfg) {
   auto kern = inject_host_kernel<T, STYLE>;
-  const size_t smem = (size_t)(a.R + 1) * 4;
+  const size_t smem = (size_t)prefix_ints(a.R, kHostWarps) * 4;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;

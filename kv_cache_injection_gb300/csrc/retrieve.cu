@@ -1,5 +1,5 @@
 // GPU-resident semantic retrieval: cosine similarity against one user's
-// stored embeddings, then an exact top-k by radix select.
+// stored embeddings, then an exact top-k (topk.cuh).
 //
 // InferScale keeps the retrieval index and the KV store both on the GPU so
 // retrieved text never crosses PCIe ("Conception de Système Native au GPU"),
@@ -63,10 +63,10 @@ cudaError_t launch_emb_norms(const void* emb, int emb_dtype, int E, const int32_
 // counter; the last one (the counter reaches tiles * n_sub) resets the counter
 // and runs the top-k of q over the scores, which are then in L2.
 //
-// Top-k: radix select on order-preserving uint32 keys, 8 bits per pass, finds
-// the k-th largest key thr and how many keys equal to thr to take; keys > thr
-// are all taken and keys == thr in ascending row order (ties go to the lower
-// fact id); the picks are sorted by (key desc, row asc); ids, scores and the
+// Top-k (topk_block): a cosine-bin histogram locates the bin of the k-th
+// score, the rows in and above it are the candidates (an exact radix select
+// takes over when ties crowd one bin), and the candidates are ordered by
+// (score desc, row asc), so ties go to the lower fact id; ids, scores and the
 // segment plan (exclusive prefix of the facts' lengths) are written.
 template <typename E, bool SMEM_KEYS>
 __global__ void __launch_bounds__(kRetThreads) retrieve_kernel(const SimArgs sa, const TopkArgs ta,
@@ -78,6 +78,10 @@ __global__ void __launch_bounds__(kRetThreads) retrieve_kernel(const SimArgs sa,
   const int q = blockIdx.y;
   const int ti = blockIdx.x / n_sub;
   const int sub = blockIdx.x - ti * n_sub;
+  // Pages written later (scores, top-k outputs, plan) and the store's per-user
+  // records: warm their translations now, in parallel with the user lookup.
+  warm8(sa.scores + (size_t)q * sa.score_stride, ta.ids_out, ta.scores_out, ta.fact_seg_off, ta.fact_src,
+        ta.seg_len, sa.user_meta, sa.emb_inv_norm);
   // The query row does not depend on the user lookup: start pulling it into L2.
   if (threadIdx.x * 128 < sa.E * (int)sizeof(E))
     prefetch_l2(reinterpret_cast<const uint8_t*>(sa.q_emb) + ((size_t)q * sa.E * sizeof(E)) + threadIdx.x * 128);

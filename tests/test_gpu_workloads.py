@@ -76,6 +76,18 @@ class TestQwen100Users:
         st = gh.check_fused_workload(api, wl, store, sample_tokens=300)
         assert st["tokens"] > 100 * 50 * 10
 
+    def test_fused_parity_tensor_core_similarity(self, api, loaded):
+        """The same 100 queries with the similarity as tcgen05 contractions
+        (one group per user), then the per-user top-k."""
+        from kv_cache_injection_gb300 import _lib
+        wl, store = loaded
+        api.is_set_retrieval_mode(store, _lib.IS_RETRIEVAL_BATCHED)
+        try:
+            st = gh.check_fused_workload(api, wl, store, sample_tokens=300, seed=1)
+        finally:
+            api.is_set_retrieval_mode(store, _lib.IS_RETRIEVAL_AUTO)
+        assert st["tokens"] > 100 * 50 * 10
+
 
 @pytest.mark.slow
 class TestCapacity:
