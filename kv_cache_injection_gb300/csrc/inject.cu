@@ -92,6 +92,11 @@ struct StageMeta {
   int32_t l;        // layer
 };
 
+// x / d for non-negative operands, in 32-bit arithmetic when both fit.
+__device__ __forceinline__ int64_t div_nn(int64_t x, int64_t d) {
+  return ((x | d) >> 31) == 0 ? (int64_t)((uint32_t)x / (uint32_t)d) : x / d;
+}
+
 // Shared-memory ints the request prefix needs: R + 1 for the block-wide scan,
 // or a 33-entry slice per warp when every warp scans R <= 32 requests itself.
 __host__ __device__ constexpr int prefix_ints(int R, int warps) { return R <= 32 ? warps * 33 : R + 1; }
@@ -290,7 +295,7 @@ __global__ void __launch_bounds__(kInjectWarpsMax * 32) inject_kernel(const Inje
   const int64_t n_items = (int64_t)total * a.n_layers;
   const int64_t warp_id = (int64_t)blockIdx.x * nwarps + warp;
   const int64_t n_warps = (int64_t)gridDim.x * nwarps;
-  const int64_t chunk = (n_items + n_warps - 1) / n_warps;
+  const int64_t chunk = div_nn(n_items + n_warps - 1, n_warps);
   const int64_t it0 = warp_id * chunk;
   const int64_t it_end = min(n_items, it0 + chunk);
   if (it0 >= it_end) return;
@@ -303,7 +308,7 @@ __global__ void __launch_bounds__(kInjectWarpsMax * 32) inject_kernel(const Inje
   TokenCursor cur;
 
   // Next item to issue, as (segment token, layer within this call).
-  int32_t nt = (int32_t)(it0 / a.n_layers);
+  int32_t nt = (int32_t)div_nn(it0, a.n_layers);
   int32_t nl = (int32_t)(it0 - (int64_t)nt * a.n_layers);
 
   // Warp-uniform: resolve the next item's token and have lane 0 start its bulk
@@ -454,7 +459,7 @@ __global__ void __launch_bounds__(kHostWarps * 32) inject_host_kernel(const Inje
   const int32_t total = segment_prefix(a, off_region, scratch, &s_off);
   const int64_t n_items = (int64_t)total * a.n_layers;
   const int64_t n_warps = (int64_t)gridDim.x * (blockDim.x >> 5);
-  const int64_t chunk = (n_items + n_warps - 1) / n_warps;
+  const int64_t chunk = div_nn(n_items + n_warps - 1, n_warps);
   const int64_t it0 = ((int64_t)blockIdx.x * (blockDim.x >> 5) + warp) * chunk;
   const int64_t it_end = min(n_items, it0 + chunk);
 
@@ -465,7 +470,7 @@ __global__ void __launch_bounds__(kHostWarps * 32) inject_host_kernel(const Inje
   TokenCursor cur;
   float cs[NF], sn[NF];
   int32_t cur_p = -1;
-  int32_t t = (int32_t)(it0 / a.n_layers);
+  int32_t t = (int32_t)div_nn(it0, a.n_layers);
   int32_t l = (int32_t)(it0 - (int64_t)t * a.n_layers) - 1;
   for (int64_t i = it0; i < it_end; ++i) {
     if (++l == a.n_layers) {

@@ -74,7 +74,6 @@ __global__ void __launch_bounds__(kRetThreads) retrieve_kernel(const SimArgs sa,
   extern __shared__ uint32_t s_keys[];         // [n] keys of the top-k phase (SMEM_KEYS)
   __shared__ TopkShared sh;
   __shared__ int s_last;
-  pdl_trigger();
   const int q = blockIdx.y;
   const int ti = blockIdx.x / n_sub;
   const int sub = blockIdx.x - ti * n_sub;
@@ -151,6 +150,12 @@ __global__ void __launch_bounds__(kRetThreads) retrieve_kernel(const SimArgs sa,
   __syncthreads();
   if (!s_last) return;
   __threadfence();
+  // The dependent inject grid may launch once every CTA has exited or
+  // triggered: here, when the last one starts its top-k.  Its launch latency
+  // then hides under the top-k, and its CTAs are placed on SMs the similarity
+  // CTAs have left (triggering at kernel start let them land among running
+  // similarity CTAs, which measured 6 us slower per Llama-3.1-8B step).
+  pdl_trigger();
   topk_block<SMEM_KEYS>(ta, sh, s_keys, q, um, n_u);
 }
 

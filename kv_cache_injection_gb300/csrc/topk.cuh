@@ -37,8 +37,7 @@ constexpr int kCosBins = 2048;
 struct TopkShared {
   uint32_t hist[kCosBins];                  // cosine bins; the radix fallback reuses it as [4][256]
   unsigned long long sel[kCandMax];         // (key << 32) | ((2^20-1 - row) << 10) | slot
-  unsigned long long cand[kCandMax];        // (length << 32) | fact id, by slot
-  int32_t len[kCandMax];                    // length by slot (rank path)
+  unsigned long long cand[kCandMax];        // (length << 32) | fact id, by slot (by rank on the rank path)
   int32_t scratch[33];
   uint32_t wsum[8];
   uint32_t bstar, above, eq, digit, cnt;
@@ -62,10 +61,10 @@ __device__ __forceinline__ void fetch_cand(const TopkArgs& a, TopkShared& sh, co
   sh.cand[slot] = ((unsigned long long)(uint32_t)a.tile_len[row] << 32) | (uint32_t)a.tile_fact[row];
 }
 
-// Writes the segment plan of query q from its facts' lengths (one warp).
-__device__ __forceinline__ void plan_tail(const TopkArgs& a, int q, int nn, int32_t total) {
+// Writes the segment plan's tail of query q (one thread): the total, the
+// fact count and the segment length; `start` is seg_start[q].
+__device__ __forceinline__ void plan_tail(const TopkArgs& a, int q, int nn, int32_t total, int32_t start) {
   int32_t* off = a.fact_seg_off + (size_t)q * a.seg_stride;
-  const int32_t start = a.seg_start[q];
   if (start < 0 || (int64_t)start + total > (int64_t)IS_MAX_POSITION) {
     latch(a.status, IS_ST_POSITION);
     nn = 0;
@@ -96,18 +95,26 @@ __device__ void topk_block(const TopkArgs& a, TopkShared& sh, uint32_t* s_keys, 
   if (a.block_table) prefetch_row_l2(a.block_table + (size_t)q * a.max_blocks, a.max_blocks, tid, kRetThreads);
   int64_t* ids = a.ids_out + (size_t)q * a.k;
   float* scs = a.scores_out + (size_t)q * a.k;
+  // Read now, used at the very end: its latency hides under the selection.
+  const int32_t start_q = (a.fact_seg_off && tid == 0) ? a.seg_start[q] : 0;
 
+  // The first batch of scores is requested before the histogram is cleared,
+  // so their latency overlaps the clearing and the barrier.
+  float v[8];
+  auto load_batch = [&](int b) {
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int j = b + u * kRetThreads + tid;
+      v[u] = j < n ? __ldcg(sc + j) : 0.f;
+    }
+  };
+  if (kk > 0) load_batch(0);
   for (int i = tid; i < kCosBins; i += kRetThreads) sh.hist[i] = 0;
   if (tid == 0) sh.cnt = 0;
   __syncthreads();
   if (kk > 0) {
     for (int b = 0; b < n; b += 8 * kRetThreads) {
-      float v[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int j = b + u * kRetThreads + tid;
-        v[u] = j < n ? __ldcg(sc + j) : 0.f;
-      }
+      if (b > 0) load_batch(b);
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
         const int j = b + u * kRetThreads + tid;
@@ -124,7 +131,7 @@ __device__ void topk_block(const TopkArgs& a, TopkShared& sh, uint32_t* s_keys, 
   }
   __syncthreads();
   if (kk == 0) {
-    if (a.fact_seg_off && tid == 0) plan_tail(a, q, 0, 0);
+    if (a.fact_seg_off && tid == 0) plan_tail(a, q, 0, 0, start_q);
     return;
   }
 
@@ -162,12 +169,28 @@ __device__ void topk_block(const TopkArgs& a, TopkShared& sh, uint32_t* s_keys, 
   if (sh.above + sh.eq <= (uint32_t)kCandMax) {
     const int bstar = sh.bstar;
     C = sh.above + sh.eq;
-    for (int b = 0; b < n; b += kRetThreads) {
-      const int j = b + tid;
-      const uint32_t key = j < n ? key_at(j) : 0u;
-      const bool take = j < n && cos_bin(key_score(key)) >= bstar;
-      const uint32_t slot = warp_claim(take, &sh.cnt, lane);
-      if (take) sh.sel[slot] = sel_entry(key, (uint32_t)j, slot);
+    if (SMEM_KEYS) {
+      // Keys in shared memory: count this thread's candidates, one block scan
+      // gives each thread its first slot, then a second pass writes them.
+      uint32_t mine = 0;
+      for (int j = tid; j < n; j += kRetThreads) mine += cos_bin(key_score(s_keys[j])) >= bstar ? 1u : 0u;
+      int32_t tot;
+      uint32_t slot = (uint32_t)block_exclusive_scan((int32_t)mine, sh.scratch, &tot);
+      for (int j = tid; j < n; j += kRetThreads) {
+        const uint32_t key = s_keys[j];
+        if (cos_bin(key_score(key)) >= bstar) {
+          sh.sel[slot] = sel_entry(key, (uint32_t)j, slot);
+          ++slot;
+        }
+      }
+    } else {
+      for (int b = 0; b < n; b += kRetThreads) {
+        const int j = b + tid;
+        const uint32_t key = j < n ? key_at(j) : 0u;
+        const bool take = j < n && cos_bin(key_score(key)) >= bstar;
+        const uint32_t slot = warp_claim(take, &sh.cnt, lane);
+        if (take) sh.sel[slot] = sel_entry(key, (uint32_t)j, slot);
+      }
     }
   } else {
     // Radix select: 8 bits per pass finds the k-th largest key thr and how
@@ -243,36 +266,44 @@ __device__ void topk_block(const TopkArgs& a, TopkShared& sh, uint32_t* s_keys, 
 
   if (C <= (uint32_t)kRetThreads) {
     // Rank selection: thread t owns candidate t; its rank is the number of
-    // candidates above it (entries are unique) and its segment offset the sum
-    // of their lengths.  The fact lookup overlaps the first pass.
+    // candidates above it (entries are unique).  The fact lookup overlaps the
+    // ranking.  The top kk are then placed by rank (fact and length in
+    // sh.cand, store token and key in the histogram's space, free by now), so
+    // thread r writes rank r's outputs and one block scan of the lengths gives
+    // the segment offsets.
     const uint32_t t = (uint32_t)tid;
-    unsigned long long e = 0;
-    int32_t f = 0, len = 0;
-    int64_t tok = 0;
-    uint32_t rank = 0;
+    int64_t* rk_tok = reinterpret_cast<int64_t*>(sh.hist);          // [256]
+    uint32_t* rk_key = sh.hist + 2 * kRetThreads;                     // [256]
     if (t < C) {
-      e = sh.sel[t];
+      const unsigned long long e = sh.sel[t];
       const uint32_t j = 0xFFFFFu - (uint32_t)((e >> 10) & 0xFFFFFu);
       const int tile = user_tile(a.user_tiles, um, (int)(j / kTile));
       const size_t row = (size_t)tile * kTile + (j % kTile);
-      f = a.tile_fact[row];
-      len = a.tile_len[row];
-      tok = a.tile_tok[row];
+      const int32_t f = a.tile_fact[row];
+      const int32_t len = a.tile_len[row];
+      const int64_t tok = a.tile_tok[row];
+      uint32_t rank = 0;
       for (uint32_t i = 0; i < C; ++i) rank += sh.sel[i] > e ? 1u : 0u;
-      sh.len[t] = len;
-    }
-    __syncthreads();
-    if (t < C && rank < (uint32_t)kk) {
-      int32_t off = 0;
-      for (uint32_t i = 0; i < C; ++i) off += sh.sel[i] > e ? sh.len[i] : 0;
-      ids[rank] = f;
-      scs[rank] = key_score((uint32_t)(e >> 32));
-      if (a.fact_seg_off) {
-        a.fact_seg_off[(size_t)q * a.seg_stride + rank] = off;
-        a.fact_src[(size_t)q * a.seg_stride + rank] = tok;
-        if (rank == (uint32_t)kk - 1) plan_tail(a, q, kk, off + len);
+      if (rank < (uint32_t)kk) {
+        sh.cand[rank] = ((unsigned long long)(uint32_t)len << 32) | (uint32_t)f;
+        rk_tok[rank] = tok;
+        rk_key[rank] = (uint32_t)(e >> 32);
       }
     }
+    __syncthreads();
+    const unsigned long long cv = t < (uint32_t)kk ? sh.cand[t] : 0ull;
+    const int32_t len = (int32_t)(cv >> 32);
+    int32_t total;
+    const int32_t off = block_exclusive_scan(len, sh.scratch, &total);
+    if (t < (uint32_t)kk) {
+      ids[t] = (int32_t)(uint32_t)cv;
+      scs[t] = key_score(rk_key[t]);
+      if (a.fact_seg_off) {
+        a.fact_seg_off[(size_t)q * a.seg_stride + t] = off;
+        a.fact_src[(size_t)q * a.seg_stride + t] = rk_tok[t];
+      }
+    }
+    if (a.fact_seg_off && t == 0) plan_tail(a, q, kk, total, start_q);
     return;
   }
 
@@ -320,7 +351,7 @@ __device__ void topk_block(const TopkArgs& a, TopkShared& sh, uint32_t* s_keys, 
       carry += tot;
     }
   }
-  if (a.fact_seg_off && tid == 0) plan_tail(a, q, kk, carry);
+  if (a.fact_seg_off && tid == 0) plan_tail(a, q, kk, carry, start_q);
 }
 
 }  // namespace isk
