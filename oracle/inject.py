@@ -17,6 +17,13 @@ Readings where the pages are silent:
 * rotated keys are computed in fp64 and rounded to the cache type with
   round-to-nearest-even; values are copied bit for bit;
 * every other element of the cache keeps its previous contents.
+
+An FP8 E4M3 cache (vLLM's 8-bit KV cache; the pages do not treat it) stores
+x / scale with one scale for K and one for V, rounded to nearest even and
+saturated to +-448.  The rotated key is divided in fp64 like the rest of the
+rotation; for V, whose byte is a quantised code of a stored value, the
+division is taken in fp32 (IEEE, correctly rounded) as the kernel takes it,
+so both sides make the same rounding decision from the same number.
 """
 from __future__ import annotations
 
@@ -48,11 +55,26 @@ def rotated_key_rows(k_token: np.ndarray, position: int, freqs: np.ndarray, styl
     return rope.rotate(numerics.decode(k_token, kv_dtype), position, freqs, style)
 
 
+def e4m3_key(k_rot: np.ndarray, k_scale: float) -> np.ndarray:
+    """Rotated keys (fp64) into E4M3 bits: k / k_scale, rounded once."""
+    return numerics.f64_to_e4m3_bits(k_rot / float(np.float32(k_scale)))
+
+
+def e4m3_value(v_enc: np.ndarray, kv_dtype: str, v_scale: float) -> np.ndarray:
+    """Stored values into E4M3 bits: fp32(v) / fp32(v_scale) in IEEE fp32, then
+    rounded to E4M3 (bf16 and fp16 values are exact in fp32)."""
+    v32 = numerics.decode(v_enc, kv_dtype).astype(np.float32)
+    return numerics.f64_to_e4m3_bits((v32 / np.float32(v_scale)).astype(np.float64))
+
+
 def inject(cache: np.ndarray, kv_dtype: str, fact_kv, fact_ids, lengths, start: int,
-           block_row, block_size: int, freqs: np.ndarray, style: int):
+           block_row, block_size: int, freqs: np.ndarray, style: int, cache_dtype: str | None = None,
+           k_scale: float = 1.0, v_scale: float = 1.0):
     """Scatter one request into ``cache`` (storage encoding, [L][2][NB][bs][H][D]),
     in place.  ``fact_kv(f)`` returns (K, V) of fact f as [len][L][H][D] in
-    storage encoding.  Returns (plan, seg_len, slots)."""
+    storage encoding.  ``cache_dtype`` "e4m3" selects an FP8 cache with the
+    given scales; otherwise the cache has the store's type.  Returns (plan,
+    seg_len, slots)."""
     plan, seg_len = compose(fact_ids, lengths, start)
     slots = []
     cur = None
@@ -64,6 +86,10 @@ def inject(cache: np.ndarray, kv_dtype: str, fact_kv, fact_ids, lengths, start: 
         slots.append(s)
         blk, off = divmod(s, block_size)
         k_rot = rotated_key_rows(K[j], p, freqs, style, kv_dtype)  # [L][H][D] fp64
-        cache[:, 0, blk, off] = numerics.encode(k_rot, kv_dtype)
-        cache[:, 1, blk, off] = V[j]
+        if cache_dtype == "e4m3":
+            cache[:, 0, blk, off] = e4m3_key(k_rot, k_scale)
+            cache[:, 1, blk, off] = e4m3_value(V[j], kv_dtype, v_scale)
+        else:
+            cache[:, 0, blk, off] = numerics.encode(k_rot, kv_dtype)
+            cache[:, 1, blk, off] = V[j]
     return plan, seg_len, np.asarray(slots, dtype=np.int64)

@@ -106,6 +106,14 @@ SPECS = {
         length_dist=("uniform", 10, 40), emb_dim=1024, emb_dtype="f16", n_queries=100, k=50,
         query_kind="planted", start=("const", 32), block_size=16, tokens_cap=50 * 40,
         block_layout="free_list", seed=4),
+    # Qwen3-14B KV shape (the pages' larger model): 40 layers, 8 KV heads,
+    # head_dim 128, theta 1e6, otherwise as the Llama-3.1-8B request.
+    "qwen3_14b": WorkloadSpec(
+        name="qwen3_14b", num_layers=40, num_kv_heads=8, head_dim=128, kv_dtype="bf16",
+        rope=RopeSpec(theta=1.0e6), n_users=1, facts_per_user=2000,
+        length_dist=("uniform", 10, 40), emb_dim=1024, emb_dtype="f16", n_queries=1, k=50,
+        query_kind="planted", start=("const", 32), block_size=16, tokens_cap=50 * 40,
+        block_layout="free_list", seed=6),
     # Capacity stress on the Llama-3.1-8B KV shape (~105 GB store).
     "capacity": WorkloadSpec(
         name="capacity", num_layers=32, num_kv_heads=8, head_dim=128, kv_dtype="bf16",

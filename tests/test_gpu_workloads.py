@@ -89,6 +89,23 @@ class TestQwen100Users:
         assert st["tokens"] > 100 * 50 * 10
 
 
+class TestQwen3_14B:
+    """The larger model the pages scale to: Qwen3-14B KV shape, k = 50."""
+
+    @pytest.fixture(scope="class")
+    @classmethod
+    def loaded(cls, api):
+        wl = workloads.get("qwen3_14b")
+        store = staging.load_store(wl, api)
+        yield wl, store
+        store.destroy()
+
+    def test_fused_parity(self, api, loaded):
+        wl, store = loaded
+        st = gh.check_fused_workload(api, wl, store, sample_tokens=200)
+        assert st["tokens"] > 50 * 10
+
+
 @pytest.mark.slow
 class TestCapacity:
     @pytest.fixture(scope="class")

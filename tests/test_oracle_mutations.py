@@ -157,3 +157,37 @@ def test_mutation_scatter_drops_rotation_or_copy(monkeypatch, which):
         monkeypatch.setattr(inject, "inject", wrong)
         assert _fails(pins.test_inject_tiny_canaries_and_copies, "f32")
         assert _fails(pins.test_theorem3_injection_equals_prompt_prefill, 0, False)
+
+
+def test_mutation_e4m3_ties_away_from_zero(monkeypatch):
+    orig = numerics.f64_to_e4m3_bits
+
+    def wrong(x):
+        # nudge every exact tie upwards in magnitude before the correct rounding
+        x = np.asarray(x, dtype=np.float64)
+        return orig(x * (1 + 2.0 ** -40))
+    monkeypatch.setattr(numerics, "f64_to_e4m3_bits", wrong)
+    assert _fails(pins.test_e4m3_rounding_golden)
+
+
+def test_mutation_e4m3_without_saturation(monkeypatch):
+    orig = numerics.f64_to_e4m3_bits
+
+    def wrong(x):
+        x = np.asarray(x, dtype=np.float64)
+        return np.where(np.abs(x) > 464, np.uint8(0x7F), orig(x)).astype(np.uint8)   # overflow -> NaN
+    monkeypatch.setattr(numerics, "f64_to_e4m3_bits", wrong)
+    assert _fails(pins.test_e4m3_rounding_golden)
+    assert _fails(pins.test_inject_fp8_cache_quantises_scaled_values)
+
+
+def test_mutation_e4m3_exponent_bias(monkeypatch):
+    orig = numerics.e4m3_bits_to_f64
+    monkeypatch.setattr(numerics, "e4m3_bits_to_f64", lambda b: orig(b) * 2.0)      # bias 6 for 7
+    assert _fails(pins.test_e4m3_decode_roundtrip_all_codes)
+
+
+def test_mutation_fp8_value_scale_multiplied(monkeypatch):
+    orig = inject.e4m3_value
+    monkeypatch.setattr(inject, "e4m3_value", lambda v, dt, s: orig(v, dt, 1.0 / s))
+    assert _fails(pins.test_inject_fp8_cache_quantises_scaled_values)

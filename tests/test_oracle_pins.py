@@ -64,6 +64,84 @@ def test_ulp_closed_forms():
     assert numerics.ulp(np.array([0.0]), "bf16")[0] == 2.0 ** -133
 
 
+# ---------------------------------------------------------------- FP8 E4M3 format
+
+def test_e4m3_rounding_golden():
+    for row in _rows("e4m3_rne_sat.txt"):
+        x = float(row[0])
+        want = int(row[1], 16)
+        got = int(numerics.f64_to_e4m3_bits(np.array([x]))[0])
+        assert got == want, (row, hex(got))
+
+
+def test_e4m3_decode_roundtrip_all_codes():
+    bits = np.arange(256, dtype=np.uint8)
+    vals = numerics.e4m3_bits_to_f64(bits)
+    nan = np.isnan(vals)
+    assert np.array_equal(np.nonzero(nan)[0], [0x7F, 0xFF])
+    assert np.array_equal(numerics.f64_to_e4m3_bits(vals[~nan]), bits[~nan])
+    pos = vals[:0x7F]
+    assert np.all(np.diff(pos) > 0) and pos[0] == 0.0 and pos[-1] == 448.0
+
+
+def test_e4m3_matches_torch_float8_within_range():
+    torch = pytest.importorskip("torch")
+    if not hasattr(torch, "float8_e4m3fn"):
+        pytest.skip("torch without float8_e4m3fn")
+    rng = np.random.default_rng(3)
+    x = np.concatenate([rng.standard_normal(20000) * 4, rng.uniform(-448, 448, 5000),
+                        rng.standard_normal(5000) * 2e-3]).astype(np.float32)
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = numerics.f64_to_e4m3_bits(x.astype(np.float64))
+    assert np.array_equal(got, ref)
+    dec = torch.arange(256, dtype=torch.int32).to(torch.uint8).view(torch.float8_e4m3fn).float().numpy()
+    ours = numerics.e4m3_bits_to_f64(np.arange(256, dtype=np.uint8))
+    fin = ~np.isnan(ours)
+    assert np.array_equal(np.isnan(dec), ~fin) and np.array_equal(dec[fin].astype(np.float64), ours[fin])
+
+
+def test_e4m3_ulp_closed_forms():
+    assert numerics.ulp(np.array([1.0]), "e4m3")[0] == 2.0 ** -3
+    assert numerics.ulp(np.array([448.0]), "e4m3")[0] == 32.0
+    assert numerics.ulp(np.array([2.0 ** -7]), "e4m3")[0] == 2.0 ** -9
+    assert numerics.ulp(np.array([0.0]), "e4m3")[0] == 2.0 ** -9
+
+
+def test_inject_fp8_cache_quantises_scaled_values():
+    """E4M3 cache: K is the rotated key / k_scale rounded once; V is
+    fp32(v) / fp32(v_scale) rounded; untouched rows keep the canary."""
+    rng = np.random.default_rng(11)
+    L, H, D, bs, NB = 2, 2, 8, 4, 6
+    lengths = np.array([3, 4])
+    store = {f: (numerics.encode(rng.standard_normal((lengths[f], L, H, D)) * 3, "bf16"),
+                 numerics.encode(rng.standard_normal((lengths[f], L, H, D)) * 3, "bf16")) for f in range(2)}
+    cache = np.full((L, 2, NB, bs, H, D), 0x7F, dtype=np.uint8)
+    before = cache.copy()
+    row = [2, 5, 0, 1, 3, 4]
+    w = rope.inv_freq(D, 1e4)
+    ks, vs = 0.37, 0.011                     # the V scale drives values past 448: saturation
+    plan, T, slots = inject.inject(cache, "bf16", lambda f: store[f], [1, 0], lengths, 5, row, bs, w, 0,
+                                   cache_dtype="e4m3", k_scale=ks, v_scale=vs)
+    touched = np.zeros(cache.shape, dtype=bool)
+    saturated = 0
+    for (f, j, p), s in zip(plan, slots):
+        blk, off = divmod(int(s), bs)
+        touched[:, :, blk, off] = True
+        krot = rope.rotate(numerics.decode(store[f][0][j], "bf16"), p, w, 0)
+        kq = numerics.e4m3_bits_to_f64(cache[:, 0, blk, off])
+        # one rounding of k / k_scale: within half an E4M3 ulp
+        assert np.all(np.abs(kq - krot / np.float32(ks)) <= 0.5 * numerics.ulp(kq, "e4m3") + 1e-12)
+        v = numerics.decode(store[f][1][j], "bf16")
+        vq = numerics.e4m3_bits_to_f64(cache[:, 1, blk, off])
+        target = (v.astype(np.float32) / np.float32(vs)).astype(np.float64)
+        sat = np.abs(target) > 448
+        saturated += int(sat.sum())
+        assert np.all(vq[sat] == np.sign(target[sat]) * 448.0)
+        assert np.all(np.abs(vq - target)[~sat] <= 0.5 * numerics.ulp(vq, "e4m3")[~sat])
+    assert saturated > 0
+    assert np.array_equal(cache[~touched], before[~touched])
+
+
 # ---------------------------------------------------------------- frequencies
 
 def test_inv_freq_plain_closed_forms():
