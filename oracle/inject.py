@@ -20,10 +20,12 @@ Readings where the pages are silent:
 
 An FP8 E4M3 cache (vLLM's 8-bit KV cache; the pages do not treat it) stores
 x / scale with one scale for K and one for V, rounded to nearest even and
-saturated to +-448.  The rotated key is divided in fp64 like the rest of the
-rotation; for V, whose byte is a quantised code of a stored value, the
-division is taken in fp32 (IEEE, correctly rounded) as the kernel takes it,
-so both sides make the same rounding decision from the same number.
+saturated to +-448.  The division is taken as a multiplication by the
+reciprocal rounded once to fp32, r = fp32(1 / scale) (equal to the division
+for power-of-two scales such as vLLM's default 1.0).  The rotated key is
+multiplied in fp64 like the rest of the rotation; for V, whose byte is a
+quantised code of a stored value, the product fp32(v) * r is taken in fp32
+as the kernel takes it, so both sides round the same number.
 """
 from __future__ import annotations
 
@@ -55,16 +57,21 @@ def rotated_key_rows(k_token: np.ndarray, position: int, freqs: np.ndarray, styl
     return rope.rotate(numerics.decode(k_token, kv_dtype), position, freqs, style)
 
 
+def scale_reciprocal(scale: float) -> np.float32:
+    """fp32(1 / scale) of an fp32 scale, the reciprocal taken in fp64."""
+    return np.float32(1.0 / float(np.float32(scale)))
+
+
 def e4m3_key(k_rot: np.ndarray, k_scale: float) -> np.ndarray:
-    """Rotated keys (fp64) into E4M3 bits: k / k_scale, rounded once."""
-    return numerics.f64_to_e4m3_bits(k_rot / float(np.float32(k_scale)))
+    """Rotated keys (fp64) into E4M3 bits: k * fp32(1 / k_scale), rounded once."""
+    return numerics.f64_to_e4m3_bits(k_rot * float(scale_reciprocal(k_scale)))
 
 
 def e4m3_value(v_enc: np.ndarray, kv_dtype: str, v_scale: float) -> np.ndarray:
-    """Stored values into E4M3 bits: fp32(v) / fp32(v_scale) in IEEE fp32, then
+    """Stored values into E4M3 bits: fp32(v) * fp32(1 / v_scale) in fp32, then
     rounded to E4M3 (bf16 and fp16 values are exact in fp32)."""
     v32 = numerics.decode(v_enc, kv_dtype).astype(np.float32)
-    return numerics.f64_to_e4m3_bits((v32 / np.float32(v_scale)).astype(np.float64))
+    return numerics.f64_to_e4m3_bits((v32 * scale_reciprocal(v_scale)).astype(np.float64))
 
 
 def inject(cache: np.ndarray, kv_dtype: str, fact_kv, fact_ids, lengths, start: int,

@@ -108,8 +108,8 @@ def test_e4m3_ulp_closed_forms():
 
 
 def test_inject_fp8_cache_quantises_scaled_values():
-    """E4M3 cache: K is the rotated key / k_scale rounded once; V is
-    fp32(v) / fp32(v_scale) rounded; untouched rows keep the canary."""
+    """E4M3 cache: K is the rotated key times fp32(1 / k_scale) rounded once;
+    V is fp32(v) * fp32(1 / v_scale) rounded; untouched rows keep the canary."""
     rng = np.random.default_rng(11)
     L, H, D, bs, NB = 2, 2, 8, 4, 6
     lengths = np.array([3, 4])
@@ -129,11 +129,12 @@ def test_inject_fp8_cache_quantises_scaled_values():
         touched[:, :, blk, off] = True
         krot = rope.rotate(numerics.decode(store[f][0][j], "bf16"), p, w, 0)
         kq = numerics.e4m3_bits_to_f64(cache[:, 0, blk, off])
-        # one rounding of k / k_scale: within half an E4M3 ulp
-        assert np.all(np.abs(kq - krot / np.float32(ks)) <= 0.5 * numerics.ulp(kq, "e4m3") + 1e-12)
+        rk, rv = np.float32(1 / np.float64(np.float32(ks))), np.float32(1 / np.float64(np.float32(vs)))
+        # one rounding of k * r_k: within half an E4M3 ulp
+        assert np.all(np.abs(kq - krot * float(rk)) <= 0.5 * numerics.ulp(kq, "e4m3") + 1e-12)
         v = numerics.decode(store[f][1][j], "bf16")
         vq = numerics.e4m3_bits_to_f64(cache[:, 1, blk, off])
-        target = (v.astype(np.float32) / np.float32(vs)).astype(np.float64)
+        target = (v.astype(np.float32) * rv).astype(np.float64)
         sat = np.abs(target) > 448
         saturated += int(sat.sum())
         assert np.all(vq[sat] == np.sign(target[sat]) * 448.0)
