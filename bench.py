@@ -216,13 +216,14 @@ def run_ours(args, rank, world, local_rank):
     api.is_set_retrieval_mode(store, {"auto": _lib.IS_RETRIEVAL_AUTO, "per_query": _lib.IS_RETRIEVAL_PER_QUERY,
                                       "batched": _lib.IS_RETRIEVAL_BATCHED}[args.retrieval])
     inp = staging.device_inputs(wl, local_rank)
-    cache = staging.canary_cache(wl, local_rank)
+    cache = staging.canary_cache(wl, local_rank, cache_dtype=args.cache_dtype)
     Q, k = s.n_queries, s.k
     ids = torch.empty((Q, k), dtype=torch.int64, device=dev)
     scores = torch.empty((Q, k), dtype=torch.float32, device=dev)
     seg_len = torch.empty(Q, dtype=torch.int32, device=dev)
     rope = staging.rope_params(wl, api)
-    cdesc = api.make_cache_desc(s.block_size, wl.num_blocks, s.kv_dtype)
+    cache_dtype = args.cache_dtype or s.kv_dtype
+    cdesc = api.make_cache_desc(s.block_size, wl.num_blocks, cache_dtype)
     flush = L2Flush(dev)
     stream = torch.cuda.current_stream()
 
@@ -320,8 +321,9 @@ def run_ours(args, rank, world, local_rank):
     result = None
     if rank == 0:
         peaks = measured_peaks()
-        per_tok = 2 * s.token_elems * s.elt_bytes            # K + V read (= bytes written)
-        inject_bytes = 2 * per_tok * tokens_per_step          # read + write per launch
+        per_tok = 2 * s.token_elems * s.elt_bytes            # K + V read per token
+        per_tok_w = 2 * s.token_elems * (1 if cache_dtype == "e4m3" else s.elt_bytes)   # written
+        inject_bytes = (per_tok + per_tok_w) * tokens_per_step  # read + write per launch
         inject_ms = stage_ms["inject"] / max(1, stage_n["inject"])
         achieved = inject_bytes / (inject_ms * 1e-3) / 1e9
         traffic_tok = ncu_traffic_per_token()
@@ -357,7 +359,7 @@ def run_ours(args, rank, world, local_rank):
                 "unit": "GB/s",
                 "frac": achieved / peaks["hbm_gbs"],
                 "frac_of_nominal_8tbs": achieved / 8000.0,
-                "traffic": (traffic_tok * tokens_per_step) if traffic_tok else None,
+                "traffic": (traffic_tok * tokens_per_step) if traffic_tok and cache_dtype == s.kv_dtype else None,
                 "algorithmic_bytes": inject_bytes,
                 "avg_launch_ms": inject_ms,
             }
@@ -388,6 +390,7 @@ def run_ours(args, rank, world, local_rank):
                        f"then {L2_FLUSH_BYTES >> 20} MiB read (clean, cold L2 at each step)"),
                 "parallelism": f"replicas x{world} (one store per GPU, no collective)",
                 "kv_placement": args.kv_placement,
+                "cache_dtype": cache_dtype,
                 "retrieval": args.retrieval,
             },
             "roofline": roofline,
@@ -530,6 +533,8 @@ def main(argv=None):
                     help="model layers (smaller K/V for profiling the retrieval kernels)")
     ap.add_argument("--kv-placement", choices=["device", "host"], default="device",
                     help="where the store's K/V arena lives (host: page-locked host DRAM)")
+    ap.add_argument("--cache-dtype", choices=["e4m3"], default=None,
+                    help="paged-cache type when it differs from the store's (e4m3: FP8, scales 1.0)")
     ap.add_argument("--retrieval", choices=["auto", "per_query", "batched"], default="auto",
                     help="similarity path: per-query kernel, tcgen05 batched contraction, or automatic")
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")

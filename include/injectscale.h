@@ -77,7 +77,10 @@ typedef enum {
 #define IS_ST_COUNT        0x40u  /* n_ids[r] < 0 or > ids_stride */
 #define IS_ST_TIMEOUT      0x80u  /* a bounded device wait gave up */
 
-typedef enum { IS_F32 = 0, IS_BF16 = 1, IS_F16 = 2 } is_dtype_t;
+/* IS_FP8_E4M3 is a paged-cache type only (never a store type): 8-bit floats
+ * in the OCP E4M3 format (no infinities, largest finite 448), the 8-bit KV
+ * cache of vLLM, the engine InferScale injects into. */
+typedef enum { IS_F32 = 0, IS_BF16 = 1, IS_F16 = 2, IS_FP8_E4M3 = 3 } is_dtype_t;
 
 /* Where the store's K/V arena lives (is_store_config_t.kv_placement).
  * InferScale ("Résultats", Scalabilité) offloads the KV store to host DRAM to go past the
@@ -126,8 +129,17 @@ typedef struct {
 typedef struct {
   int32_t block_size;
   int32_t num_blocks;
-  int32_t dtype;             /* is_dtype_t; must equal the store's kv_dtype */
+  int32_t dtype;             /* is_dtype_t: the store's kv_dtype, or IS_FP8_E4M3 for an
+                                IS_BF16 / IS_F16 store (see below) */
+  float k_scale;             /* IS_FP8_E4M3 only: the cache holds K / k_scale and */
+  float v_scale;             /* V / v_scale; finite and > 0 (vLLM's default is 1.0) */
 } is_cache_desc_t;
+/* FP8 cache: each rotated key element k (fp32) and value element v is stored
+ * as E4M3(x * r) with r = fp32(1 / scale) (the reciprocal rounded once from
+ * double; equal to x / scale for power-of-two scales), rounded to nearest
+ * even and saturated to +-448.  Element order and layout are those of the
+ * other caches with 1-byte elements.  The store keeps its 16-bit K/V; only the
+ * cache is 8-bit. */
 
 typedef struct {
   int64_t n_facts, n_tokens;
@@ -279,6 +291,8 @@ is_status_t is_retrieve_and_inject(is_store_t* store, int32_t Q, const int32_t* 
  *   ids_stride           1 <= ids_stride <= IS_NOALLOC_MAX_FACTS
  *   status_out           device uint32, caller-owned: IS_ST_* bits are OR-ed in
  *                        (the caller clears it)
+ *   cache                cache->dtype must equal kv_dtype (no FP8 cache here:
+ *                        IS_ERR_INVALID_ARG)
  * Other arguments as in is_inject (no user check).  Sizes beyond the limits
  * return IS_ERR_UNSUPPORTED before anything is enqueued.  The first call on a
  * device looks up the static array's device address (once per device, under

@@ -12,7 +12,7 @@ IS_OK = 0
 STATUS_NAMES = {0: "IS_OK", 1: "IS_ERR_INVALID_ARG", 2: "IS_ERR_OOM", 3: "IS_ERR_CAPACITY",
                 4: "IS_ERR_OUT_OF_RANGE", 5: "IS_ERR_CUDA", 6: "IS_ERR_TIMEOUT", 7: "IS_ERR_DEVICE",
                 8: "IS_ERR_UNSUPPORTED"}
-IS_F32, IS_BF16, IS_F16 = 0, 1, 2
+IS_F32, IS_BF16, IS_F16, IS_FP8_E4M3 = 0, 1, 2, 3
 IS_ST_FACT_RANGE, IS_ST_FACT_USER, IS_ST_BLOCK_TABLE, IS_ST_BLOCK_ID = 0x01, 0x02, 0x04, 0x08
 IS_ST_USER_RANGE, IS_ST_POSITION, IS_ST_COUNT, IS_ST_TIMEOUT = 0x10, 0x20, 0x40, 0x80
 IS_STAGE_SIMILARITY, IS_STAGE_TOPK, IS_STAGE_PLAN, IS_STAGE_INJECT = 0, 1, 2, 3
@@ -37,7 +37,8 @@ class RopeParams(ctypes.Structure):
 
 
 class CacheDesc(ctypes.Structure):
-    _fields_ = [("block_size", c_int32), ("num_blocks", c_int32), ("dtype", c_int32)]
+    _fields_ = [("block_size", c_int32), ("num_blocks", c_int32), ("dtype", c_int32),
+                ("k_scale", ctypes.c_float), ("v_scale", ctypes.c_float)]
 
 
 class StoreInfo(ctypes.Structure):

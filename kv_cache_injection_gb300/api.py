@@ -14,7 +14,7 @@ import numpy as np
 from . import _lib
 from ._lib import CacheDesc, RopeParams, StoreConfig, StoreInfo
 
-DTYPE_CODES = {"f32": _lib.IS_F32, "bf16": _lib.IS_BF16, "f16": _lib.IS_F16}
+DTYPE_CODES = {"f32": _lib.IS_F32, "bf16": _lib.IS_BF16, "f16": _lib.IS_F16, "e4m3": _lib.IS_FP8_E4M3}
 
 
 class ISError(RuntimeError):
@@ -86,8 +86,11 @@ def make_rope(theta: float, style: int = 0, scaling: int = 0, factor: float = 1.
                       original_max_pos)
 
 
-def make_cache_desc(block_size: int, num_blocks: int, dtype) -> CacheDesc:
-    return CacheDesc(block_size, num_blocks, DTYPE_CODES[dtype] if isinstance(dtype, str) else dtype)
+def make_cache_desc(block_size: int, num_blocks: int, dtype, k_scale: float = 1.0,
+                    v_scale: float = 1.0) -> CacheDesc:
+    """dtype "e4m3" (IS_FP8_E4M3): an FP8 cache holding K / k_scale and V / v_scale."""
+    return CacheDesc(block_size, num_blocks, DTYPE_CODES[dtype] if isinstance(dtype, str) else dtype,
+                     k_scale, v_scale)
 
 
 def is_store_create(config: StoreConfig, device: int = 0, stream=None) -> Store:

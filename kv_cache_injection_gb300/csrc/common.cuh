@@ -4,6 +4,7 @@
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -49,9 +50,11 @@ struct InjectArgs {
   int32_t layer0;               // first layer this call injects
   int32_t n_layers;             // layers this call injects
   int64_t layer_stride;         // bytes between consecutive layers of the destination cache
-  int32_t row_bytes;            // H * D * elt
+  int32_t row_bytes;            // H * D * elt of the store
   int32_t half_vecs;            // NeoX: 16-byte vectors per half head (D / 2 / VE)
   int32_t head_vecs;            // 16-byte vectors per head (D / VE)
+  int32_t cache_row_bytes;      // H * D * elt of the cache (row_bytes, or H * D for FP8)
+  float k_inv, v_inv;           // FP8 cache: fp32(1 / k_scale), fp32(1 / v_scale)
 };
 
 // Segment planning for an explicit fact list (is_inject).
@@ -173,6 +176,22 @@ __device__ __forceinline__ void st_v4(void* ptr, const uint4& v) {
   asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(ptr), "r"(v.x), "r"(v.y),
                "r"(v.z), "r"(v.w)
                : "memory");
+}
+
+__device__ __forceinline__ void st_v2(void* ptr, const uint2& v) {
+  asm volatile("st.global.v2.u32 [%0], {%1, %2};" ::"l"(ptr), "r"(v.x), "r"(v.y) : "memory");
+}
+
+// Eight fp32 values times r into eight FP8 E4M3 bytes (one 8-byte word,
+// element 0 in the lowest byte): one fp32 multiply each, then the hardware
+// conversion, which rounds to nearest even and saturates to +-448.
+__device__ __forceinline__ uint2 to_e4m3x8(const float* x, float r) {
+  uint32_t w[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e)
+    w[e] = __nv_cvt_float2_to_fp8x2(make_float2(__fmul_rn(x[2 * e], r), __fmul_rn(x[2 * e + 1], r)),
+                                    __NV_SATFINITE, __NV_E4M3);
+  return make_uint2(w[0] | (w[1] << 16), w[2] | (w[3] << 16));
 }
 
 __device__ __forceinline__ void prefetch_l2(const void* p) {

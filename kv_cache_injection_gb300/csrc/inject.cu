@@ -259,13 +259,14 @@ struct TokenCursor {
   }
 };
 
-template <typename T, int STYLE>
+template <typename T, int STYLE, bool F8>
 __global__ void __launch_bounds__(kInjectWarpsMax * 32) inject_kernel(const InjectArgs a,
                                                                       const RopeTurns rt, int P) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ int32_t scratch[33];
   constexpr int VE = Vec<T>::N;
   constexpr int NF = STYLE == 0 ? VE : VE / 2;
+  static_assert(!F8 || VE == 8, "an FP8 cache takes 16-bit store rows");
 
   const int nwarps = blockDim.x >> 5;
   const int warp = threadIdx.x >> 5;
@@ -370,9 +371,9 @@ __global__ void __launch_bounds__(kInjectWarpsMax * 32) inject_kernel(const Inje
         }
       }
       const uint32_t kst = stage0 + (uint32_t)s * item_bytes;
-      uint8_t* dk = a.cache + (size_t)m.l * a.layer_stride + (size_t)m.slot * a.row_bytes;
-      uint8_t* dv = dk + (size_t)a.num_blocks * a.block_size * a.row_bytes;
-      if (lane == 0) bulk_store(dv, kst + a.row_bytes, a.row_bytes);
+      uint8_t* dk = a.cache + (size_t)m.l * a.layer_stride + (size_t)m.slot * a.cache_row_bytes;
+      uint8_t* dv = dk + (size_t)a.num_blocks * a.block_size * a.cache_row_bytes;
+      if (!F8 && lane == 0) bulk_store(dv, kst + a.row_bytes, a.row_bytes);
       for (int c = 0; c < vpl; ++c) {
         const int v = c * 32 + lane;
         float x[VE], y[VE];
@@ -395,7 +396,15 @@ __global__ void __launch_bounds__(kInjectWarpsMax * 32) inject_kernel(const Inje
             y[2 * e + 1] = fmaf(w, cs[e], u * sn[e]);
           }
         }
-        st_v4(dk + (size_t)v * 16, Vec<T>::pack(y));
+        if (F8) {
+          // 8-bit cache: V is converted on the way too (no bulk store).
+          float xv[VE];
+          Vec<T>::unpack(ld_shared_v4(kst + a.row_bytes + v * 16), xv);
+          st_v2(dv + (size_t)v * 8, to_e4m3x8(xv, a.v_inv));
+          st_v2(dk + (size_t)v * 8, to_e4m3x8(y, a.k_inv));
+        } else {
+          st_v4(dk + (size_t)v * 16, Vec<T>::pack(y));
+        }
       }
     }
     if (lane == 0) bulk_commit();                 // one bulk group per item (maybe empty)
@@ -442,7 +451,7 @@ constexpr int kHostChunk = 4;
 // Plain 16-byte global load: valid for device memory and for mapped host memory.
 __device__ __forceinline__ uint4 ld_plain(const uint8_t* p) { return *reinterpret_cast<const uint4*>(p); }
 
-template <typename T, int STYLE>
+template <typename T, int STYLE, bool F8>
 __global__ void __launch_bounds__(kHostWarps * 32) inject_host_kernel(const InjectArgs a,
                                                                       const RopeTurns rt) {
   extern __shared__ __align__(16) int32_t off_region[];   // prefix_ints(R, kHostWarps)
@@ -466,7 +475,8 @@ __global__ void __launch_bounds__(kHostWarps * 32) inject_host_kernel(const Inje
   const int vpl = a.row_bytes >> 9;
   const int hv = a.half_vecs;
   const int fbase = STYLE == 0 ? (lane % hv) * VE : (lane % a.head_vecs) * (VE / 2);
-  const size_t plane = (size_t)a.num_blocks * a.block_size * a.row_bytes;
+  static_assert(!F8 || VE == 8, "an FP8 cache takes 16-bit store rows");
+  const size_t plane = (size_t)a.num_blocks * a.block_size * a.cache_row_bytes;
   TokenCursor cur;
   float cs[NF], sn[NF];
   int32_t cur_p = -1;
@@ -490,7 +500,7 @@ __global__ void __launch_bounds__(kHostWarps * 32) inject_host_kernel(const Inje
       }
     }
     const uint8_t* src = a.kv + ((size_t)cur.src * a.L + a.layer0 + l) * 2 * (size_t)a.row_bytes;
-    uint8_t* dk = a.cache + (size_t)l * a.layer_stride + (size_t)cur.slot * a.row_bytes;
+    uint8_t* dk = a.cache + (size_t)l * a.layer_stride + (size_t)cur.slot * a.cache_row_bytes;
     uint8_t* dv = dk + plane;
     for (int c0 = 0; c0 < vpl; c0 += kHostChunk) {
       uint4 kx[kHostChunk], vx[kHostChunk];
@@ -505,7 +515,13 @@ __global__ void __launch_bounds__(kHostWarps * 32) inject_host_kernel(const Inje
       for (int c = 0; c < kHostChunk; ++c)
         if (c0 + c < vpl) {                     // warp-uniform
           const int v = (c0 + c) * 32 + lane;
-          st_v4(dv + (size_t)v * 16, vx[c]);
+          if (F8) {
+            float xv[VE];
+            Vec<T>::unpack(vx[c], xv);
+            st_v2(dv + (size_t)v * 8, to_e4m3x8(xv, a.v_inv));
+          } else {
+            st_v4(dv + (size_t)v * 16, vx[c]);
+          }
           float x[VE], y[VE];
           Vec<T>::unpack(kx[c], x);
           if (STYLE == 0) {
@@ -526,7 +542,10 @@ __global__ void __launch_bounds__(kHostWarps * 32) inject_host_kernel(const Inje
               y[2 * e + 1] = fmaf(w, cs[e], u * sn[e]);
             }
           }
-          st_v4(dk + (size_t)v * 16, Vec<T>::pack(y));
+          if (F8)
+            st_v2(dk + (size_t)v * 8, to_e4m3x8(y, a.k_inv));
+          else
+            st_v4(dk + (size_t)v * 16, Vec<T>::pack(y));
         }
     }
   }
@@ -592,24 +611,24 @@ struct LaunchMemo {
 };
 static std::mutex g_launch_mu;
 
-template <typename T, int STYLE, bool HOST>
+template <typename T, int STYLE, bool F8, bool HOST>
 static LaunchMemo& launch_memo(int dev) {
   static LaunchMemo memo[64];
   return memo[dev & 63];
 }
 
-template <typename T, int STYLE>
+template <typename T, int STYLE, bool F8>
 static cudaError_t launch_inject_t(const InjectArgs& a, const RopeTurns& rt, const LaunchCfg& cfg) {
   const InjectShape sh = inject_shape(a);
   if (sh.warps == 0) return cudaErrorInvalidValue;
-  auto kern = inject_kernel<T, STYLE>;
+  auto kern = inject_kernel<T, STYLE, F8>;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   int per_sm = 0;
   {
     std::lock_guard<std::mutex> lock(g_launch_mu);
-    LaunchMemo& m = launch_memo<T, STYLE, false>(dev);
+    LaunchMemo& m = launch_memo<T, STYLE, F8, false>(dev);
     if (sh.smem > m.smem_set) {
       e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sh.smem);
       if (e != cudaSuccess) return e;
@@ -627,9 +646,9 @@ static cudaError_t launch_inject_t(const InjectArgs& a, const RopeTurns& rt, con
                    cfg.stream, cfg.pdl, a, rt, sh.stages);
 }
 
-template <typename T, int STYLE>
+template <typename T, int STYLE, bool F8>
 static cudaError_t launch_inject_host_t(const InjectArgs& a, const RopeTurns& rt, const LaunchCfg& cfg) {
-  auto kern = inject_host_kernel<T, STYLE>;
+  auto kern = inject_host_kernel<T, STYLE, F8>;
   const size_t smem = (size_t)prefix_ints(a.R, kHostWarps) * 4;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -637,7 +656,7 @@ static cudaError_t launch_inject_host_t(const InjectArgs& a, const RopeTurns& rt
   int per_sm = 0;
   {
     std::lock_guard<std::mutex> lock(g_launch_mu);
-    LaunchMemo& m = launch_memo<T, STYLE, true>(dev);
+    LaunchMemo& m = launch_memo<T, STYLE, F8, true>(dev);
     if (m.occ_smem != smem || m.occ_warps != kHostWarps) {
       e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&m.occ_blocks, kern, kHostWarps * 32, smem);
       if (e != cudaSuccess) return e;
@@ -650,22 +669,31 @@ static cudaError_t launch_inject_host_t(const InjectArgs& a, const RopeTurns& rt
                    cfg.stream, cfg.pdl, a, rt);
 }
 
-template <typename T, int STYLE>
+template <typename T, int STYLE, bool F8>
 static cudaError_t launch_inject_any(const InjectArgs& a, const RopeTurns& rt, bool host_src,
                                      const LaunchCfg& cfg) {
-  return host_src ? launch_inject_host_t<T, STYLE>(a, rt, cfg) : launch_inject_t<T, STYLE>(a, rt, cfg);
+  return host_src ? launch_inject_host_t<T, STYLE, F8>(a, rt, cfg)
+                  : launch_inject_t<T, STYLE, F8>(a, rt, cfg);
+}
+
+template <typename T>
+static cudaError_t launch_inject_styled(const InjectArgs& a, const RopeTurns& rt, int style, bool host_src,
+                                        bool fp8_cache, const LaunchCfg& cfg) {
+  if (fp8_cache) {
+    if constexpr (Vec<T>::N == 8)
+      return style == 0 ? launch_inject_any<T, 0, true>(a, rt, host_src, cfg)
+                        : launch_inject_any<T, 1, true>(a, rt, host_src, cfg);
+    return cudaErrorInvalidValue;               // an FP8 cache takes 16-bit store rows
+  }
+  return style == 0 ? launch_inject_any<T, 0, false>(a, rt, host_src, cfg)
+                    : launch_inject_any<T, 1, false>(a, rt, host_src, cfg);
 }
 
 cudaError_t launch_inject(const InjectArgs& a, const RopeTurns& rt, int kv_dtype, int style,
-                          bool host_src, const LaunchCfg& cfg) {
-  if (kv_dtype == IS_BF16)
-    return style == 0 ? launch_inject_any<__nv_bfloat16, 0>(a, rt, host_src, cfg)
-                      : launch_inject_any<__nv_bfloat16, 1>(a, rt, host_src, cfg);
-  if (kv_dtype == IS_F16)
-    return style == 0 ? launch_inject_any<__half, 0>(a, rt, host_src, cfg)
-                      : launch_inject_any<__half, 1>(a, rt, host_src, cfg);
-  return style == 0 ? launch_inject_any<float, 0>(a, rt, host_src, cfg)
-                    : launch_inject_any<float, 1>(a, rt, host_src, cfg);
+                          bool host_src, bool fp8_cache, const LaunchCfg& cfg) {
+  if (kv_dtype == IS_BF16) return launch_inject_styled<__nv_bfloat16>(a, rt, style, host_src, fp8_cache, cfg);
+  if (kv_dtype == IS_F16) return launch_inject_styled<__half>(a, rt, style, host_src, fp8_cache, cfg);
+  return launch_inject_styled<float>(a, rt, style, host_src, fp8_cache, cfg);
 }
 
 bool inject_shape_ok(int row_bytes, int R) {
@@ -823,6 +851,7 @@ extern "C" is_status_t is_inject_noalloc(
   a.n_layers = num_layers;
   a.layer_stride = 2LL * cache->num_blocks * cache->block_size * row_bytes;
   a.row_bytes = (int32_t)row_bytes;
+  a.cache_row_bytes = (int32_t)row_bytes;
   a.half_vecs = head_dim / 2 / ve;
   a.head_vecs = head_dim / ve;
   RopeTurns rt;
@@ -834,7 +863,7 @@ extern "C" is_status_t is_inject_noalloc(
     rt.lo[i] = (float)(turns - (double)rt.hi[i]);
   }
   const LaunchCfg cfg_dep{stream, d.num_sms, true};
-  if (launch_inject(a, rt, kv_dtype, rope->style, false, cfg_dep) != cudaSuccess)
+  if (launch_inject(a, rt, kv_dtype, rope->style, false, false, cfg_dep) != cudaSuccess)
     return na_fail(IS_ERR_CUDA, "inject launch failed");
   return IS_OK;
 }

@@ -59,9 +59,10 @@ cudaError_t launch_topk_batched(const TopkArgs& ta, int Q, int32_t max_users, in
 
 // Persistent launch: one CTA per SM times the occupancy its shared-memory
 // plan allows.  host_src: the arena a.kv is mapped host memory, read with
-// plain loads instead of bulk copies.
+// plain loads instead of bulk copies.  fp8_cache: the cache is FP8 E4M3
+// (a.cache_row_bytes, a.k_inv, a.v_inv set; 16-bit stores only).
 cudaError_t launch_inject(const InjectArgs& a, const RopeTurns& turns, int kv_dtype, int style,
-                          bool host_src, const LaunchCfg& cfg);
+                          bool host_src, bool fp8_cache, const LaunchCfg& cfg);
 
 // Whether a row of row_bytes (K or V of one layer) and R requests fit the
 // inject kernel's shared-memory plan.

@@ -270,11 +270,25 @@ is_status_t check_cache(const is_store_t* s, const is_cache_desc_t* c, const voi
   if (!c || !kv_cache) return fail(IS_ERR_INVALID_ARG, "cache descriptor or kv_cache is NULL");
   if (c->block_size <= 0 || c->num_blocks <= 0)
     return fail(IS_ERR_INVALID_ARG, "block_size and num_blocks must be > 0");
-  if (c->dtype != s->cfg.kv_dtype)
+  if (c->dtype == IS_FP8_E4M3) {
+    if (s->cfg.kv_dtype != IS_BF16 && s->cfg.kv_dtype != IS_F16)
+      return fail(IS_ERR_UNSUPPORTED, "an FP8 cache takes a bf16 or fp16 store");
+    if (!(c->k_scale > 0.f) || !(c->v_scale > 0.f) || !std::isfinite(c->k_scale) || !std::isfinite(c->v_scale))
+      return fail(IS_ERR_INVALID_ARG, "FP8 cache scales must be finite and > 0");
+  } else if (c->dtype != s->cfg.kv_dtype) {
     return fail(IS_ERR_INVALID_ARG, "cache dtype %d differs from the store's kv dtype %d", c->dtype,
                 s->cfg.kv_dtype);
+  }
   if (((uintptr_t)kv_cache & 15) != 0) return fail(IS_ERR_INVALID_ARG, "kv_cache must be 16-byte aligned");
   return IS_OK;
+}
+
+// Bytes of one (layer, K or V) row of the cache and of one layer of the cache.
+int64_t cache_row_bytes(const is_store_t* s, const is_cache_desc_t* c) {
+  return c->dtype == IS_FP8_E4M3 ? s->row_bytes / s->elt : s->row_bytes;
+}
+int64_t cache_layer_bytes(const is_store_t* s, const is_cache_desc_t* c) {
+  return 2LL * c->num_blocks * c->block_size * cache_row_bytes(s, c);
 }
 
 is_status_t upload_user_index(is_store_t* s, cudaStream_t st) {
@@ -749,13 +763,17 @@ static is_status_t launch_injection(is_store_t* s, int32_t R, const int64_t* ids
   a.n_layers = n_layers;
   a.layer_stride = layer_stride;
   a.row_bytes = (int32_t)s->row_bytes;
+  a.cache_row_bytes = (int32_t)cache_row_bytes(s, cache);
+  a.k_inv = (float)(1.0 / (double)cache->k_scale);
+  a.v_inv = (float)(1.0 / (double)cache->v_scale);
   const int ve = 16 / s->elt;
   a.half_vecs = s->cfg.head_dim / 2 / ve;
   a.head_vecs = s->cfg.head_dim / ve;
   const RopeTurns rt = make_turns(*rope, s->cfg.head_dim);
   const LaunchCfg cfg{stream, s->num_sms, true};      // follows the planning kernel
   StageTimer tm(s, IS_STAGE_INJECT, stream);
-  CUDA_TRY(launch_inject(a, rt, s->cfg.kv_dtype, rope->style, s->cfg.kv_placement == IS_KV_HOST, cfg));
+  CUDA_TRY(launch_inject(a, rt, s->cfg.kv_dtype, rope->style, s->cfg.kv_placement == IS_KV_HOST,
+                         cache->dtype == IS_FP8_E4M3, cfg));
   return IS_OK;
 }
 
@@ -811,7 +829,7 @@ is_status_t is_inject(is_store_t* s, int32_t R, const int64_t* fact_ids, const i
   s->plan_seg_len = seg_len;
   return launch_injection(s, R, fact_ids, ids_stride, seg_len, seg_start, rope, block_table, max_blocks,
                           cache, kv_cache, slot_mapping_out, stream, 0, s->cfg.num_layers,
-                          2LL * cache->num_blocks * cache->block_size * s->row_bytes);
+                          cache_layer_bytes(s, cache));
 }
 
 is_status_t is_inject_layer(is_store_t* s, int32_t layer, int32_t R, const int64_t* fact_ids,
@@ -877,7 +895,7 @@ is_status_t is_retrieve_and_inject(is_store_t* s, int32_t Q, const int32_t* user
   s->plan_seg_len = seg_len;
   return launch_injection(s, Q, ids, k, seg_len, seg_start, rope, block_table, max_blocks, cache,
                           kv_cache, slot_mapping_out, stream, 0, s->cfg.num_layers,
-                          2LL * cache->num_blocks * cache->block_size * s->row_bytes);
+                          cache_layer_bytes(s, cache));
 }
 
 is_status_t is_get_status(is_store_t* s, cudaStream_t stream, uint32_t* bits_out) {

@@ -36,7 +36,7 @@ def _lib():
 
 def torch_dtype(dtype: str):
     import torch
-    return {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}[dtype]
+    return {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16, "e4m3": torch.uint8}[dtype]
 
 
 def fill_kv(out, dtype: str, seed: int, stream_id: int, first: int) -> None:
@@ -108,12 +108,16 @@ def device_inputs(wl: Workload, device: int = 0) -> dict:
                 block_table=torch.from_numpy(np.ascontiguousarray(wl.block_table)).to(dev))
 
 
-def canary_cache(wl: Workload, device: int = 0, num_blocks: int | None = None):
+def canary_cache(wl: Workload, device: int = 0, num_blocks: int | None = None,
+                 cache_dtype: str | None = None):
+    """A paged cache for ``wl`` filled with the canary; ``cache_dtype`` "e4m3"
+    gives an FP8 cache (uint8 elements), else the store's type."""
     import torch
     s = wl.spec
+    dt = cache_dtype or s.kv_dtype
     shape = cache_shape(s, wl.num_blocks if num_blocks is None else num_blocks)
-    cache = torch.empty(shape, dtype=torch_dtype(s.kv_dtype), device=f"cuda:{device}")
-    refill_canary(cache, s.kv_dtype)
+    cache = torch.empty(shape, dtype=torch_dtype(dt), device=f"cuda:{device}")
+    refill_canary(cache, dt)
     return cache
 
 
@@ -121,14 +125,17 @@ def refill_canary(cache, dtype: str) -> None:
     import torch
     if dtype == "f32":
         cache.view(torch.int32).fill_(CANARY_BITS["f32"])
+    elif dtype == "e4m3":
+        cache.fill_(CANARY_BITS["e4m3"])
     else:
         cache.view(torch.int16).fill_(CANARY_BITS[dtype])
 
 
 def cache_bits(cache) -> np.ndarray:
-    """Host copy in storage encoding: float32, float16, or uint16 bits for bf16."""
+    """Host copy in storage encoding: float32, float16, uint16 bits for bf16,
+    uint8 bits for an FP8 cache."""
     import torch
-    if cache.dtype == torch.float32:
+    if cache.dtype in (torch.float32, torch.uint8):
         return cache.cpu().numpy()
     bits = cache.view(torch.int16).cpu().numpy().view(np.uint16)
     return bits.view(np.float16) if cache.dtype == torch.float16 else bits

@@ -256,6 +256,6 @@ def cache_shape(spec: WorkloadSpec, num_blocks: int) -> tuple:
     return (spec.num_layers, 2, num_blocks, spec.block_size, spec.num_kv_heads, spec.head_dim)
 
 
-CANARY_BITS = {"bf16": 0x7FA5, "f16": 0x7E5A, "f32": 0x7FC0A5A5}
+CANARY_BITS = {"bf16": 0x7FA5, "f16": 0x7E5A, "f32": 0x7FC0A5A5, "e4m3": 0x7F}
 """Bit pattern every cache element holds before injection (a NaN payload that
 no finite rotated key or copied value can equal)."""

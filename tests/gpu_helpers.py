@@ -13,7 +13,8 @@ def ensure_built():
     build.build()
 
 
-def run_fused(api, store, wl, inp, cache, k=None, style=None, slot_cap=None):
+def run_fused(api, store, wl, inp, cache, k=None, style=None, slot_cap=None, cache_dtype=None,
+              k_scale=1.0, v_scale=1.0):
     import torch
     dev = cache.device
     Q = int(inp["users"].shape[0])
@@ -24,7 +25,8 @@ def run_fused(api, store, wl, inp, cache, k=None, style=None, slot_cap=None):
     cap = slot_cap or Q * k * int(wl.lengths.max())
     slot_map = torch.full((cap,), -9, dtype=torch.int64, device=dev)
     rope = staging.rope_params(wl, api, style)
-    cdesc = api.make_cache_desc(wl.spec.block_size, cache.shape[2], wl.spec.kv_dtype)
+    cdesc = api.make_cache_desc(wl.spec.block_size, cache.shape[2], cache_dtype or wl.spec.kv_dtype,
+                                k_scale, v_scale)
     api.is_retrieve_and_inject(store, inp["users"], inp["q_emb"], k, inp["seg_start"], rope,
                                inp["block_table"], cdesc, cache, ids, scores, seg_len, slot_map)
     bits = api.is_get_status(store)
@@ -50,6 +52,8 @@ def changed_slots(cache, dtype: str) -> np.ndarray:
     L, _, NB, bs, H, D = cache.shape
     if dtype == "f32":
         b = cache.view(torch.int32).reshape(L, 2, NB * bs, H * D)
+    elif dtype == "e4m3":
+        b = cache.reshape(L, 2, NB * bs, H * D)
     else:
         b = cache.view(torch.int16).reshape(L, 2, NB * bs, H * D)
     canary = CANARY_BITS[dtype]
@@ -68,14 +72,16 @@ def assert_only_slots_changed(cache, dtype: str, slots) -> None:
         f"{int((ch != exp).sum())} cache rows differ from the expected set"
 
 
-def check_fused_workload(api, wl, store, k=None, sample_tokens=160, seed=0):
+def check_fused_workload(api, wl, store, k=None, sample_tokens=160, seed=0, cache_dtype=None,
+                         k_scale=1.0, v_scale=1.0):
     """Fused retrieve + inject of ``wl`` through ``store`` against the oracle:
     every top-k, segment length and slot; a sample of injected tokens; and
     that exactly the targeted cache rows changed.  Returns the cache too."""
     inp = staging.device_inputs(wl)
-    cache = staging.canary_cache(wl)
+    cache = staging.canary_cache(wl, cache_dtype=cache_dtype)
     k = wl.spec.k if k is None else k
-    out = run_fused(api, store, wl, inp, cache, k=k)
+    out = run_fused(api, store, wl, inp, cache, k=k, cache_dtype=cache_dtype, k_scale=k_scale,
+                    v_scale=v_scale)
     assert out["status"] == 0, hex(out["status"])
     swapped = 0
     for q in range(wl.spec.n_queries):
@@ -86,7 +92,7 @@ def check_fused_workload(api, wl, store, k=None, sample_tokens=160, seed=0):
     want_slots = np.concatenate([[e[3] for e in pl] for pl in plans]).astype(np.int64)
     assert np.array_equal(out["slot_map"][: len(want_slots)], want_slots)
     assert len(np.unique(want_slots)) == len(want_slots)
-    assert_only_slots_changed(cache, wl.spec.kv_dtype, want_slots)
+    assert_only_slots_changed(cache, cache_dtype or wl.spec.kv_dtype, want_slots)
     # sampled tokens: first and last token of every segment, plus random ones
     entries = [e for pl in plans for e in pl]
     rng = np.random.default_rng(seed)
@@ -98,6 +104,10 @@ def check_fused_workload(api, wl, store, k=None, sample_tokens=160, seed=0):
         off += len(pl)
     sample = [entries[i] for i in sorted(pick)]
     gk, gv = gather_rows(cache, [e[3] for e in sample])
-    stats = parity.compare_tokens(wl, gk, gv, sample, parity.oracle_freqs(wl), wl.spec.rope.style,
-                                  parity.FactCache(wl))
+    if cache_dtype == "e4m3":
+        stats = parity.compare_tokens_fp8(wl, gk, gv, sample, parity.oracle_freqs(wl), wl.spec.rope.style,
+                                          parity.FactCache(wl), k_scale, v_scale)
+    else:
+        stats = parity.compare_tokens(wl, gk, gv, sample, parity.oracle_freqs(wl), wl.spec.rope.style,
+                                      parity.FactCache(wl))
     return {"tokens": int(lens.sum()), "swapped": swapped, "cache": cache, **stats}

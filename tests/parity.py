@@ -9,7 +9,11 @@ Tolerances (the method is exact, so these only absorb rounding):
 * rotated keys, bf16: |g - o| <= 1 bf16 ulp of o, or |g - o| <= 2^-20 (|a| + |b|)
   where (a, b) is the rotated pair (the fp32-arithmetic floor near
   cancellation, where the ulp of the result is far below the inputs');
-* rotated keys, fp32: |g - o| <= 4 ulp_f32(o) + 2^-22 (|a| + |b|).
+* rotated keys, fp32: |g - o| <= 4 ulp_f32(o) + 2^-22 (|a| + |b|);
+* FP8 E4M3 cache (x stored as E4M3(x * r), r = fp32(1 / scale)): V bytes
+  bit-exact against the oracle's fp32 product; keys |g - t| <= 1 E4M3 ulp of
+  t = o * r, or 2^-20 (|a| + |b|) r near cancellation, and exactly +-448 where
+  |t| > 448 (saturation).
 """
 from __future__ import annotations
 
@@ -136,3 +140,37 @@ def oracle_freqs(wl):
 
 def canary_value(dtype: str):
     return CANARY_BITS[dtype]
+
+
+def check_rotated_e4m3(g_bits, o_f64, x_f64, style: int, k_scale: float) -> dict:
+    """Keys in an E4M3 cache against the oracle's fp64 rotation o."""
+    r = float(oinject.scale_reciprocal(k_scale))
+    g = numerics.e4m3_bits_to_f64(g_bits)
+    t = o_f64 * r
+    D = g.shape[-1]
+    mag = (np.abs(x_f64) + np.abs(x_f64[..., partner_index(D, style)])) * r
+    sat = np.abs(t) > numerics.E4M3_MAX
+    within = np.abs(g - t) <= numerics.ulp(t, "e4m3")
+    ok = np.where(sat, g == np.sign(t) * numerics.E4M3_MAX, within | (np.abs(g - t) <= 2.0 ** -20 * mag))
+    bad = np.argwhere(~ok)
+    assert bad.size == 0, (f"{len(bad)} FP8 keys out of tolerance, first at {bad[0]}: "
+                           f"gpu {g[tuple(bad[0])]!r} oracle {t[tuple(bad[0])]!r}")
+    return {"n": int(g.size), "within_1ulp": int((within & ~sat).sum()), "saturated": int(sat.sum())}
+
+
+def compare_tokens_fp8(wl, gathered_k, gathered_v, entries, freqs, style: int, facts: FactCache,
+                       k_scale: float, v_scale: float) -> dict:
+    """As compare_tokens, for an E4M3 cache (gathered rows are uint8 bits)."""
+    dtype = wl.spec.kv_dtype
+    stats = {"n": 0, "within_1ulp": 0, "saturated": 0, "v_saturated": 0}
+    for i, (f, j, p, _) in enumerate(entries):
+        Kj, Vj = facts.token(f, j)
+        want_v = oinject.e4m3_value(Vj, dtype, v_scale)
+        assert np.array_equal(np.asarray(gathered_v[i]), want_v), f"FP8 V of fact {f} token {j} differs"
+        stats["v_saturated"] += int((np.abs(numerics.e4m3_bits_to_f64(want_v)) == numerics.E4M3_MAX).sum())
+        x = numerics.decode(Kj, dtype)
+        o = oinject.rotated_key_rows(Kj, p, freqs, style, dtype)
+        st = check_rotated_e4m3(gathered_k[i], o, x, style, k_scale)
+        for key in ("n", "within_1ulp", "saturated"):
+            stats[key] += st[key]
+    return stats

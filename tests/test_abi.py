@@ -41,7 +41,7 @@ def test_status_strings(lib):
 def test_struct_layouts_match_header():
     assert ctypes.sizeof(_lib.StoreConfig) == 72
     assert ctypes.sizeof(_lib.RopeParams) == 48
-    assert ctypes.sizeof(_lib.CacheDesc) == 12
+    assert ctypes.sizeof(_lib.CacheDesc) == 20
     assert ctypes.sizeof(_lib.StoreInfo) == 64
 
 
