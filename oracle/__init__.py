@@ -19,7 +19,11 @@ LLM Serving" (arXiv 2607.27090), as summarised on the pages:
 * the scatter-copy of the composed K/V into a vLLM-style paged KV cache
   ("Méthodologie", phase 2, "Injection") (``inject``);
 * Theorem 3 / Theorem 6 self-checks on a tiny one-layer causal attention
-  (``attention``).
+  (``attention``);
+* Context-Window Encoding ("Méthodologie", phase 1): each fact encoded with a
+  window of w preceding turns, only the fact's pre-RoPE K/V kept (``cwe``),
+  on a tiny multi-layer decoder with synthetic weights (``model``);
+* storage encodings, including the FP8 E4M3 cache (``numerics``).
 
 Every function is pinned by ``tests/test_oracle_*.py`` against closed forms,
 hand-computed values, invariants and brute force; none is "parity unpinned".
