@@ -189,6 +189,47 @@ is_status_t is_store_add_facts(is_store_t* store, int32_t user, int32_t n,
 
 is_status_t is_store_info(const is_store_t* store, is_store_info_t* out);
 
+/* ---- Context-Window Encoding capture ----------------------------------------
+ * InferScale ("Méthodologie", phase 1, "Encodage de la Fenêtre de Contexte")
+ * encodes each memory fact together with a window of w preceding conversation
+ * turns, so that the stored K/V carry the context that disambiguates the fact,
+ * and keeps only the fact's tokens: the window's are dropped.  The encoder is
+ * the serving engine's own prefill; these calls take its output one layer at a
+ * time, as a layer-wise KV connector hands it over, and store the facts.
+ *
+ * is_store_capture_begin: opens a capture of n facts of `user`.
+ *   window_host, lengths_host  host int32[n]: tokens of each fact's window (>= 0)
+ *                              and of the fact (>= 1).  Encoded sequence i is
+ *                              [window_i tokens || lengths_i tokens]; the layer
+ *                              buffers hold the sequences back to back.
+ *   emb                        device or host, [n][E] in emb_dtype
+ * The facts' embeddings and metadata are written now but the facts stay
+ * invisible to retrieval until is_store_capture_end.  n <= IS_MAX_CAPTURE_FACTS.
+ * While a capture is open, is_store_add_facts and a second begin fail with
+ * IS_ERR_INVALID_ARG.  Errors otherwise as is_store_add_facts.  Synchronous.
+ *
+ * is_store_capture_layer: one layer of the encoder's output.
+ *   k_pre_rope, v   device (or mapped host) [sum(window_i + lengths_i)][H][D] in
+ *                   kv_dtype, 16-byte aligned: keys intercepted before RoPE
+ * Each layer is captured exactly once per capture (IS_ERR_INVALID_ARG
+ * otherwise).  Asynchronous on stream; the buffers must stay valid until the
+ * work on stream has run.
+ *
+ * is_store_capture_end: publishes the facts (retrievable by the next call) and
+ * writes their ids to ids_out (host int64[n], may be NULL).  If a layer was not
+ * captured it returns IS_ERR_INVALID_ARG and drops the capture: the store is as
+ * before begin.  Synchronous.
+ *
+ * is_store_capture_abort: drops an open capture (no-op if none). */
+#define IS_MAX_CAPTURE_FACTS 65536
+is_status_t is_store_capture_begin(is_store_t* store, int32_t user, int32_t n,
+                                   const int32_t* window_host, const int32_t* lengths_host,
+                                   const void* emb, cudaStream_t stream);
+is_status_t is_store_capture_layer(is_store_t* store, int32_t layer, const void* k_pre_rope,
+                                   const void* v, cudaStream_t stream);
+is_status_t is_store_capture_end(is_store_t* store, int64_t* ids_out, cudaStream_t stream);
+is_status_t is_store_capture_abort(is_store_t* store);
+
 /* ---- is_retrieve_topk -------------------------------------------------------
  * For each query q, the cosine similarity of q_emb[q] with every stored
  * embedding of user users[q], then the k best (InferScale retrieves the

@@ -18,6 +18,7 @@ IS_ST_USER_RANGE, IS_ST_POSITION, IS_ST_COUNT, IS_ST_TIMEOUT = 0x10, 0x20, 0x40,
 IS_STAGE_SIMILARITY, IS_STAGE_TOPK, IS_STAGE_PLAN, IS_STAGE_INJECT = 0, 1, 2, 3
 IS_MAX_K, IS_MAX_QUERIES, IS_MAX_REQUESTS, IS_EMB_TILE = 1024, 1024, 4096, 128
 IS_NOALLOC_MAX_REQUESTS, IS_NOALLOC_MAX_FACTS = 256, 256
+IS_MAX_CAPTURE_FACTS = 65536
 IS_RETRIEVAL_AUTO, IS_RETRIEVAL_PER_QUERY, IS_RETRIEVAL_BATCHED = 0, 1, 2
 IS_KV_DEVICE, IS_KV_HOST = 0, 1
 
@@ -55,6 +56,11 @@ SIGNATURES = {
     "is_store_add_facts": [c_void_p, c_int32, c_int32, POINTER(c_int32), c_void_p, c_void_p,
                            c_void_p, POINTER(c_int64), c_void_p],
     "is_store_info": [c_void_p, POINTER(StoreInfo)],
+    "is_store_capture_begin": [c_void_p, c_int32, c_int32, POINTER(c_int32), POINTER(c_int32), c_void_p,
+                               c_void_p],
+    "is_store_capture_layer": [c_void_p, c_int32, c_void_p, c_void_p, c_void_p],
+    "is_store_capture_end": [c_void_p, POINTER(c_int64), c_void_p],
+    "is_store_capture_abort": [c_void_p],
     "is_retrieve_topk": [c_void_p, c_int32, c_void_p, c_void_p, c_int32, c_void_p, c_void_p,
                          c_void_p],
     "is_inject": [c_void_p, c_int32, c_void_p, c_void_p, c_int32, c_void_p, c_void_p,

@@ -113,6 +113,35 @@ def is_store_add_facts(store: Store, user: int, lengths, k_pre_rope, v, emb, str
     return ids
 
 
+def is_store_capture_begin(store: Store, user: int, window, lengths, emb, stream=None) -> None:
+    """Open a Context-Window Encoding capture of len(lengths) facts of ``user``."""
+    window = np.ascontiguousarray(window, dtype=np.int32)
+    lengths = np.ascontiguousarray(lengths, dtype=np.int32)
+    if window.shape != lengths.shape:
+        raise ValueError("window and lengths must have one entry per fact")
+    _check(_lib.load().is_store_capture_begin(
+        c_void_p(store.handle), int(user), len(lengths),
+        window.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
+        lengths.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)), _ptr(emb), _stream(stream)))
+
+
+def is_store_capture_layer(store: Store, layer: int, k_pre_rope, v, stream=None) -> None:
+    _check(_lib.load().is_store_capture_layer(c_void_p(store.handle), int(layer), _ptr(k_pre_rope), _ptr(v),
+                                              _stream(stream)))
+
+
+def is_store_capture_end(store: Store, n: int, stream=None) -> np.ndarray:
+    ids = np.empty(n, dtype=np.int64)
+    _check(_lib.load().is_store_capture_end(c_void_p(store.handle),
+                                            ids.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)),
+                                            _stream(stream)))
+    return ids
+
+
+def is_store_capture_abort(store: Store) -> None:
+    _check(_lib.load().is_store_capture_abort(c_void_p(store.handle)))
+
+
 def is_store_info(store: Store) -> dict:
     info = StoreInfo()
     _check(_lib.load().is_store_info(c_void_p(store.handle), byref(info)))

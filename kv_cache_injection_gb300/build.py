@@ -25,7 +25,7 @@ SYNTH_LIB = os.path.join(ROOT, "synth", "lib", "libsynthgen.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
                      "--expt-relaxed-constexpr", "-I" + INCLUDE, "-I" + CSRC]
-SOURCES = ["store.cu", "retrieve.cu", "inject.cu", "simgemm.cu"]
+SOURCES = ["store.cu", "retrieve.cu", "inject.cu", "simgemm.cu", "capture.cu"]
 HEADERS = [os.path.join(INCLUDE, "injectscale.h")] + [
     os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".cuh", ".h"))]
 

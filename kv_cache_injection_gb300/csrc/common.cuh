@@ -57,6 +57,20 @@ struct InjectArgs {
   float k_inv, v_inv;           // FP8 cache: fp32(1 / k_scale), fp32(1 / v_scale)
 };
 
+// One layer of a Context-Window Encoding capture (is_store_capture_layer).
+struct CaptureArgs {
+  const uint8_t* k;             // engine layer output [src tokens][H][D], keys before RoPE
+  const uint8_t* v;             // [src tokens][H][D]
+  uint8_t* kv;                  // store arena [max_tokens][L][2][H][D]
+  const int64_t* seg;           // [n][2]: first source token of the fact's tokens, first arena token
+  int32_t n;                    // facts
+  int64_t tok0;                 // arena token of the first fact's first token
+  int64_t tokens;               // fact tokens (contiguous in the arena from tok0)
+  int32_t L;
+  int32_t layer;
+  int32_t row_bytes;            // H * D * elt
+};
+
 // Segment planning for an explicit fact list (is_inject).
 struct PlanArgs {
   const int64_t* ids;

@@ -64,6 +64,9 @@ cudaError_t launch_topk_batched(const TopkArgs& ta, int Q, int32_t max_users, in
 cudaError_t launch_inject(const InjectArgs& a, const RopeTurns& turns, int kv_dtype, int style,
                           bool host_src, bool fp8_cache, const LaunchCfg& cfg);
 
+// Context-Window Encoding capture: the fact tokens' rows of one layer into the arena.
+cudaError_t launch_capture_layer(const CaptureArgs& a, const LaunchCfg& cfg);
+
 // Whether a row of row_bytes (K or V of one layer) and R requests fit the
 // inject kernel's shared-memory plan.
 bool inject_shape_ok(int row_bytes, int R);

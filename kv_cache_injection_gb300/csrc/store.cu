@@ -60,6 +60,17 @@ struct EventPair {
 
 }  // namespace
 
+// Facts written to the device but not yet visible to retrieval: their embedding
+// rows, tiles and arena tokens follow the store's current counters.
+struct PendingFacts {
+  int32_t user = -1;
+  int32_t n = 0;
+  int64_t f0 = 0, tok0 = 0, tokens = 0;
+  int32_t max_len = 0;
+  int32_t tiles_used = 0;
+  std::vector<int32_t> rows, new_tiles;
+};
+
 struct is_store {
   is_store_config_t cfg{};
   int device = 0;
@@ -117,6 +128,13 @@ struct is_store {
   int32_t max_user_tiles = 0;
   int64_t max_user_facts = 0;
 
+  // open Context-Window Encoding capture
+  bool cap_open = false;
+  int64_t cap_src_tokens = 0;
+  std::vector<uint8_t> cap_layers;
+  int64_t* cap_seg = nullptr;     // [IS_MAX_CAPTURE_FACTS][2] {first source token, first arena token}
+  PendingFacts cap_pending;
+
   bool timing = false;
   std::vector<EventPair> pending[IS_NUM_STAGES];
   std::vector<cudaEvent_t> event_pool;
@@ -168,7 +186,8 @@ void free_store(is_store_t* s) {
   void* ptrs[] = {s->kv, s->fact_tok, s->fact_len, s->fact_user, s->emb, s->emb_inv_norm,
                   s->tile_fact, s->tile_len, s->user_meta, s->tile_tok, s->fact_src, s->user_tiles, s->scores,
                   s->ids_tmp, s->scores_tmp, s->fact_seg_off, s->n_ids, s->seg_len_tmp,
-                  s->rows_tmp, s->status, s->arrive, s->qg, s->q_inv, s->qperm, s->groups, s->counts};
+                  s->rows_tmp, s->status, s->arrive, s->qg, s->q_inv, s->qperm, s->groups, s->counts,
+                  s->cap_seg};
   for (void* p : ptrs)
     if (p) cudaFree(p);
   for (int st = 0; st < IS_NUM_STAGES; ++st)
@@ -449,6 +468,7 @@ is_status_t is_store_create(const is_store_config_t* config, int device, cudaStr
   ALLOC(qperm, Q * 4, "query order");
   ALLOC(groups, Q * sizeof(int4), "query groups");
   ALLOC(counts, 8, "group counts");
+  ALLOC(cap_seg, (size_t)std::min<int64_t>(c.max_facts, IS_MAX_CAPTURE_FACTS) * 16, "capture segments");
 #undef ALLOC
   s->scratch_bytes = (int64_t)(Q * s->score_stride * 4 + Q * c.max_k * 12 +
                                R * (s->seg_stride * 4 + 8) + (size_t)c.max_facts * 4 + 4);
@@ -491,12 +511,11 @@ is_status_t is_store_info(const is_store_t* s, is_store_info_t* out) {
   return IS_OK;
 }
 
-is_status_t is_store_add_facts(is_store_t* s, int32_t user, int32_t n, const int32_t* lengths,
-                               const void* k, const void* v, const void* emb, int64_t* ids_out,
-                               cudaStream_t stream) {
-  if (!s) return fail(IS_ERR_INVALID_ARG, "NULL store");
-  if (n <= 0 || !lengths || !k || !v || !emb)
-    return fail(IS_ERR_INVALID_ARG, "n must be > 0 and lengths, k, v, emb non-NULL");
+// Validates n facts of one user and writes everything but their K/V: the
+// embedding rows (and their norms), the per-fact table and the row -> fact
+// map.  Nothing becomes visible until commit_facts.  Synchronous.
+static is_status_t stage_facts(is_store_t* s, int32_t user, int32_t n, const int32_t* lengths,
+                               const void* emb, cudaStream_t stream, PendingFacts* pf) {
   if (user < 0 || user >= s->cfg.max_users)
     return fail(IS_ERR_OUT_OF_RANGE, "user %d outside [0, %d)", user, s->cfg.max_users);
   int64_t tokens = 0;
@@ -533,13 +552,6 @@ is_status_t is_store_add_facts(is_store_t* s, int32_t user, int32_t n, const int
     }
   }
   DeviceGuard g(s->device);
-  const int L = s->cfg.num_layers;
-  // K and V into the token-major arena [T][L][2][H][D].
-  uint8_t* dst = s->kv + (size_t)s->n_tokens * s->tok_bytes;
-  CUDA_TRY(cudaMemcpy2DAsync(dst, 2 * s->row_bytes, k, s->row_bytes, s->row_bytes,
-                             (size_t)tokens * L, cudaMemcpyDefault, stream));
-  CUDA_TRY(cudaMemcpy2DAsync(dst + s->row_bytes, 2 * s->row_bytes, v, s->row_bytes, s->row_bytes,
-                             (size_t)tokens * L, cudaMemcpyDefault, stream));
   // Embeddings, one copy per run of consecutive rows.
   const size_t erow = (size_t)s->cfg.emb_dim * s->emb_elt;
   for (int i = 0; i < n;) {
@@ -577,23 +589,142 @@ is_status_t is_store_add_facts(is_store_t* s, int32_t user, int32_t n, const int
   CUDA_TRY(launch_emb_norms(s->emb, s->cfg.emb_dtype, s->cfg.emb_dim, s->rows_tmp, n,
                             s->emb_inv_norm, stream));
   CUDA_TRY(cudaStreamSynchronize(stream));
+  pf->user = user;
+  pf->n = n;
+  pf->f0 = f0;
+  pf->tok0 = s->n_tokens;
+  pf->tokens = tokens;
+  pf->max_len = max_len;
+  pf->tiles_used = tiles_used;
+  pf->rows = std::move(rows);
+  pf->new_tiles = std::move(new_tiles);
+  return IS_OK;
+}
 
-  // Commit the host mirror only once every copy succeeded.
-  for (int32_t t : new_tiles) {
+// Makes staged facts (whose K/V are in place) visible to retrieval.
+static is_status_t commit_facts(is_store_t* s, const PendingFacts& pf, int64_t* ids_out, cudaStream_t stream) {
+  const int32_t user = pf.user;
+  for (int32_t t : pf.new_tiles) {
     s->user_tiles_h[user].push_back(t);
     s->tile_rows_h.push_back(0);
   }
-  for (int i = 0; i < n; ++i) s->tile_rows_h[rows[i] / kTile] = rows[i] % kTile + 1;
-  s->n_tiles = tiles_used;
-  s->user_nfacts_h[user] += n;
+  for (int i = 0; i < pf.n; ++i) s->tile_rows_h[pf.rows[i] / kTile] = pf.rows[i] % kTile + 1;
+  s->n_tiles = pf.tiles_used;
+  s->user_nfacts_h[user] += pf.n;
   s->max_user_tiles = std::max<int32_t>(s->max_user_tiles, (int32_t)s->user_tiles_h[user].size());
   s->max_user_facts = std::max<int64_t>(s->max_user_facts, s->user_nfacts_h[user]);
-  s->max_len = std::max(s->max_len, max_len);
-  s->n_facts += n;
-  s->n_tokens += tokens;
+  s->max_len = std::max(s->max_len, pf.max_len);
+  s->n_facts += pf.n;
+  s->n_tokens += pf.tokens;
   if (ids_out)
-    for (int i = 0; i < n; ++i) ids_out[i] = f0 + i;
+    for (int i = 0; i < pf.n; ++i) ids_out[i] = pf.f0 + i;
+  DeviceGuard g(s->device);
   return upload_user_index(s, stream);
+}
+
+is_status_t is_store_add_facts(is_store_t* s, int32_t user, int32_t n, const int32_t* lengths,
+                               const void* k, const void* v, const void* emb, int64_t* ids_out,
+                               cudaStream_t stream) {
+  if (!s) return fail(IS_ERR_INVALID_ARG, "NULL store");
+  if (n <= 0 || !lengths || !k || !v || !emb)
+    return fail(IS_ERR_INVALID_ARG, "n must be > 0 and lengths, k, v, emb non-NULL");
+  if (s->cap_open) return fail(IS_ERR_INVALID_ARG, "a capture is open; end or abort it first");
+  PendingFacts pf;
+  is_status_t st = stage_facts(s, user, n, lengths, emb, stream, &pf);
+  if (st != IS_OK) return st;
+  DeviceGuard g(s->device);
+  const int L = s->cfg.num_layers;
+  // K and V into the token-major arena [T][L][2][H][D].
+  uint8_t* dst = s->kv + (size_t)pf.tok0 * s->tok_bytes;
+  CUDA_TRY(cudaMemcpy2DAsync(dst, 2 * s->row_bytes, k, s->row_bytes, s->row_bytes,
+                             (size_t)pf.tokens * L, cudaMemcpyDefault, stream));
+  CUDA_TRY(cudaMemcpy2DAsync(dst + s->row_bytes, 2 * s->row_bytes, v, s->row_bytes, s->row_bytes,
+                             (size_t)pf.tokens * L, cudaMemcpyDefault, stream));
+  CUDA_TRY(cudaStreamSynchronize(stream));
+  return commit_facts(s, pf, ids_out, stream);
+}
+
+// ---------------------------------------------------------------------------
+// Context-Window Encoding capture.
+
+is_status_t is_store_capture_begin(is_store_t* s, int32_t user, int32_t n, const int32_t* window,
+                                   const int32_t* lengths, const void* emb, cudaStream_t stream) {
+  if (!s) return fail(IS_ERR_INVALID_ARG, "NULL store");
+  if (s->cap_open) return fail(IS_ERR_INVALID_ARG, "a capture is already open");
+  if (n <= 0 || !window || !lengths || !emb)
+    return fail(IS_ERR_INVALID_ARG, "n must be > 0 and window, lengths, emb non-NULL");
+  if (n > IS_MAX_CAPTURE_FACTS)
+    return fail(IS_ERR_UNSUPPORTED, "at most %d facts per capture", IS_MAX_CAPTURE_FACTS);
+  if (s->n_facts + n > s->cfg.max_facts)
+    return fail(IS_ERR_CAPACITY, "store holds %lld of %lld facts; %d more do not fit",
+                (long long)s->n_facts, (long long)s->cfg.max_facts, n);
+  std::vector<int64_t> seg(2 * (size_t)n);      // per fact: {source token of its first fact token, its first arena token}
+  int64_t src = 0, dst = s->n_tokens;
+  for (int i = 0; i < n; ++i) {
+    if (window[i] < 0) return fail(IS_ERR_INVALID_ARG, "fact %d has window %d", i, window[i]);
+    if (lengths[i] <= 0) return fail(IS_ERR_INVALID_ARG, "fact %d has length %d", i, lengths[i]);
+    src += window[i];
+    seg[2 * i] = src;
+    seg[2 * i + 1] = dst;
+    src += lengths[i];
+    dst += lengths[i];
+  }
+  if (src > (int64_t)INT32_MAX) return fail(IS_ERR_UNSUPPORTED, "a capture may span at most 2^31-1 tokens");
+  PendingFacts pf;
+  is_status_t st = stage_facts(s, user, n, lengths, emb, stream, &pf);
+  if (st != IS_OK) return st;
+  DeviceGuard g(s->device);
+  CUDA_TRY(cudaMemcpyAsync(s->cap_seg, seg.data(), seg.size() * 8, cudaMemcpyHostToDevice, stream));
+  CUDA_TRY(cudaStreamSynchronize(stream));
+  s->cap_pending = pf;
+  s->cap_src_tokens = src;
+  s->cap_layers.assign(s->cfg.num_layers, 0);
+  s->cap_open = true;
+  return IS_OK;
+}
+
+is_status_t is_store_capture_layer(is_store_t* s, int32_t layer, const void* k_pre_rope, const void* v,
+                                   cudaStream_t stream) {
+  if (!s) return fail(IS_ERR_INVALID_ARG, "NULL store");
+  if (!s->cap_open) return fail(IS_ERR_INVALID_ARG, "no capture is open");
+  if (layer < 0 || layer >= s->cfg.num_layers)
+    return fail(IS_ERR_OUT_OF_RANGE, "layer %d outside [0, %d)", layer, s->cfg.num_layers);
+  if (s->cap_layers[layer]) return fail(IS_ERR_INVALID_ARG, "layer %d was already captured", layer);
+  if (!k_pre_rope || !v) return fail(IS_ERR_INVALID_ARG, "k_pre_rope or v is NULL");
+  if ((((uintptr_t)k_pre_rope) | ((uintptr_t)v)) & 15)
+    return fail(IS_ERR_INVALID_ARG, "k_pre_rope and v must be 16-byte aligned");
+  DeviceGuard g(s->device);
+  CaptureArgs ca{};
+  ca.k = static_cast<const uint8_t*>(k_pre_rope);
+  ca.v = static_cast<const uint8_t*>(v);
+  ca.kv = s->kv;
+  ca.seg = s->cap_seg;
+  ca.n = s->cap_pending.n;
+  ca.tok0 = s->cap_pending.tok0;
+  ca.tokens = s->cap_pending.tokens;
+  ca.L = s->cfg.num_layers;
+  ca.layer = layer;
+  ca.row_bytes = (int32_t)s->row_bytes;
+  CUDA_TRY(launch_capture_layer(ca, LaunchCfg{stream, s->num_sms, false}));
+  s->cap_layers[layer] = 1;
+  return IS_OK;
+}
+
+is_status_t is_store_capture_end(is_store_t* s, int64_t* ids_out, cudaStream_t stream) {
+  if (!s) return fail(IS_ERR_INVALID_ARG, "NULL store");
+  if (!s->cap_open) return fail(IS_ERR_INVALID_ARG, "no capture is open");
+  s->cap_open = false;
+  for (int l = 0; l < s->cfg.num_layers; ++l)
+    if (!s->cap_layers[l]) return fail(IS_ERR_INVALID_ARG, "layer %d was not captured; capture dropped", l);
+  DeviceGuard g(s->device);
+  CUDA_TRY(cudaStreamSynchronize(stream));
+  return commit_facts(s, s->cap_pending, ids_out, stream);
+}
+
+is_status_t is_store_capture_abort(is_store_t* s) {
+  if (!s) return fail(IS_ERR_INVALID_ARG, "NULL store");
+  s->cap_open = false;
+  return IS_OK;
 }
 
 // ---------------------------------------------------------------------------
