@@ -68,10 +68,13 @@ __global__ void __launch_bounds__(256) plan_kernel(const PlanArgs a) {
 // ---------------------------------------------------------------------------
 // Gather + Chunked RoPE + paged scatter.
 //
-// Work item = (segment token t, layer l): the K row and the V row of one layer,
-// H*D elements each, adjacent in the token-major store, so one bulk copy of
-// 2 * row_bytes brings both into shared memory.  Items are numbered t*L + l
-// over all requests back to back and each warp takes one contiguous run.
+// Work item = (segment token t, group of G consecutive layers): per layer the
+// K row and the V row, H*D elements each; a token's layers sit back to back in
+// the token-major store, so one bulk copy of 2 * G * row_bytes brings the
+// group into shared memory.  G is 1 for rows of 2 KiB and more and grows for
+// smaller rows so that one copy moves about 4 KiB (per-item costs are per
+// copy, not per byte).  Items are numbered t * groups + g over all requests
+// back to back and each warp takes one contiguous run.
 //
 // Each warp runs its own pipeline over a ring of P shared-memory stages: lane
 // 0 issues the bulk load of item i + P - 1 while the warp works on item i, so
@@ -89,7 +92,8 @@ constexpr uint64_t kWaitBudgetNs = 2000000000ull;   // 2 s per wait
 struct StageMeta {
   int64_t slot;     // destination slot, -1 = nothing to do
   int32_t p;        // position (rotation angle)
-  int32_t l;        // layer
+  int16_t l;        // first layer of the group (within this call)
+  int16_t nl;       // layers in the group
 };
 
 // x / d for non-negative operands, in 32-bit arithmetic when both fit.
@@ -261,7 +265,7 @@ struct TokenCursor {
 
 template <typename T, int STYLE, bool F8>
 __global__ void __launch_bounds__(kInjectWarpsMax * 32) inject_kernel(const InjectArgs a,
-                                                                      const RopeTurns rt, int P) {
+                                                                      const RopeTurns rt, int P, int G) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ int32_t scratch[33];
   constexpr int VE = Vec<T>::N;
@@ -271,7 +275,7 @@ __global__ void __launch_bounds__(kInjectWarpsMax * 32) inject_kernel(const Inje
   const int nwarps = blockDim.x >> 5;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const uint32_t item_bytes = 2u * (uint32_t)a.row_bytes;
+  const uint32_t item_bytes = 2u * (uint32_t)G * (uint32_t)a.row_bytes;   // one stage
   int32_t* off_region = reinterpret_cast<int32_t*>(smem);
   const size_t off_bytes = ((size_t)prefix_ints(a.R, kInjectWarpsMax) * 4 + 127) & ~(size_t)127;
   uint8_t* stages = smem + off_bytes + (size_t)warp * P * item_bytes;
@@ -293,7 +297,8 @@ __global__ void __launch_bounds__(kInjectWarpsMax * 32) inject_kernel(const Inje
   const int32_t* s_off;
   const int32_t total = segment_prefix(a, off_region, scratch, &s_off);
 
-  const int64_t n_items = (int64_t)total * a.n_layers;
+  const int groups = (a.n_layers + G - 1) / G;   // items per token
+  const int64_t n_items = (int64_t)total * groups;
   const int64_t warp_id = (int64_t)blockIdx.x * nwarps + warp;
   const int64_t n_warps = (int64_t)gridDim.x * nwarps;
   const int64_t chunk = div_nn(n_items + n_warps - 1, n_warps);
@@ -308,16 +313,17 @@ __global__ void __launch_bounds__(kInjectWarpsMax * 32) inject_kernel(const Inje
 
   TokenCursor cur;
 
-  // Next item to issue, as (segment token, layer within this call).
-  int32_t nt = (int32_t)div_nn(it0, a.n_layers);
-  int32_t nl = (int32_t)(it0 - (int64_t)nt * a.n_layers);
+  // Next item to issue, as (segment token, layer group within this call).
+  int32_t nt = (int32_t)div_nn(it0, groups);
+  int32_t ng = (int32_t)(it0 - (int64_t)nt * groups);
 
   // Warp-uniform: resolve the next item's token and have lane 0 start its bulk
   // load into stage s.  Items are issued in order.  Returns true if a load was issued.
   auto issue = [&](int s) -> bool {
-    const int32_t t = nt, l = nl;
-    if (++nl == a.n_layers) {
-      nl = 0;
+    const int32_t t = nt, l = ng * G;
+    const int32_t nlay = min(G, a.n_layers - l);
+    if (++ng == groups) {
+      ng = 0;
       ++nt;
     }
     cur.seek(a, s_off, t, lane);
@@ -328,12 +334,14 @@ __global__ void __launch_bounds__(kInjectWarpsMax * 32) inject_kernel(const Inje
       if (l == 0 && a.slot_mapping) a.slot_mapping[t] = tok_slot;
       meta[s].slot = tok_slot;
       meta[s].p = tok_p;
-      meta[s].l = l;
+      meta[s].l = (int16_t)l;
+      meta[s].nl = (int16_t)nlay;
       if (tok_slot >= 0) {
         const uint32_t bar = smem_addr(&bars[s]);
-        mbar_expect_tx(bar, item_bytes);
+        const uint32_t bytes = 2u * (uint32_t)nlay * (uint32_t)a.row_bytes;
+        mbar_expect_tx(bar, bytes);
         bulk_load(stage0 + (uint32_t)s * item_bytes,
-                  a.kv + ((size_t)tok_src * a.L + a.layer0 + l) * 2 * (size_t)a.row_bytes, item_bytes, bar);
+                  a.kv + ((size_t)tok_src * a.L + a.layer0 + l) * 2 * (size_t)a.row_bytes, bytes, bar);
       }
     }
     return tok_slot >= 0;
@@ -370,40 +378,42 @@ __global__ void __launch_bounds__(kInjectWarpsMax * 32) inject_kernel(const Inje
           sincospif(2.0f * fr, &sn[e], &cs[e]);
         }
       }
-      const uint32_t kst = stage0 + (uint32_t)s * item_bytes;
-      uint8_t* dk = a.cache + (size_t)m.l * a.layer_stride + (size_t)m.slot * a.cache_row_bytes;
-      uint8_t* dv = dk + (size_t)a.num_blocks * a.block_size * a.cache_row_bytes;
-      if (!F8 && lane == 0) bulk_store(dv, kst + a.row_bytes, a.row_bytes);
-      for (int c = 0; c < vpl; ++c) {
-        const int v = c * 32 + lane;
-        float x[VE], y[VE];
-        Vec<T>::unpack(ld_shared_v4(kst + v * 16), x);
-        if (STYLE == 0) {
-          float z[VE];
-          Vec<T>::unpack(ld_shared_v4(kst + (v ^ hv) * 16), z);
-          if ((v & hv) == 0) {
-#pragma unroll
-            for (int e = 0; e < VE; ++e) y[e] = fmaf(x[e], cs[e], -z[e] * sn[e]);
+      for (int gl = 0; gl < m.nl; ++gl) {
+        const uint32_t kst = stage0 + (uint32_t)s * item_bytes + (uint32_t)gl * 2u * (uint32_t)a.row_bytes;
+        uint8_t* dk = a.cache + (size_t)(m.l + gl) * a.layer_stride + (size_t)m.slot * a.cache_row_bytes;
+        uint8_t* dv = dk + (size_t)a.num_blocks * a.block_size * a.cache_row_bytes;
+        if (!F8 && lane == 0) bulk_store(dv, kst + a.row_bytes, a.row_bytes);
+        for (int c = 0; c < vpl; ++c) {
+          const int v = c * 32 + lane;
+          float x[VE], y[VE];
+          Vec<T>::unpack(ld_shared_v4(kst + v * 16), x);
+          if (STYLE == 0) {
+            float z[VE];
+            Vec<T>::unpack(ld_shared_v4(kst + (v ^ hv) * 16), z);
+            if ((v & hv) == 0) {
+  #pragma unroll
+              for (int e = 0; e < VE; ++e) y[e] = fmaf(x[e], cs[e], -z[e] * sn[e]);
+            } else {
+  #pragma unroll
+              for (int e = 0; e < VE; ++e) y[e] = fmaf(x[e], cs[e], z[e] * sn[e]);
+            }
           } else {
-#pragma unroll
-            for (int e = 0; e < VE; ++e) y[e] = fmaf(x[e], cs[e], z[e] * sn[e]);
+  #pragma unroll
+            for (int e = 0; e < VE / 2; ++e) {
+              const float u = x[2 * e], w = x[2 * e + 1];
+              y[2 * e] = fmaf(u, cs[e], -w * sn[e]);
+              y[2 * e + 1] = fmaf(w, cs[e], u * sn[e]);
+            }
           }
-        } else {
-#pragma unroll
-          for (int e = 0; e < VE / 2; ++e) {
-            const float u = x[2 * e], w = x[2 * e + 1];
-            y[2 * e] = fmaf(u, cs[e], -w * sn[e]);
-            y[2 * e + 1] = fmaf(w, cs[e], u * sn[e]);
+          if (F8) {
+            // 8-bit cache: V is converted on the way too (no bulk store).
+            float xv[VE];
+            Vec<T>::unpack(ld_shared_v4(kst + a.row_bytes + v * 16), xv);
+            st_v2(dv + (size_t)v * 8, to_e4m3x8(xv, a.v_inv));
+            st_v2(dk + (size_t)v * 8, to_e4m3x8(y, a.k_inv));
+          } else {
+            st_v4(dk + (size_t)v * 16, Vec<T>::pack(y));
           }
-        }
-        if (F8) {
-          // 8-bit cache: V is converted on the way too (no bulk store).
-          float xv[VE];
-          Vec<T>::unpack(ld_shared_v4(kst + a.row_bytes + v * 16), xv);
-          st_v2(dv + (size_t)v * 8, to_e4m3x8(xv, a.v_inv));
-          st_v2(dk + (size_t)v * 8, to_e4m3x8(y, a.k_inv));
-        } else {
-          st_v4(dk + (size_t)v * 16, Vec<T>::pack(y));
         }
       }
     }
@@ -576,15 +586,25 @@ void prefer_max_shared(const void* kern) {
   }
 }
 
-// Shared memory plan of one inject launch: warps per CTA and stages per warp.
+// Shared memory plan of one inject launch: warps per CTA, stages per warp and
+// layers per work item.
 struct InjectShape {
   int warps;
   int stages;
   size_t smem;
+  int layers_per_item;
 };
 
+// Layers per work item: as many as keep one bulk copy within about 4 KiB.
+static int layers_per_item(const InjectArgs& a) {
+  int g = 1;
+  while (g < 8 && 2 * g < std::max(1, a.n_layers) + 1 && 2 * (size_t)(2 * g) * a.row_bytes <= 4096) g *= 2;
+  return g;
+}
+
 static InjectShape inject_shape(const InjectArgs& a) {
-  const size_t item = 2 * (size_t)a.row_bytes;
+  const int G = layers_per_item(a);
+  const size_t item = 2 * (size_t)G * a.row_bytes;
   const size_t off_bytes = ((size_t)prefix_ints(a.R, kInjectWarpsMax) * 4 + 127) & ~(size_t)127;
   const size_t per_stage = item + 8 + sizeof(StageMeta);
   const size_t stage_budget = 96 * 1024;        // two CTAs per SM
@@ -596,9 +616,9 @@ static InjectShape inject_shape(const InjectArgs& a) {
       --p;
       need = off_bytes + (size_t)w * p * per_stage;
     }
-    if (need <= smem_max) return {w, p, need};
+    if (need <= smem_max) return {w, p, need, G};
   }
-  return {0, 0, 0};
+  return {0, 0, 0, 0};
 }
 
 // Per device and kernel instance: the dynamic shared memory limit already set
@@ -643,7 +663,7 @@ static cudaError_t launch_inject_t(const InjectArgs& a, const RopeTurns& rt, con
     per_sm = m.occ_blocks;
   }
   return launch_ex(kern, dim3(cfg.num_sms * std::max(1, per_sm)), dim3(sh.warps * 32), sh.smem,
-                   cfg.stream, cfg.pdl, a, rt, sh.stages);
+                   cfg.stream, cfg.pdl, a, rt, sh.stages, sh.layers_per_item);
 }
 
 template <typename T, int STYLE, bool F8>
