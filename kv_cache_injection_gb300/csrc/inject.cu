@@ -86,7 +86,7 @@ __global__ void __launch_bounds__(256) plan_kernel(const PlanArgs a) {
 // needs depend only on its lane index, so it computes VE (or VE/2) sin/cos
 // once per position.  Every mbarrier wait is bounded: on time-out the warp
 // latches IS_ST_TIMEOUT, stops issuing, drains its copies and returns.
-constexpr int kInjectWarpsMax = 4;
+constexpr int kInjectWarpsMax = 8;
 constexpr uint64_t kWaitBudgetNs = 2000000000ull;   // 2 s per wait
 
 struct StageMeta {
