@@ -175,8 +175,10 @@ cudaError_t launch_retrieve(const SimArgs& sa, const TopkArgs& ta, int emb_dtype
                             int64_t max_user_facts, int32_t* arrive, const LaunchCfg& cfg) {
   // Split tiles into sub-tiles until the grid covers the SMs a few times over.
   const int tiles = std::max(1, max_user_tiles);
+  // At most one row per warp: a sub-tile keeps every warp of the CTA busy.
+  constexpr int kMaxSub = kTile / (kRetThreads / 32);
   int n_sub = 1;
-  while (n_sub < 16 && (int64_t)tiles * sa.Q * n_sub < 4LL * cfg.num_sms) n_sub *= 2;
+  while (n_sub < kMaxSub && (int64_t)tiles * sa.Q * n_sub < 4LL * cfg.num_sms) n_sub *= 2;
   const dim3 grid(tiles * n_sub, sa.Q);
   if (emb_dtype == IS_F16)
     return launch_retrieve_t<__half>(sa, ta, n_sub, grid, max_user_facts, arrive, cfg);

@@ -33,13 +33,15 @@ __device__ __forceinline__ uint32_t warp_excl_scan(uint32_t x, int lane, uint32_
 
 constexpr int kCandMax = IS_MAX_K;          // candidates sorted exactly (10-bit slot index)
 constexpr int kCosBins = 2048;
+static_assert(kCosBins % kRetThreads == 0 && kRetThreads <= kCandMax && kRetThreads <= 1024,
+              "bins split evenly over the threads; the rank path holds one candidate per thread");
 
 struct TopkShared {
   uint32_t hist[kCosBins];                  // cosine bins; the radix fallback reuses it as [4][256]
   unsigned long long sel[kCandMax];         // (key << 32) | ((2^20-1 - row) << 10) | slot
   unsigned long long cand[kCandMax];        // (length << 32) | fact id, by slot (by rank on the rank path)
+  int64_t rk_tok[kCandMax];                 // rank path: arena token by rank
   int32_t scratch[33];
-  uint32_t wsum[8];
   uint32_t bstar, above, eq, digit, cnt;
 };
 
@@ -135,25 +137,23 @@ __device__ void topk_block(const TopkArgs& a, TopkShared& sh, uint32_t* s_keys, 
     return;
   }
 
-  // B: warp w scans bins 2047 - 256w downwards, lane l eight of them.
+  // B: the bins in descending order, BPT per thread in thread order; a block
+  // scan of the per-thread counts finds the thread holding the k-th score.
   {
-    const int hi = kCosBins - 1 - 256 * warp - 8 * lane;
-    uint32_t c[8], sum = 0;
+    constexpr int BPT = kCosBins / kRetThreads;
+    const int hi = kCosBins - 1 - BPT * tid;
+    uint32_t c[BPT], sum = 0;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
+    for (int i = 0; i < BPT; ++i) {
       c[i] = sh.hist[hi - i];
       sum += c[i];
     }
-    uint32_t wtot;
-    const uint32_t before_l = warp_excl_scan(sum, lane, &wtot);
-    if (lane == 0) sh.wsum[warp] = wtot;
-    __syncthreads();
-    uint32_t before = before_l;
-    for (int w = 0; w < warp; ++w) before += sh.wsum[w];
+    int32_t tot;
+    const uint32_t before = (uint32_t)block_exclusive_scan((int32_t)sum, sh.scratch, &tot);
     if (before < (uint32_t)kk && before + sum >= (uint32_t)kk) {
       uint32_t run = before;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
+      for (int i = 0; i < BPT; ++i) {
         if (run < (uint32_t)kk && run + c[i] >= (uint32_t)kk) {
           sh.bstar = hi - i;
           sh.above = run;
@@ -268,12 +268,12 @@ __device__ void topk_block(const TopkArgs& a, TopkShared& sh, uint32_t* s_keys, 
     // Rank selection: thread t owns candidate t; its rank is the number of
     // candidates above it (entries are unique).  The fact lookup overlaps the
     // ranking.  The top kk are then placed by rank (fact and length in
-    // sh.cand, store token and key in the histogram's space, free by now), so
+    // sh.cand, store token in sh.rk_tok, key in the histogram's space), so
     // thread r writes rank r's outputs and one block scan of the lengths gives
     // the segment offsets.
     const uint32_t t = (uint32_t)tid;
-    int64_t* rk_tok = reinterpret_cast<int64_t*>(sh.hist);          // [256]
-    uint32_t* rk_key = sh.hist + 2 * kRetThreads;                     // [256]
+    int64_t* rk_tok = sh.rk_tok;
+    uint32_t* rk_key = sh.hist;                                       // free by now
     if (t < C) {
       const unsigned long long e = sh.sel[t];
       const uint32_t j = 0xFFFFFu - (uint32_t)((e >> 10) & 0xFFFFFu);
