@@ -185,6 +185,27 @@ def is_retrieve_and_inject(store: Store, users, q_emb, k: int, seg_start, rope: 
         _ptr(slot_mapping_out), _stream(stream)))
 
 
+def prepare_retrieve_and_inject(store: Store, users, q_emb, k: int, seg_start, rope: RopeParams,
+                                block_table, cache: CacheDesc, kv_cache, ids_out=None, scores_out=None,
+                                seg_len_out=None, slot_mapping_out=None, stream=None):
+    """is_retrieve_and_inject with every argument marshalled once: returns a
+    callable that issues the call on the same buffers (whose contents may
+    change between calls) and raises ISError on a non-OK status.  For serving
+    loops that reuse their buffers."""
+    fn = _lib.load().is_retrieve_and_inject
+    args = (c_void_p(store.handle), int(users.shape[0]), _ptr(users), _ptr(q_emb), int(k), _ptr(seg_start),
+            byref(rope), _ptr(block_table), int(block_table.shape[1]), byref(cache), _ptr(kv_cache),
+            _ptr(ids_out), _ptr(scores_out), _ptr(seg_len_out), _ptr(slot_mapping_out), _stream(stream))
+    keep = (rope, cache)                      # the structs must outlive the callable
+
+    def call():
+        st = fn(*args)
+        if st != _lib.IS_OK:
+            _check(st)
+        return keep is not None
+    return call
+
+
 def is_inject_noalloc(kv_arena, fact_tok, fact_len, max_fact_len: int, num_layers: int,
                       num_kv_heads: int, head_dim: int, kv_dtype, fact_ids, n_ids, seg_start,
                       rope: RopeParams, block_table, cache: CacheDesc, kv_cache, status_out,

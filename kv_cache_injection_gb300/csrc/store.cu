@@ -128,6 +128,11 @@ struct is_store {
   int32_t max_user_tiles = 0;
   int64_t max_user_facts = 0;
 
+  // rotation table of the last RoPE parameters seen
+  bool turns_valid = false;
+  is_rope_params_t turns_key{};
+  RopeTurns turns{};
+
   // open Context-Window Encoding capture
   bool cap_open = false;
   int64_t cap_src_tokens = 0;
@@ -269,6 +274,12 @@ is_status_t check_rope(const is_rope_params_t* r, int D, int kv_dtype) {
     return fail(IS_ERR_UNSUPPORTED, "head_dim %d with this dtype/style needs %d vectors per %s", D,
                 vecs, r->style == 0 ? "half head (max 32)" : "head (max 32)");
   return IS_OK;
+}
+
+bool same_rope(const is_rope_params_t& a, const is_rope_params_t& b) {
+  return a.theta == b.theta && a.style == b.style && a.scaling == b.scaling && a.factor == b.factor &&
+         a.low_freq_factor == b.low_freq_factor && a.high_freq_factor == b.high_freq_factor &&
+         a.original_max_pos == b.original_max_pos;
 }
 
 RopeTurns make_turns(const is_rope_params_t& r, int D) {
@@ -900,7 +911,14 @@ static is_status_t launch_injection(is_store_t* s, int32_t R, const int64_t* ids
   const int ve = 16 / s->elt;
   a.half_vecs = s->cfg.head_dim / 2 / ve;
   a.head_vecs = s->cfg.head_dim / ve;
-  const RopeTurns rt = make_turns(*rope, s->cfg.head_dim);
+  // The rotation table of the last RoPE parameters is kept: serving loops pass
+  // the same parameters on every call.
+  if (!s->turns_valid || !same_rope(s->turns_key, *rope)) {
+    s->turns = make_turns(*rope, s->cfg.head_dim);
+    s->turns_key = *rope;
+    s->turns_valid = true;
+  }
+  const RopeTurns& rt = s->turns;
   const LaunchCfg cfg{stream, s->num_sms, true};      // follows the planning kernel
   StageTimer tm(s, IS_STAGE_INJECT, stream);
   CUDA_TRY(launch_inject(a, rt, s->cfg.kv_dtype, rope->style, s->cfg.kv_placement == IS_KV_HOST,
