@@ -115,7 +115,11 @@ typedef struct {
 /* Rotary embedding of the model the facts were encoded with. */
 typedef struct {
   double theta;              /* base, w_i = theta^(-2i/D) */
-  int32_t style;             /* 0 = NeoX half split (i, i+D/2); 1 = interleaved (2i, 2i+1) */
+  int32_t style;             /* 0 = NeoX half split (i, i+D/2); 1 = interleaved (2i, 2i+1).
+                                The kernels take at most 32 16-byte vectors per half head
+                                (NeoX) or per head (interleaved): D <= 512 for 16-bit NeoX,
+                                D <= 256 for 16-bit interleaved and fp32 NeoX, D <= 128 for
+                                fp32 interleaved; larger D returns IS_ERR_UNSUPPORTED */
   int32_t scaling;           /* 0 = none; 1 = Llama-3.1 frequency scaling */
   double factor;             /* Llama-3.1: scale factor (e.g. 8) */
   double low_freq_factor;    /* Llama-3.1: e.g. 1 */
