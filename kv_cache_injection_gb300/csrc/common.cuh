@@ -55,6 +55,9 @@ struct InjectArgs {
   int32_t head_vecs;            // 16-byte vectors per head (D / VE)
   int32_t cache_row_bytes;      // H * D * elt of the cache (row_bytes, or H * D for FP8)
   float k_inv, v_inv;           // FP8 cache: fp32(1 / k_scale), fp32(1 / v_scale)
+  uint32_t* work_ctr;           // pool chunks claimed in this launch (zero at its start)
+  uint32_t* work_ctr_next;      // the counter of the next launch, zeroed by this one
+  int32_t chunk_items;          // items per pool chunk (set by the launcher)
 };
 
 // One layer of a Context-Window Encoding capture (is_store_capture_layer).

@@ -301,10 +301,35 @@ __global__ void __launch_bounds__(kInjectWarpsMax * 32) inject_kernel(const Inje
   const int64_t n_items = (int64_t)total * groups;
   const int64_t warp_id = (int64_t)blockIdx.x * nwarps + warp;
   const int64_t n_warps = (int64_t)gridDim.x * nwarps;
-  const int64_t chunk = div_nn(n_items + n_warps - 1, n_warps);
-  const int64_t it0 = warp_id * chunk;
-  const int64_t it_end = min(n_items, it0 + chunk);
-  if (it0 >= it_end) return;
+  // Each warp first takes a fixed, contiguous share of kStaticPct % of an even
+  // split; the rest of the items form a pool handed out in chunks of CH to
+  // whichever warp asks first (a counter in global memory).  Warps that run
+  // faster take more of the pool, so the launch ends with the work rather
+  // than with its slowest warp, and the claims come late and spread out in
+  // time.  A warp claims its next chunk when its current run is down to its
+  // last kClaimAhead items, so the claim's latency hides behind them.  The
+  // counter of this launch was zeroed by the previous one; this launch zeroes
+  // the other counter for the next.
+  // Launches with little work per warp (fewer than kMinShare static items)
+  // split the items evenly and use no pool: their claims would all arrive at
+  // once on one address.
+  constexpr int kClaimAhead = 2;
+  constexpr int kStaticPct = 50;
+  constexpr int kMinShare = 64;
+  if (blockIdx.x == 0 && threadIdx.x == 0) *a.work_ctr_next = 0u;
+  const int64_t CH = a.chunk_items;
+  int64_t share = div_nn(n_items * kStaticPct / 100, n_warps);
+  if (share < kMinShare) share = div_nn(n_items + n_warps - 1, n_warps);
+  const int64_t pool0 = min(n_items, share * n_warps);   // first pool item
+  const int64_t n_chunks = div_nn(n_items - pool0 + CH - 1, CH);
+  int64_t next_claim = 0;                        // lane 0: the pool chunk claimed next
+  bool claimed = n_chunks == 0;                  // warp-uniform: next_claim is valid (no pool: never claim)
+  if (n_chunks == 0) next_claim = 0;             // c = 0 >= n_chunks ends the stream
+  const int64_t j0 = warp_id * share;
+  int64_t left = max((int64_t)0, min(share, n_items - j0));   // items left in the current run
+  bool stream_done = false;
+  int32_t nt = (int32_t)div_nn(j0, groups);      // next item: (segment token, layer group)
+  int32_t ng = (int32_t)(j0 - (int64_t)nt * groups);
 
   const uint32_t stage0 = smem_addr(stages);
   const int vpl = a.row_bytes >> 9;             // 16-byte vectors per lane per row
@@ -313,19 +338,41 @@ __global__ void __launch_bounds__(kInjectWarpsMax * 32) inject_kernel(const Inje
 
   TokenCursor cur;
 
-  // Next item to issue, as (segment token, layer group within this call).
-  int32_t nt = (int32_t)div_nn(it0, groups);
-  int32_t ng = (int32_t)(it0 - (int64_t)nt * groups);
-
-  // Warp-uniform: resolve the next item's token and have lane 0 start its bulk
-  // load into stage s.  Items are issued in order.  Returns true if a load was issued.
-  auto issue = [&](int s) -> bool {
-    const int32_t t = nt, l = ng * G;
-    const int32_t nlay = min(G, a.n_layers - l);
+  // Warp-uniform: the next item of this warp's stream into (t, l); false
+  // once the stream has ended.
+  auto next_item = [&](int32_t& t, int32_t& l) -> bool {
+    if (left == 0) {
+      if (stream_done) return false;
+      if (!claimed && lane == 0) next_claim = (int64_t)atomicAdd(a.work_ctr, 1u);
+      claimed = false;
+      const int64_t c = __shfl_sync(0xffffffffu, next_claim, 0);
+      if (c >= n_chunks) {
+        stream_done = true;
+        return false;
+      }
+      const int64_t j = pool0 + c * CH;
+      left = min(CH, n_items - j);
+      nt = (int32_t)div_nn(j, groups);
+      ng = (int32_t)(j - (int64_t)nt * groups);
+    }
+    t = nt;
+    l = ng * G;
+    --left;
+    if (left <= kClaimAhead && !claimed) {
+      if (lane == 0) next_claim = (int64_t)atomicAdd(a.work_ctr, 1u);
+      claimed = true;
+    }
     if (++ng == groups) {
       ng = 0;
       ++nt;
     }
+    return true;
+  };
+
+  // Warp-uniform: resolve item (t, l)'s token and have lane 0 start its bulk
+  // load into stage s.  Returns true if a load was issued.
+  auto issue = [&](int s, int32_t t, int32_t l) -> bool {
+    const int32_t nlay = min(G, a.n_layers - l);
     cur.seek(a, s_off, t, lane);
     const int64_t tok_slot = cur.slot;
     const int32_t tok_p = cur.p;
@@ -349,15 +396,20 @@ __global__ void __launch_bounds__(kInjectWarpsMax * 32) inject_kernel(const Inje
 
   uint32_t phase = 0;        // expected parity of each stage's next completion
   uint32_t pending = 0;      // stages with a bulk load in flight
-  for (int s = 0; s < P && it0 + s < it_end; ++s)
-    if (issue(s)) pending |= 1u << s;
+  int64_t issued = 0;        // items issued; item i sits in stage i % P
+  for (int s = 0; s < P; ++s) {
+    int32_t t, l;
+    if (!next_item(t, l)) break;
+    if (issue(s, t, l)) pending |= 1u << s;
+    ++issued;
+  }
   __syncwarp();
 
   float cs[NF], sn[NF];
   int32_t cur_p = -1;
   bool aborted = false;
   int s = 0;
-  for (int64_t i = it0; i < it_end; ++i) {
+  for (int64_t i = 0; i < issued; ++i) {
     const StageMeta m = meta[s];
     if (m.slot >= 0) {
       const uint32_t bar = smem_addr(&bars[s]);
@@ -391,14 +443,14 @@ __global__ void __launch_bounds__(kInjectWarpsMax * 32) inject_kernel(const Inje
             float z[VE];
             Vec<T>::unpack(ld_shared_v4(kst + (v ^ hv) * 16), z);
             if ((v & hv) == 0) {
-  #pragma unroll
+#pragma unroll
               for (int e = 0; e < VE; ++e) y[e] = fmaf(x[e], cs[e], -z[e] * sn[e]);
             } else {
-  #pragma unroll
+#pragma unroll
               for (int e = 0; e < VE; ++e) y[e] = fmaf(x[e], cs[e], z[e] * sn[e]);
             }
           } else {
-  #pragma unroll
+#pragma unroll
             for (int e = 0; e < VE / 2; ++e) {
               const float u = x[2 * e], w = x[2 * e + 1];
               y[2 * e] = fmaf(u, cs[e], -w * sn[e]);
@@ -421,13 +473,15 @@ __global__ void __launch_bounds__(kInjectWarpsMax * 32) inject_kernel(const Inje
     // Refill the stage of item i - 1 with item i - 1 + P once its V store has
     // finished reading shared memory (all groups but the newest).
     const int sp = s == 0 ? P - 1 : s - 1;
-    if (i > it0 && i - 1 + P < it_end) {
+    int32_t t, l;
+    if (i > 0 && next_item(t, l)) {
       if (lane == 0) {
         bulk_wait_read<1>();
         fence_proxy_async_smem();
       }
       __syncwarp();
-      if (issue(sp)) pending |= 1u << sp;
+      if (issue(sp, t, l)) pending |= 1u << sp;
+      ++issued;
     }
     __syncwarp();
     s = s + 1 == P ? 0 : s + 1;
@@ -637,10 +691,15 @@ static LaunchMemo& launch_memo(int dev) {
   return memo[dev & 63];
 }
 
+// Items per pool chunk: about 32 KiB of K/V.
+constexpr size_t kChunkBytes = 32 * 1024;
+
 template <typename T, int STYLE, bool F8>
-static cudaError_t launch_inject_t(const InjectArgs& a, const RopeTurns& rt, const LaunchCfg& cfg) {
-  const InjectShape sh = inject_shape(a);
-  if (sh.warps == 0) return cudaErrorInvalidValue;
+static cudaError_t launch_inject_t(const InjectArgs& args, const RopeTurns& rt, const LaunchCfg& cfg) {
+  const InjectShape sh = inject_shape(args);
+  if (sh.warps == 0 || !args.work_ctr || !args.work_ctr_next) return cudaErrorInvalidValue;
+  InjectArgs a = args;
+  a.chunk_items = (int32_t)std::max<size_t>(1, kChunkBytes / (2 * (size_t)sh.layers_per_item * a.row_bytes));
   auto kern = inject_kernel<T, STYLE, F8>;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -737,14 +796,17 @@ namespace {
 
 constexpr int kNaRequests = IS_NOALLOC_MAX_REQUESTS;
 constexpr int kNaSegStride = IS_NOALLOC_MAX_FACTS + 1;
-constexpr size_t kNaWords = (size_t)kNaRequests * kNaSegStride + 2 * kNaRequests;
+constexpr size_t kNaWords = (size_t)kNaRequests * kNaSegStride + 2 * kNaRequests + 2;
 constexpr int kNaMaxDevices = 64;
 
-// [0, R*stride): per-request prefix of fact lengths; then n_ids[R]; then seg_len[R].
+// [0, R*stride): per-request prefix of fact lengths; then n_ids[R]; then
+// seg_len[R]; then the inject kernel's two chunk counters, used by alternate
+// launches (zero at load; each launch zeroes the other one).
 static __device__ __align__(256) int32_t g_noalloc_scratch[kNaWords];
 
 struct NoAllocDevice {
   bool ready = false;
+  int parity = 0;               // which of the two chunk counters the next launch uses
   int32_t* scratch = nullptr;   // device address of g_noalloc_scratch on this device
   int num_sms = 0;
 };
@@ -872,6 +934,12 @@ extern "C" is_status_t is_inject_noalloc(
   a.layer_stride = 2LL * cache->num_blocks * cache->block_size * row_bytes;
   a.row_bytes = (int32_t)row_bytes;
   a.cache_row_bytes = (int32_t)row_bytes;
+  {
+    uint32_t* ctr = reinterpret_cast<uint32_t*>(d.scratch + (size_t)kNaRequests * kNaSegStride + 2 * kNaRequests);
+    a.work_ctr = ctr + d.parity;
+    a.work_ctr_next = ctr + (d.parity ^ 1);
+    d.parity ^= 1;
+  }
   a.half_vecs = head_dim / 2 / ve;
   a.head_vecs = head_dim / ve;
   RopeTurns rt;

@@ -138,6 +138,8 @@ struct is_store {
   int64_t cap_src_tokens = 0;
   std::vector<uint8_t> cap_layers;
   int64_t* cap_seg = nullptr;     // [IS_MAX_CAPTURE_FACTS][2] {first source token, first arena token}
+  uint32_t* work_ctr = nullptr;   // [2] the inject kernel's chunk counters, alternate launches
+  int work_parity = 0;
   PendingFacts cap_pending;
 
   bool timing = false;
@@ -192,7 +194,7 @@ void free_store(is_store_t* s) {
                   s->tile_fact, s->tile_len, s->user_meta, s->tile_tok, s->fact_src, s->user_tiles, s->scores,
                   s->ids_tmp, s->scores_tmp, s->fact_seg_off, s->n_ids, s->seg_len_tmp,
                   s->rows_tmp, s->status, s->arrive, s->qg, s->q_inv, s->qperm, s->groups, s->counts,
-                  s->cap_seg};
+                  s->cap_seg, s->work_ctr};
   for (void* p : ptrs)
     if (p) cudaFree(p);
   for (int st = 0; st < IS_NUM_STAGES; ++st)
@@ -480,12 +482,14 @@ is_status_t is_store_create(const is_store_config_t* config, int device, cudaStr
   ALLOC(groups, Q * sizeof(int4), "query groups");
   ALLOC(counts, 8, "group counts");
   ALLOC(cap_seg, (size_t)std::min<int64_t>(c.max_facts, IS_MAX_CAPTURE_FACTS) * 16, "capture segments");
+  ALLOC(work_ctr, 8, "inject chunk counters");
 #undef ALLOC
   s->scratch_bytes = (int64_t)(Q * s->score_stride * 4 + Q * c.max_k * 12 +
                                R * (s->seg_stride * 4 + 8) + (size_t)c.max_facts * 4 + 4);
   cudaError_t e = cudaMemsetAsync(s->status, 0, 4, stream);
   if (e == cudaSuccess) e = cudaMemsetAsync(s->user_meta, 0, (size_t)c.max_users * sizeof(int4), stream);
   if (e == cudaSuccess) e = cudaMemsetAsync(s->arrive, 0, Q * 4, stream);
+  if (e == cudaSuccess) e = cudaMemsetAsync(s->work_ctr, 0, 8, stream);
   if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
   if (e != cudaSuccess) {
     free_store(s);
@@ -906,6 +910,8 @@ static is_status_t launch_injection(is_store_t* s, int32_t R, const int64_t* ids
   a.layer_stride = layer_stride;
   a.row_bytes = (int32_t)s->row_bytes;
   a.cache_row_bytes = (int32_t)cache_row_bytes(s, cache);
+  a.work_ctr = s->work_ctr + s->work_parity;
+  a.work_ctr_next = s->work_ctr + (s->work_parity ^ 1);
   a.k_inv = (float)(1.0 / (double)cache->k_scale);
   a.v_inv = (float)(1.0 / (double)cache->v_scale);
   const int ve = 16 / s->elt;
@@ -923,6 +929,7 @@ static is_status_t launch_injection(is_store_t* s, int32_t R, const int64_t* ids
   StageTimer tm(s, IS_STAGE_INJECT, stream);
   CUDA_TRY(launch_inject(a, rt, s->cfg.kv_dtype, rope->style, s->cfg.kv_placement == IS_KV_HOST,
                          cache->dtype == IS_FP8_E4M3, cfg));
+  s->work_parity ^= 1;
   return IS_OK;
 }
 
