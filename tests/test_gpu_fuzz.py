@@ -1,0 +1,73 @@
+"""Seeded random configurations against the oracle, every injected token
+compared: element type, pairing style and frequency scaling, layer count and
+head shape, block size (1 to 64), fact lengths, k, number and mix of users,
+segment starts, the store's placement and an FP8 cache.  Sizes stay small so
+the oracle compares every row."""
+import numpy as np
+import pytest
+
+from synth import staging, workloads
+from tests import gpu_helpers as gh
+from tests import parity
+
+pytestmark = pytest.mark.gpu
+
+N_CASES = 48
+
+
+@pytest.fixture(scope="module")
+def api():
+    gh.ensure_built()
+    from kv_cache_injection_gb300 import api as a
+    return a
+
+
+def _case(i):
+    rng = np.random.default_rng(1000 + i)
+    dtype = ["f32", "bf16", "f16"][i % 3]
+    elt = 4 if dtype == "f32" else 2
+    style = int(rng.integers(0, 2))
+    ve = 16 // elt
+    max_d = 32 * ve * (2 if style == 0 else 1)           # widest head the kernels take
+    D = int(rng.choice([d for d in (16, 32, 64, 128, 256, 512) if d <= max_d]))
+    H = max(1, 512 // (D * elt)) * int(rng.choice([1, 2]))   # rows of a multiple of 512 bytes
+    scaled = bool(rng.integers(0, 2))
+    rope = (workloads.RopeSpec(theta=float(rng.choice([1e4, 5e5, 1e6])), style=style, scaling=1,
+                               factor=float(rng.choice([4.0, 8.0])), low_freq_factor=1.0,
+                               high_freq_factor=4.0, original_max_pos=int(rng.choice([64, 512, 8192])))
+            if scaled else workloads.RopeSpec(theta=float(rng.choice([1e4, 5e5, 1e6])), style=style))
+    n_users = int(rng.integers(1, 5))
+    k = int(rng.choice([1, 3, 8, 17, 33, 64]))
+    max_len = int(rng.choice([1, 4, 12, 30]))
+    bs = int(rng.choice([1, 8, 16, 32, 64]))
+    n_q = n_users if rng.integers(0, 2) else int(rng.integers(1, 9))
+    share = n_q != n_users
+    spec = workloads.WorkloadSpec(
+        name=f"fuzz{i}", num_layers=int(rng.integers(1, 5)), num_kv_heads=H, head_dim=D, kv_dtype=dtype,
+        rope=rope, n_users=n_users, facts_per_user=int(rng.integers(max(k // 2, 1), 400)),
+        length_dist=("uniform", 1, max_len), emb_dim=int(rng.choice([64, 128, 256])),
+        emb_dtype="f32" if dtype == "f32" else "f16", n_queries=n_q, k=k, query_kind="planted",
+        start=("uniform", 0, int(rng.choice([1, 100, 5000, 100000]))), block_size=bs,
+        tokens_cap=k * max_len, block_layout="free_list", queries_share_user=share, seed=2000 + i)
+    placement = "host" if rng.integers(0, 4) == 0 else "device"
+    fp8 = dtype != "f32" and rng.integers(0, 4) == 0
+    scales = (float(rng.uniform(0.2, 2.0)), float(rng.uniform(0.2, 2.0)))
+    return spec, placement, fp8, scales
+
+
+@pytest.mark.parametrize("i", range(N_CASES))
+def test_random_configuration(api, i):
+    spec, placement, fp8, scales = _case(i)
+    wl = workloads.generate(spec)
+    if spec.queries_share_user and spec.n_users > 1:
+        wl.users[:] = np.random.default_rng(i).integers(0, spec.n_users, size=spec.n_queries).astype(np.int32)
+    store = staging.load_store(wl, api, kv_placement=placement)
+    try:
+        n_tok = sum(len(pl) for pl in parity.oracle_plans(wl, [
+            parity.oracle_retrieve(wl, q, spec.k)[0] for q in range(spec.n_queries)])[0])
+        st = gh.check_fused_workload(api, wl, store, sample_tokens=max(n_tok, 1),
+                                     cache_dtype="e4m3" if fp8 else None,
+                                     k_scale=scales[0], v_scale=scales[1])
+        assert st["tokens"] == n_tok
+    finally:
+        store.destroy()
