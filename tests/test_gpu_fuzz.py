@@ -71,3 +71,51 @@ def test_random_configuration(api, i):
         assert st["tokens"] == n_tok
     finally:
         store.destroy()
+
+
+def _batched_case(i):
+    rng = np.random.default_rng(3000 + i)
+    n_users = int(rng.integers(1, 5))
+    per_user = [int(rng.integers(1, 151)) for _ in range(n_users)]
+    users = np.concatenate([np.full(c, u, np.int32) for u, c in enumerate(per_user)])
+    users = rng.permutation(users)[:1024]
+    k = int(rng.choice([1, 7, 50, 100, 200]))
+    spec = workloads.WorkloadSpec(
+        name=f"fuzz_batched{i}", num_layers=1, num_kv_heads=4, head_dim=64, kv_dtype="bf16",
+        rope=workloads.RopeSpec(theta=1e4), n_users=n_users, facts_per_user=int(rng.integers(64, 3000)),
+        length_dist=("uniform", 1, 3), emb_dim=int(rng.choice([64, 72, 136, 200, 1024])), emb_dtype="f16",
+        n_queries=len(users), k=k, query_kind="planted", start=("uniform", 0, 50), block_size=16,
+        tokens_cap=k * 3, block_layout="free_list", queries_share_user=True, seed=4000 + i)
+    return spec, users
+
+
+@pytest.mark.parametrize("i", range(12))
+def test_random_tensor_core_retrieval(api, i):
+    """The tcgen05 similarity path on random embedding widths (not only
+    multiples of the 64-element TMA chunk), users and group sizes (groups of
+    at most 64 queries per user): top-k against the oracle, scores against the
+    per-query path."""
+    import torch
+    from kv_cache_injection_gb300 import _lib
+    spec, users = _batched_case(i)
+    wl = workloads.generate(spec)
+    wl.users[:] = users
+    store = staging.load_store(wl, api)
+    try:
+        inp = staging.device_inputs(wl)
+        Q, k = spec.n_queries, spec.k
+        out = {}
+        for mode in (_lib.IS_RETRIEVAL_BATCHED, _lib.IS_RETRIEVAL_PER_QUERY):
+            api.is_set_retrieval_mode(store, mode)
+            ids = torch.full((Q, k), -7, dtype=torch.int64, device="cuda")
+            sc = torch.zeros((Q, k), dtype=torch.float32, device="cuda")
+            api.is_retrieve_topk(store, inp["users"], inp["q_emb"], k, ids, sc)
+            assert api.is_get_status(store) == 0
+            out[mode] = (ids.cpu().numpy(), sc.cpu().numpy())
+        ids_b, sc_b = out[_lib.IS_RETRIEVAL_BATCHED]
+        for q in range(Q):
+            o_ids, o_sc, score_of = parity.oracle_retrieve(wl, q, k)
+            parity.check_topk(ids_b[q], sc_b[q], o_ids, o_sc, score_of, k)
+        assert np.max(np.abs(sc_b - out[_lib.IS_RETRIEVAL_PER_QUERY][1])) <= 2e-6
+    finally:
+        store.destroy()
