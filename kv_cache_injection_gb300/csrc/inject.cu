@@ -96,6 +96,43 @@ struct StageMeta {
   int16_t nl;       // layers in the group
 };
 
+// Chunked RoPE on one 16-byte vector of a key row (VE elements).  x holds the
+// vector; for NeoX pairs (i, i + D/2), z holds its partner vector v ^ half_vecs
+// and `first` says whether v is the pair's first half (a' = a cos - b sin) or
+// second (b' = b cos + a sin); interleaved pairs (2i, 2i + 1) lie inside the
+// vector and z is unused.  cs / sn are the lane's cos / sin, one per frequency.
+template <typename T, int STYLE>
+__device__ __forceinline__ void rotate_vec(const float* x, const float* z, bool first, const float* cs,
+                                           const float* sn, float* y) {
+  constexpr int VE = Vec<T>::N;
+  if (STYLE == 0) {
+    if (first) {
+#pragma unroll
+      for (int e = 0; e < VE; ++e) y[e] = fmaf(x[e], cs[e], -z[e] * sn[e]);
+    } else {
+#pragma unroll
+      for (int e = 0; e < VE; ++e) y[e] = fmaf(x[e], cs[e], z[e] * sn[e]);
+    }
+  } else {
+#pragma unroll
+    for (int e = 0; e < VE / 2; ++e) {
+      const float u = x[2 * e], w = x[2 * e + 1];
+      y[2 * e] = fmaf(u, cs[e], -w * sn[e]);
+      y[2 * e + 1] = fmaf(w, cs[e], u * sn[e]);
+    }
+  }
+}
+
+// Rotated key vector v of a row at dk: 16 bytes in the store's type, or 8
+// E4M3 bytes (times fp32(1 / k_scale)) for an FP8 cache.
+template <typename T, bool F8>
+__device__ __forceinline__ void store_key(uint8_t* dk, int v, const float* y, float k_inv) {
+  if (F8)
+    st_v2(dk + (size_t)v * 8, to_e4m3x8(y, k_inv));
+  else
+    st_v4(dk + (size_t)v * 16, Vec<T>::pack(y));
+}
+
 // x / d for non-negative operands, in 32-bit arithmetic when both fit.
 __device__ __forceinline__ int64_t div_nn(int64_t x, int64_t d) {
   return ((x | d) >> 31) == 0 ? (int64_t)((uint32_t)x / (uint32_t)d) : x / d;
@@ -437,35 +474,17 @@ __global__ void __launch_bounds__(kInjectWarpsMax * 32) inject_kernel(const Inje
         if (!F8 && lane == 0) bulk_store(dv, kst + a.row_bytes, a.row_bytes);
         for (int c = 0; c < vpl; ++c) {
           const int v = c * 32 + lane;
-          float x[VE], y[VE];
+          float x[VE], z[VE], y[VE];
           Vec<T>::unpack(ld_shared_v4(kst + v * 16), x);
-          if (STYLE == 0) {
-            float z[VE];
-            Vec<T>::unpack(ld_shared_v4(kst + (v ^ hv) * 16), z);
-            if ((v & hv) == 0) {
-#pragma unroll
-              for (int e = 0; e < VE; ++e) y[e] = fmaf(x[e], cs[e], -z[e] * sn[e]);
-            } else {
-#pragma unroll
-              for (int e = 0; e < VE; ++e) y[e] = fmaf(x[e], cs[e], z[e] * sn[e]);
-            }
-          } else {
-#pragma unroll
-            for (int e = 0; e < VE / 2; ++e) {
-              const float u = x[2 * e], w = x[2 * e + 1];
-              y[2 * e] = fmaf(u, cs[e], -w * sn[e]);
-              y[2 * e + 1] = fmaf(w, cs[e], u * sn[e]);
-            }
-          }
+          if (STYLE == 0) Vec<T>::unpack(ld_shared_v4(kst + (v ^ hv) * 16), z);
+          rotate_vec<T, STYLE>(x, z, (v & hv) == 0, cs, sn, y);
           if (F8) {
             // 8-bit cache: V is converted on the way too (no bulk store).
             float xv[VE];
             Vec<T>::unpack(ld_shared_v4(kst + a.row_bytes + v * 16), xv);
             st_v2(dv + (size_t)v * 8, to_e4m3x8(xv, a.v_inv));
-            st_v2(dk + (size_t)v * 8, to_e4m3x8(y, a.k_inv));
-          } else {
-            st_v4(dk + (size_t)v * 16, Vec<T>::pack(y));
           }
+          store_key<T, F8>(dk, v, y, a.k_inv);
         }
       }
     }
@@ -586,30 +605,11 @@ __global__ void __launch_bounds__(kHostWarps * 32) inject_host_kernel(const Inje
           } else {
             st_v4(dv + (size_t)v * 16, vx[c]);
           }
-          float x[VE], y[VE];
+          float x[VE], z[VE], y[VE];
           Vec<T>::unpack(kx[c], x);
-          if (STYLE == 0) {
-            float z[VE];
-            Vec<T>::unpack(hv < 32 ? shfl_xor4(kx[c], hv) : kx[c ^ 1], z);
-            if ((v & hv) == 0) {
-#pragma unroll
-              for (int e = 0; e < VE; ++e) y[e] = fmaf(x[e], cs[e], -z[e] * sn[e]);
-            } else {
-#pragma unroll
-              for (int e = 0; e < VE; ++e) y[e] = fmaf(x[e], cs[e], z[e] * sn[e]);
-            }
-          } else {
-#pragma unroll
-            for (int e = 0; e < VE / 2; ++e) {
-              const float u = x[2 * e], w = x[2 * e + 1];
-              y[2 * e] = fmaf(u, cs[e], -w * sn[e]);
-              y[2 * e + 1] = fmaf(w, cs[e], u * sn[e]);
-            }
-          }
-          if (F8)
-            st_v2(dk + (size_t)v * 8, to_e4m3x8(y, a.k_inv));
-          else
-            st_v4(dk + (size_t)v * 16, Vec<T>::pack(y));
+          if (STYLE == 0) Vec<T>::unpack(hv < 32 ? shfl_xor4(kx[c], hv) : kx[c ^ 1], z);
+          rotate_vec<T, STYLE>(x, z, (v & hv) == 0, cs, sn, y);
+          store_key<T, F8>(dk, v, y, a.k_inv);
         }
     }
   }
