@@ -119,3 +119,117 @@ def test_random_tensor_core_retrieval(api, i):
         assert np.max(np.abs(sc_b - out[_lib.IS_RETRIEVAL_PER_QUERY][1])) <= 2e-6
     finally:
         store.destroy()
+
+
+@pytest.mark.parametrize("i", range(12))
+def test_random_explicit_lists_and_layerwise(api, i):
+    """is_inject with random explicit lists (empty requests, a fact repeated
+    within and across requests, any order), then the same plan layer by layer
+    through is_inject_layer into per-layer caches: every token against the
+    oracle, every layer equal to the whole-cache injection."""
+    import torch
+    spec, placement, fp8, scales = _case(100 + i)
+    rng = np.random.default_rng(5000 + i)
+    wl = workloads.generate(spec.with_(n_users=1, queries_share_user=True))
+    s = wl.spec
+    store = staging.load_store(wl, api, kv_placement=placement)
+    try:
+        R, stride = s.n_queries, s.k
+        n_ids = rng.integers(0, stride + 1, size=R).astype(np.int32)
+        ids = np.full((R, stride), -1, dtype=np.int64)
+        for r in range(R):
+            ids[r, :n_ids[r]] = rng.integers(0, s.n_facts, size=n_ids[r])      # repeats allowed
+        inp = staging.device_inputs(wl)
+        cdt = "e4m3" if fp8 else None
+        cache = staging.canary_cache(wl, cache_dtype=cdt)
+        cd = api.make_cache_desc(s.block_size, cache.shape[2], cdt or s.kv_dtype, *scales)
+        rope = staging.rope_params(wl, api)
+        seg_len = torch.empty(R, dtype=torch.int32, device="cuda")
+        slots = torch.full((R * stride * int(wl.lengths.max()) + 1,), -9, dtype=torch.int64, device="cuda")
+        d_ids, d_n = torch.from_numpy(ids).cuda(), torch.from_numpy(n_ids).cuda()
+        api.is_inject(store, d_ids, d_n, inp["seg_start"], rope, inp["block_table"], cd, cache,
+                      users=inp["users"], seg_len_out=seg_len, slot_mapping_out=slots)
+        assert api.is_get_status(store) == 0
+        rows = [ids[r, :n_ids[r]] for r in range(R)]
+        plans, lens = parity.oracle_plans(wl, rows)
+        assert np.array_equal(seg_len.cpu().numpy(), lens)
+        want = np.concatenate([[e[3] for e in pl] for pl in plans] + [[]]).astype(np.int64)
+        assert np.array_equal(slots.cpu().numpy()[: len(want)], want)
+        gh.assert_only_slots_changed(cache, cdt or s.kv_dtype, want)
+        entries = [e for pl in plans for e in pl]
+        if entries:
+            gk, gv = gh.gather_rows(cache, [e[3] for e in entries])
+            if fp8:
+                parity.compare_tokens_fp8(wl, gk, gv, entries, parity.oracle_freqs(wl), s.rope.style,
+                                          parity.FactCache(wl), *scales)
+            else:
+                parity.compare_tokens(wl, gk, gv, entries, parity.oracle_freqs(wl), s.rope.style,
+                                      parity.FactCache(wl))
+        # the same plan, layer by layer, into per-layer caches
+        for layer in range(s.num_layers):
+            lc = staging.canary_cache(wl, cache_dtype=cdt)[0].contiguous()
+            if layer == 0:
+                api.is_inject_layer(store, 0, R, inp["seg_start"], rope, inp["block_table"], cd, lc,
+                                    fact_ids=d_ids, n_ids=d_n, users=inp["users"])
+            else:
+                api.is_inject_layer(store, layer, R, inp["seg_start"], rope, inp["block_table"], cd, lc)
+            assert api.is_get_status(store) == 0
+            assert torch.equal(lc.view(torch.uint8), cache[layer].contiguous().view(torch.uint8))
+    finally:
+        store.destroy()
+
+
+@pytest.mark.parametrize("i", range(8))
+def test_random_capture_equals_add_facts(api, i):
+    """Context-Window Encoding capture with random windows and lengths (layer
+    buffers with random content) stores exactly the fact rows: a store built
+    by is_store_add_facts from those rows injects the same cache byte for byte."""
+    import torch
+    rng = np.random.default_rng(6000 + i)
+    spec, placement, _, _ = _case(200 + i)
+    L, H, D, dt = spec.num_layers, spec.num_kv_heads, spec.head_dim, spec.kv_dtype
+    tdt = staging.torch_dtype(dt)
+    n = int(rng.integers(1, 40))
+    lengths = rng.integers(1, 20, size=n).astype(np.int32)
+    windows = rng.integers(0, 50, size=n).astype(np.int32)
+    total = int((lengths + windows).sum())
+    gen = torch.Generator(device="cuda").manual_seed(i)
+    layers = [(torch.randn(total, H, D, device="cuda", generator=gen).to(tdt),
+               torch.randn(total, H, D, device="cuda", generator=gen).to(tdt)) for _ in range(L)]
+    emb = torch.nn.functional.normalize(torch.randn(n, 64, device="cuda", generator=gen), dim=1)
+    emb = emb.half() if spec.emb_dtype == "f16" else emb
+    def store():
+        cfg = api.make_config(num_layers=L, num_kv_heads=H, head_dim=D, emb_dim=64, kv_dtype=dt,
+                              emb_dtype=spec.emb_dtype, max_facts=n, max_tokens=int(lengths.sum()),
+                              max_users=1, max_queries=1, max_k=n, max_requests=1, kv_placement=placement)
+        return api.is_store_create(cfg, 0)
+    a, b = store(), store()
+    try:
+        api.is_store_capture_begin(a, 0, windows, lengths, emb)
+        for l in rng.permutation(L):
+            api.is_store_capture_layer(a, int(l), layers[l][0], layers[l][1])
+        assert np.array_equal(api.is_store_capture_end(a, n), np.arange(n))
+        # the fact rows, token-major [tokens][L][H][D]
+        starts = np.cumsum(np.concatenate([[0], lengths + windows]))[:-1] + windows
+        idx = torch.from_numpy(np.concatenate([np.arange(st, st + ln) for st, ln in zip(starts, lengths)])).cuda()
+        k = torch.stack([layers[l][0].index_select(0, idx) for l in range(L)], 1).contiguous()
+        v = torch.stack([layers[l][1].index_select(0, idx) for l in range(L)], 1).contiguous()
+        api.is_store_add_facts(b, 0, lengths, k, v, emb)
+        bs = 16
+        T = int(lengths.sum())
+        nb = T // bs + 2
+        bt = torch.arange(nb, dtype=torch.int32, device="cuda")[None].flip(1).contiguous()
+        rope = api.make_rope(1e4, spec.rope.style)
+        cd = api.make_cache_desc(bs, nb, dt)
+        order = torch.from_numpy(rng.permutation(n).astype(np.int64)[None]).cuda()
+        outs = []
+        for st in (a, b):
+            cache = torch.zeros((L, 2, nb, bs, H, D), dtype=tdt, device="cuda")
+            api.is_inject(st, order, torch.tensor([n], dtype=torch.int32, device="cuda"),
+                          torch.zeros(1, dtype=torch.int32, device="cuda"), rope, bt, cd, cache)
+            assert api.is_get_status(st) == 0
+            outs.append(cache)
+        assert torch.equal(outs[0].view(torch.uint8), outs[1].view(torch.uint8))
+    finally:
+        a.destroy()
+        b.destroy()
