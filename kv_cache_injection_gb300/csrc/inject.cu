@@ -138,22 +138,26 @@ __device__ __forceinline__ int64_t div_nn(int64_t x, int64_t d) {
   return ((x | d) >> 31) == 0 ? (int64_t)((uint32_t)x / (uint32_t)d) : x / d;
 }
 
-// Shared-memory ints the request prefix needs: R + 1 for the block-wide scan,
-// or a 33-entry slice per warp when every warp scans R <= 32 requests itself.
-__host__ __device__ constexpr int prefix_ints(int R, int warps) { return R <= 32 ? warps * 33 : R + 1; }
+// Shared-memory ints the request table needs: the prefix (R + 1) and the
+// starts (R) for the block-wide scan, or a 66-entry slice per warp when every
+// warp scans R <= 32 requests itself.
+__host__ __device__ constexpr int prefix_ints(int R, int warps) { return R <= 32 ? warps * 66 : 2 * R + 1; }
 
 // Exclusive prefix of seg_len over the R requests; returns the total token
-// count and points *s_off at the prefix (R + 1 entries, the last = total).
+// count, points *s_off at the prefix (R + 1 entries, the last = total) and
+// *s_start at the requests' seg_start (read in the same round, so a token's
+// position, and with it its block-table entry, is known before its fact).
 // Up to 32 requests, each warp loads and scans them with shuffles into its
 // own slice of `region`, so no block-wide barrier sits between the planning
 // kernel's outputs and the warp's first copy; more requests are scanned by the
 // whole block.  All threads of the block call it.
 __device__ __forceinline__ int32_t segment_prefix(const InjectArgs& a, int32_t* region, int32_t* scratch,
-                                                  const int32_t** s_off) {
+                                                  const int32_t** s_off, const int32_t** s_start) {
   if (a.R <= 32) {
     const int lane = threadIdx.x & 31;
-    int32_t* mine = region + (threadIdx.x >> 5) * 33;
+    int32_t* mine = region + (threadIdx.x >> 5) * 66;
     const int32_t v = lane < a.R ? a.seg_len[lane] : 0;
+    if (lane < a.R) mine[33 + lane] = a.seg_start[lane];
     int32_t inc = v;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -165,6 +169,7 @@ __device__ __forceinline__ int32_t segment_prefix(const InjectArgs& a, int32_t* 
     if (lane == 0) mine[a.R] = total;
     __syncwarp();
     *s_off = mine;
+    *s_start = mine + 33;
     return total;
   }
   int32_t total = 0;
@@ -176,11 +181,13 @@ __device__ __forceinline__ int32_t segment_prefix(const InjectArgs& a, int32_t* 
   int32_t base = block_exclusive_scan(sum, scratch, &total);
   for (int i = b; i < e; ++i) {
     region[i] = base;
+    region[a.R + 1 + i] = a.seg_start[i];
     base += a.seg_len[i];
   }
   if (threadIdx.x == 0) region[a.R] = total;
   __syncthreads();
   *s_off = region;
+  *s_start = region + a.R + 1;
   return total;
 }
 
@@ -191,13 +198,13 @@ __device__ __forceinline__ int32_t segment_prefix(const InjectArgs& a, int32_t* 
 //
 // Finding the fact of a token is on the critical path of every warp's first
 // item, so it is one round of independent loads: the request's fact count and
-// start position, and the first 128 entries of its plan (segment offset and
-// store token of each fact, four per lane); a ballot then picks the last fact
-// whose offset is <= the token's.  Longer plans continue with a strided search
-// over the rest.
+// the first 128 entries of its plan (segment offset and store token of each
+// fact, four per lane); a ballot then picks the last fact whose offset is <=
+// the token's.  Longer plans continue with a strided search over the rest.
+// The token's block-table entry depends only on its position, so its load is
+// issued before the fact lookup and overlaps it.
 struct TokenCursor {
   int32_t t = -1, r = -1, j = 0, lo = 0, hi = 0;
-  int32_t start = 0;    // seg_start of request r
   int64_t src0 = 0;     // store token of fact j's first token
   int32_t lb = -1, blk = -1;
   int64_t src = 0;      // store token
@@ -210,7 +217,6 @@ struct TokenCursor {
     const int32_t* off = a.fact_seg_off + (size_t)rr * a.seg_stride;
     const int64_t* fsrc = a.fact_src ? a.fact_src + (size_t)rr * a.seg_stride : nullptr;
     const int n = a.n_ids[rr];
-    start = a.seg_start[rr];
     int32_t o[kPer];
     int64_t sv[kPer];
 #pragma unroll
@@ -269,10 +275,10 @@ struct TokenCursor {
     }
     r = rr;
     j = jlo;
-    lb = -1;
   }
 
-  __device__ __forceinline__ void seek(const InjectArgs& a, const int32_t* s_off, int32_t tt, int lane) {
+  __device__ __forceinline__ void seek(const InjectArgs& a, const int32_t* s_off, const int32_t* s_start,
+                                       int32_t tt, int lane) {
     if (tt == t) return;
     t = tt;
     int rlo = 0, rhi = a.R;
@@ -281,14 +287,15 @@ struct TokenCursor {
       if (s_off[mid] <= tt) rlo = mid; else rhi = mid;
     }
     const int32_t ts = tt - s_off[rlo];
+    const int32_t pn = s_start[rlo] + ts;
+    const int32_t lbn = pn / a.block_size;
+    if (rlo != r || lbn != lb) {
+      blk = lbn < a.max_blocks ? a.block_table[(size_t)rlo * a.max_blocks + lbn] : -1;
+      lb = lbn;
+    }
     if (rlo != r || ts < lo || ts >= hi) find_fact(a, rlo, ts, lane);
     src = src0 + (ts - lo);
-    p = start + ts;
-    const int32_t lbn = p / a.block_size;
-    if (lbn != lb) {
-      lb = lbn;
-      blk = lbn < a.max_blocks ? a.block_table[(size_t)r * a.max_blocks + lbn] : -1;
-    }
+    p = pn;
     slot = -1;
     if (lb >= a.max_blocks) {
       if (lane == 0) latch(a.status, IS_ST_BLOCK_TABLE);
@@ -331,8 +338,8 @@ __global__ void __launch_bounds__(kInjectWarpsMax * 32) inject_kernel(const Inje
   warm8(a.seg_len, a.n_ids, a.fact_seg_off, a.fact_src, a.seg_start, a.block_table, a.slot_mapping, a.ids);
   pdl_wait();                                   // outputs of the planning kernel
 
-  const int32_t* s_off;
-  const int32_t total = segment_prefix(a, off_region, scratch, &s_off);
+  const int32_t *s_off, *s_start;
+  const int32_t total = segment_prefix(a, off_region, scratch, &s_off, &s_start);
 
   const int groups = (a.n_layers + G - 1) / G;   // items per token
   const int64_t n_items = (int64_t)total * groups;
@@ -410,7 +417,7 @@ __global__ void __launch_bounds__(kInjectWarpsMax * 32) inject_kernel(const Inje
   // load into stage s.  Returns true if a load was issued.
   auto issue = [&](int s, int32_t t, int32_t l) -> bool {
     const int32_t nlay = min(G, a.n_layers - l);
-    cur.seek(a, s_off, t, lane);
+    cur.seek(a, s_off, s_start, t, lane);
     const int64_t tok_slot = cur.slot;
     const int32_t tok_p = cur.p;
     const int64_t tok_src = cur.src;
@@ -547,8 +554,8 @@ __global__ void __launch_bounds__(kHostWarps * 32) inject_host_kernel(const Inje
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int32_t* s_off;
-  const int32_t total = segment_prefix(a, off_region, scratch, &s_off);
+  const int32_t *s_off, *s_start;
+  const int32_t total = segment_prefix(a, off_region, scratch, &s_off, &s_start);
   const int64_t n_items = (int64_t)total * a.n_layers;
   const int64_t n_warps = (int64_t)gridDim.x * (blockDim.x >> 5);
   const int64_t chunk = div_nn(n_items + n_warps - 1, n_warps);
@@ -570,7 +577,7 @@ __global__ void __launch_bounds__(kHostWarps * 32) inject_host_kernel(const Inje
       l = 0;
       ++t;
     }
-    cur.seek(a, s_off, t, lane);
+    cur.seek(a, s_off, s_start, t, lane);
     if (l == 0 && lane == 0 && a.slot_mapping) a.slot_mapping[t] = cur.slot;
     if (cur.slot < 0) continue;
     if (cur.p != cur_p) {
@@ -661,7 +668,8 @@ static InjectShape inject_shape(const InjectArgs& a) {
   const size_t item = 2 * (size_t)G * a.row_bytes;
   const size_t off_bytes = ((size_t)prefix_ints(a.R, kInjectWarpsMax) * 4 + 127) & ~(size_t)127;
   const size_t per_stage = item + 8 + sizeof(StageMeta);
-  const size_t stage_budget = 96 * 1024;        // two CTAs per SM
+  // Two CTAs per SM: the stages get what the request table leaves of ~110 KiB.
+  const size_t stage_budget = std::max<size_t>(16 * 1024, std::min<size_t>(96 * 1024, 110 * 1024 - off_bytes));
   const size_t smem_max = 227 * 1024 - 1024;
   for (int w = kInjectWarpsMax; w >= 1; w >>= 1) {
     int p = (int)std::min<size_t>(16, std::max<size_t>(2, stage_budget / (w * item)));
