@@ -121,14 +121,25 @@ __global__ void __launch_bounds__(1024) group_kernel(const GroupArgs a) {
   pdl_trigger();
   const int tid = threadIdx.x;
   const int Q = a.Q;
+  // The query rows are packed after the sort: pull them into L2 now, one
+  // 128-byte line per thread and pass, so their latency hides under the sort.
+  {
+    const size_t lines = ((size_t)Q * a.E * 2 + 127) / 128;
+    const uint8_t* base = reinterpret_cast<const uint8_t*>(a.q_emb);
+    for (size_t i = tid; i < lines; i += blockDim.x) prefetch_l2(base + i * 128);
+  }
   int P = 1;
   while (P < Q) P <<= 1;
   for (int i = tid; i < P; i += blockDim.x) {
     uint32_t u = 0xFFFFFFFFu;                        // unknown users sort last, form no group
     if (i < Q) {
       const int32_t uu = a.users[i];
-      if (uu >= 0 && uu < a.max_users) u = (uint32_t)uu;
-      else latch(a.status, IS_ST_USER_RANGE);
+      if (uu >= 0 && uu < a.max_users) {
+        u = (uint32_t)uu;
+        prefetch_l2(a.user_meta + uu);               // read after the sort
+      } else {
+        latch(a.status, IS_ST_USER_RANGE);
+      }
     }
     key[i] = i < Q ? (((unsigned long long)u << 32) | (uint32_t)i) : ~0ull;
   }
