@@ -189,6 +189,13 @@ def measure_h2d_gbs(dev, nbytes: int = 1 << 30, reps: int = 5) -> float:
     return nbytes / (best * 1e-3) / 1e9
 
 
+def workload_description(s) -> str:
+    Q, k = s.n_queries, s.k
+    return (f"{s.name}: {s.num_layers} layers x {s.num_kv_heads} KV heads x head_dim {s.head_dim} "
+            f"{s.kv_dtype}; {s.n_facts} facts {s.length_dist}; {Q} quer{'y' if Q == 1 else 'ies'}, "
+            f"k={k}, block {s.block_size}")
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
 
@@ -395,10 +402,7 @@ def run_ours(args, rank, world, local_rank):
             "dtype": s.kv_dtype,
             "data": "synthetic (seeded; LoCoMo and model weights not available)",
             "config": {
-                "workload": (f"{s.name}: {s.num_layers} layers x {s.num_kv_heads} KV heads x "
-                             f"head_dim {s.head_dim} {s.kv_dtype}; {s.n_facts} facts "
-                             f"{s.length_dist}; {Q} quer{'y' if Q == 1 else 'ies'}, k={k}, "
-                             f"block {s.block_size}"),
+                "workload": workload_description(s),
                 "tokens_per_step": tokens_per_step,
                 "bytes_per_step": path_bytes,
                 "l2": (f"flushed between steps, outside the events: {L2_FLUSH_BYTES >> 20} MiB write "
@@ -525,7 +529,10 @@ def run_reference(args, rank, world):
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": dt * 1e3 / args.steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
-            "config": {"workload": f"{wl.spec.name} (oracle on host cores, bounded sample)"},
+            "config": {"workload": workload_description(wl.spec),
+                       "parallelism": "oracle on host cores (rank 0), bounded sample",
+                       "kv_placement": args.kv_placement, "cache_dtype": args.cache_dtype or wl.spec.kv_dtype,
+                       "retrieval": args.retrieval},
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
