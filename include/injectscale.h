@@ -28,9 +28,10 @@
  * - A store is used by one stream at a time; calls on one store are not
  *   thread-safe.
  * - Dtypes: K/V in the store and in the cache share one dtype (f32, bf16 or
- *   f16); embeddings and query embeddings share one dtype (f16 or f32).
- *   Rotation arithmetic is fp32; rotated keys are rounded to the cache
- *   dtype to nearest even; values are copied bit for bit.
+ *   f16), or the cache is FP8 E4M3 for a bf16 / f16 store (is_cache_desc_t);
+ *   embeddings and query embeddings share one dtype (f16 or f32).  Rotation
+ *   arithmetic is fp32; rotated keys are rounded to the cache dtype to
+ *   nearest even; values are copied bit for bit (FP8: converted like keys).
  */
 #ifndef INJECTSCALE_H
 #define INJECTSCALE_H
@@ -191,6 +192,10 @@ is_status_t is_store_add_facts(is_store_t* store, int32_t user, int32_t n,
                                const void* v, const void* emb, int64_t* fact_ids_out_host,
                                cudaStream_t stream);
 
+/* Counters and sizes of a store (host struct, filled on return): facts and
+ * tokens stored, embedding tiles in use, the largest user's tiles and facts,
+ * the arena, embedding and scratch bytes, the SM count and where the arena
+ * lives.  Reads host-side state only; never synchronises. */
 is_status_t is_store_info(const is_store_t* store, is_store_info_t* out);
 
 /* ---- Context-Window Encoding capture ----------------------------------------
