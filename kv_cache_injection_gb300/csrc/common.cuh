@@ -201,13 +201,20 @@ __device__ __forceinline__ void st_v2(void* ptr, const uint2& v) {
 
 // Eight fp32 values times r into eight FP8 E4M3 bytes (one 8-byte word,
 // element 0 in the lowest byte): one fp32 multiply each, then the hardware
-// conversion, which rounds to nearest even and saturates to +-448.
+// conversion, which rounds to nearest even and saturates to +-448.  With
+// r == 1 (the usual unit scale) the multiplies are exact no-ops and skipped.
 __device__ __forceinline__ uint2 to_e4m3x8(const float* x, float r) {
   uint32_t w[4];
+  if (r == 1.0f) {
 #pragma unroll
-  for (int e = 0; e < 4; ++e)
-    w[e] = __nv_cvt_float2_to_fp8x2(make_float2(__fmul_rn(x[2 * e], r), __fmul_rn(x[2 * e + 1], r)),
-                                    __NV_SATFINITE, __NV_E4M3);
+    for (int e = 0; e < 4; ++e)
+      w[e] = __nv_cvt_float2_to_fp8x2(make_float2(x[2 * e], x[2 * e + 1]), __NV_SATFINITE, __NV_E4M3);
+  } else {
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      w[e] = __nv_cvt_float2_to_fp8x2(make_float2(__fmul_rn(x[2 * e], r), __fmul_rn(x[2 * e + 1], r)),
+                                      __NV_SATFINITE, __NV_E4M3);
+  }
   return make_uint2(w[0] | (w[1] << 16), w[2] | (w[3] << 16));
 }
 
