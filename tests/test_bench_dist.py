@@ -10,6 +10,9 @@ torch = pytest.importorskip("torch")
 import torch.distributed as dist  # noqa: E402
 import torch.multiprocessing as mp  # noqa: E402
 
+_ENV_BEFORE = {v for v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS")
+               if os.environ.get(v) == "1"}
+
 
 def _free_port():
     with socket.socket() as s:
@@ -42,3 +45,19 @@ def test_two_ranks_reduce_and_distinct_seeds():
     assert res[0][0] == res[1][0] == 2.5
     assert res[0][1] == res[1][1] == 3000.0
     assert res[0][2] != res[1][2]
+
+
+def test_oracle_pool_counts_every_step_once():
+    """The CPU baseline's process pool runs exactly the steps it is given and
+    sums the tokens of all workers (tiny workload, 2 spawned workers)."""
+    import bench
+    from synth import workloads
+    wl = workloads.get("tiny")
+    cache = bench._host_cache(wl)()
+    per_step = bench.oracle_step(wl, 0, 4, lambda: cache)
+    run = bench.oracle_pool(wl.spec, 4, 2, [3, 2], warmup=1)
+    assert run["reps"] == 5
+    assert run["tokens"] == 5 * per_step
+    assert run["wall_s"] > 0 and run["value"] == run["tokens"] / run["wall_s"]
+    for v in bench._ONE_THREAD:                  # the parent's environment is restored
+        assert os.environ.get(v) != "1" or v in _ENV_BEFORE
