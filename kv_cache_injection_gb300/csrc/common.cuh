@@ -96,6 +96,9 @@ struct PlanArgs {
   int32_t R;
 };
 
+// Uniform bins of the cosine in [-1, 1] used by the top-k's first pass.
+constexpr int kCosBins = 2048;
+
 struct SimArgs {
   const void* emb;              // tiles [n_tiles * kTile][E]
   const float* emb_inv_norm;    // [n_tiles * kTile]
@@ -132,6 +135,7 @@ struct TopkArgs {
   int32_t* seg_len;             // [Q] or null
   const int32_t* block_table;   // [Q][max_blocks] or null (prefetched into L2)
   int32_t max_blocks;
+  uint32_t* hist;               // [Q][kCosBins] cosine-bin counts filled by the similarity CTAs, or null
   uint32_t* status;
   int32_t Q;
   int32_t k;
@@ -172,6 +176,16 @@ struct GemmArgs {
 // ------------------------------------------------------------------ device helpers
 
 __device__ __forceinline__ void latch(uint32_t* status, uint32_t bits) { atomicOr(status, bits); }
+
+// Atomic add with acquire-release semantics at GPU scope: the caller's earlier
+// writes (and those of its CTA, ordered before by a barrier) are visible to
+// whoever observes the new value, and the caller's later reads see what the
+// earlier arrivals released.
+__device__ __forceinline__ uint32_t atom_add_acq_rel(uint32_t* p, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
 
 __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t p;

@@ -61,7 +61,10 @@ cudaError_t launch_emb_norms(const void* emb, int emb_dtype, int E, const int32_
 // numbered 0 .. n_u-1 in fill order (tile after tile), which is insertion
 // order, hence ascending fact id.  After its rows, each CTA arrives on q's
 // counter; the last one (the counter reaches tiles * n_sub) resets the counter
-// and runs the top-k of q over the scores, which are then in L2.
+// and runs the top-k of q over the scores, which are then in L2.  Up to
+// kRegKeys rows per user, each row's score is also counted into q's cosine
+// bins in global memory (ta.hist), so the top-k starts from a finished
+// histogram.
 //
 // Top-k (topk_block): a cosine-bin histogram locates the bin of the k-th
 // score, the rows in and above it are the candidates (an exact radix select
@@ -69,7 +72,7 @@ cudaError_t launch_emb_norms(const void* emb, int emb_dtype, int E, const int32_
 // (score desc, row asc), so ties go to the lower fact id; ids, scores and the
 // segment plan (exclusive prefix of the facts' lengths) are written.
 template <typename E, bool SMEM_KEYS>
-__global__ void __launch_bounds__(kRetThreads) retrieve_kernel(const SimArgs sa, const TopkArgs ta,
+__global__ void __launch_bounds__(kRetThreads, 4) retrieve_kernel(const SimArgs sa, const TopkArgs ta,
                                                                int n_sub, int32_t* arrive) {
   extern __shared__ uint32_t s_keys[];         // [n] keys of the top-k phase (SMEM_KEYS)
   __shared__ TopkShared sh;
@@ -84,6 +87,11 @@ __global__ void __launch_bounds__(kRetThreads) retrieve_kernel(const SimArgs sa,
   // The query row does not depend on the user lookup: start pulling it into L2.
   if (threadIdx.x * 128 < sa.E * (int)sizeof(E))
     prefetch_l2(reinterpret_cast<const uint8_t*>(sa.q_emb) + ((size_t)q * sa.E * sizeof(E)) + threadIdx.x * 128);
+  // The cosine bins the rows below may count into (64 lines of 128 bytes per
+  // query, one per CTA in turn) and the start the top-k reads last.
+  if (ta.hist && threadIdx.x == 32)
+    prefetch_l2(ta.hist + (size_t)q * kCosBins + (blockIdx.x % (kCosBins / 32)) * 32);
+  if (ta.seg_start && threadIdx.x == 64 && blockIdx.x == 0) prefetch_l2(ta.seg_start + q);
   const int user = sa.users[q];
   const bool user_ok = user >= 0 && user < sa.max_users;
   const int4 um = user_ok ? sa.user_meta[user] : make_int4(0, 0, 0, -1);
@@ -107,6 +115,7 @@ __global__ void __launch_bounds__(kRetThreads) retrieve_kernel(const SimArgs sa,
   const E* qv = reinterpret_cast<const E*>(sa.q_emb) + (size_t)q * sa.E;
   const E* base = reinterpret_cast<const E*>(sa.emb) + (size_t)tile * kTile * sa.E;
   float* out = sa.scores + (size_t)q * sa.score_stride + (size_t)ti * kTile;
+  uint32_t* bins = topk_uses_hist(ta, n_u) ? ta.hist + (size_t)q * kCosBins : nullptr;
   // The top-k will look up the fact, length and arena token of its candidate
   // rows: warm those lines of this CTA's rows now.
   if (threadIdx.x < 3 && r_begin < r_end) {
@@ -136,20 +145,22 @@ __global__ void __launch_bounds__(kRetThreads) retrieve_kernel(const SimArgs sa,
       qq += __shfl_xor_sync(0xffffffffu, qq, o);
     }
     if (lane == 0) {
-      out[r] = dot * (qq > 0.f ? 1.0f / sqrtf(qq) : 0.f) * inv_e;
-      __threadfence();                          // the score before the arrival below
+      const float score = dot * (qq > 0.f ? 1.0f / sqrtf(qq) : 0.f) * inv_e;
+      out[r] = score;
+      if (bins) atomicAdd(bins + cos_bin(score), 1u);
     }
   }
-  // Arrive; the last CTA of query q runs its top-k.
+  // Arrive; the last CTA of query q runs its top-k.  The arrival releases
+  // the CTA's scores and bin counts (ordered before it by the barrier) and,
+  // for the last CTA, acquires everyone else's.
   __syncthreads();
   if (threadIdx.x == 0) {
-    const int done = atomicAdd(&arrive[q], 1);
-    s_last = done == ntiles * n_sub - 1;
+    const uint32_t done = atom_add_acq_rel(reinterpret_cast<uint32_t*>(&arrive[q]), 1u);
+    s_last = done == (uint32_t)(ntiles * n_sub - 1);
     if (s_last) arrive[q] = 0;
   }
   __syncthreads();
   if (!s_last) return;
-  __threadfence();
   // The dependent inject grid may launch once every CTA has exited or
   // triggered: here, when the last one starts its top-k.  Its launch latency
   // then hides under the top-k, and its CTAs are placed on SMs the similarity

@@ -104,6 +104,7 @@ struct is_store {
   int32_t* rows_tmp = nullptr;
   uint32_t* status = nullptr;
   int32_t* arrive = nullptr;      // per-query arrival counters of the retrieval kernel
+  uint32_t* hist = nullptr;       // per-query cosine-bin counts of the retrieval kernel (left zeroed)
   // batched (tensor-core) retrieval
   __half* qg = nullptr;           // [max_queries][E] queries packed in group order
   float* q_inv = nullptr;
@@ -194,7 +195,7 @@ void free_store(is_store_t* s) {
                   s->tile_fact, s->tile_len, s->user_meta, s->tile_tok, s->fact_src, s->user_tiles, s->scores,
                   s->ids_tmp, s->scores_tmp, s->fact_seg_off, s->n_ids, s->seg_len_tmp,
                   s->rows_tmp, s->status, s->arrive, s->qg, s->q_inv, s->qperm, s->groups, s->counts,
-                  s->cap_seg, s->work_ctr};
+                  s->cap_seg, s->work_ctr, s->hist};
   for (void* p : ptrs)
     if (p) cudaFree(p);
   for (int st = 0; st < IS_NUM_STAGES; ++st)
@@ -476,6 +477,7 @@ is_status_t is_store_create(const is_store_config_t* config, int device, cudaStr
   ALLOC(rows_tmp, (size_t)c.max_facts * 4, "row list");
   ALLOC(status, 4, "status word");
   ALLOC(arrive, Q * 4, "arrival counters");
+  ALLOC(hist, Q * kCosBins * 4, "cosine bins");
   ALLOC(qg, Q * (size_t)c.emb_dim * 2, "packed queries");
   ALLOC(q_inv, Q * 4, "query norms");
   ALLOC(qperm, Q * 4, "query order");
@@ -484,11 +486,12 @@ is_status_t is_store_create(const is_store_config_t* config, int device, cudaStr
   ALLOC(cap_seg, (size_t)std::min<int64_t>(c.max_facts, IS_MAX_CAPTURE_FACTS) * 16, "capture segments");
   ALLOC(work_ctr, 8, "inject chunk counters");
 #undef ALLOC
-  s->scratch_bytes = (int64_t)(Q * s->score_stride * 4 + Q * c.max_k * 12 +
+  s->scratch_bytes = (int64_t)(Q * s->score_stride * 4 + Q * c.max_k * 12 + Q * kCosBins * 4 +
                                R * (s->seg_stride * 4 + 8) + (size_t)c.max_facts * 4 + 4);
   cudaError_t e = cudaMemsetAsync(s->status, 0, 4, stream);
   if (e == cudaSuccess) e = cudaMemsetAsync(s->user_meta, 0, (size_t)c.max_users * sizeof(int4), stream);
   if (e == cudaSuccess) e = cudaMemsetAsync(s->arrive, 0, Q * 4, stream);
+  if (e == cudaSuccess) e = cudaMemsetAsync(s->hist, 0, Q * kCosBins * 4, stream);
   if (e == cudaSuccess) e = cudaMemsetAsync(s->work_ctr, 0, 8, stream);
   if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
   if (e != cudaSuccess) {
@@ -801,6 +804,7 @@ static is_status_t run_retrieval(is_store_t* s, int32_t Q, const int32_t* users,
   ta.Q = Q;
   ta.k = k;
   ta.max_users = s->cfg.max_users;
+  ta.hist = batched ? nullptr : s->hist;
   if (!batched) {
     StageTimer tm(s, IS_STAGE_SIMILARITY, stream);
     CUDA_TRY(launch_retrieve(sa, ta, s->cfg.emb_dtype, s->max_user_tiles, s->max_user_facts, s->arrive,

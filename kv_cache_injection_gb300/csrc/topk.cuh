@@ -32,7 +32,8 @@ __device__ __forceinline__ uint32_t warp_excl_scan(uint32_t x, int lane, uint32_
 }
 
 constexpr int kCandMax = IS_MAX_K;          // candidates sorted exactly (10-bit slot index)
-constexpr int kCosBins = 2048;
+constexpr int kRegPer = 8;                  // scores per thread held in registers (REG mode)
+constexpr int kRegKeys = kRegPer * kRetThreads;
 static_assert(kCosBins % kRetThreads == 0 && kRetThreads <= kCandMax && kRetThreads <= 1024,
               "bins split evenly over the threads; the rank path holds one candidate per thread");
 
@@ -53,6 +54,13 @@ __device__ __forceinline__ int cos_bin(float s) {
 
 __device__ __forceinline__ unsigned long long sel_entry(uint32_t key, uint32_t row, uint32_t slot) {
   return ((unsigned long long)key << 32) | ((unsigned long long)(0xFFFFFu - row) << 10) | slot;
+}
+
+// True when the similarity CTAs of a query over n rows count their scores
+// into a.hist and its top-k takes the register path (the two sides must agree:
+// the top-k zeroes the bins it read for the next call).
+__device__ __forceinline__ bool topk_uses_hist(const TopkArgs& a, int n) {
+  return a.hist != nullptr && n >= 1 && n <= kRegKeys;
 }
 
 // Records candidate `slot` = row j of the user: its fact id and length.
@@ -79,7 +87,9 @@ __device__ __forceinline__ void plan_tail(const TopkArgs& a, int q, int nn, int3
 
 // The top-k of query q by the whole CTA (kRetThreads threads):
 //  A. load the n scores (8 loads in flight per thread), stage their
-//     order-preserving keys, histogram their cosine bins;
+//     order-preserving keys, histogram their cosine bins; or, when the
+//     similarity CTAs already counted the bins (topk_uses_hist), load each
+//     thread's 8 scores and 8 bins into registers and zero those bins;
 //  B. find the bin b* holding the k-th largest score;
 //  C. candidates = every row in bins >= b* (k plus the rest of bin b*), with
 //     their fact ids and lengths fetched on the way; if more than kCandMax
@@ -93,7 +103,10 @@ __device__ void topk_block(const TopkArgs& a, TopkShared& sh, uint32_t* s_keys, 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int kk = min(a.k, n);
   const float* sc = a.scores + (size_t)q * a.score_stride;
-  auto key_at = [&](int j) -> uint32_t { return SMEM_KEYS ? s_keys[j] : score_key(__ldcg(sc + j)); };
+  const bool reg = topk_uses_hist(a, n);
+  auto key_at = [&](int j) -> uint32_t {
+    return (SMEM_KEYS && !reg) ? s_keys[j] : score_key(__ldcg(sc + j));
+  };
   if (a.block_table) prefetch_row_l2(a.block_table + (size_t)q * a.max_blocks, a.max_blocks, tid, kRetThreads);
   int64_t* ids = a.ids_out + (size_t)q * a.k;
   float* scs = a.scores_out + (size_t)q * a.k;
@@ -102,23 +115,38 @@ __device__ void topk_block(const TopkArgs& a, TopkShared& sh, uint32_t* s_keys, 
 
   // The first batch of scores is requested before the histogram is cleared,
   // so their latency overlaps the clearing and the barrier.
-  float v[8];
+  constexpr int BPT = kCosBins / kRetThreads;
+  const int hi = kCosBins - 1 - BPT * tid;     // this thread's bins: hi, hi - 1, .., hi - BPT + 1
+  float v[kRegPer];
+  uint32_t c[BPT];
   auto load_batch = [&](int b) {
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
+    for (int u = 0; u < kRegPer; ++u) {
       const int j = b + u * kRetThreads + tid;
       v[u] = j < n ? __ldcg(sc + j) : 0.f;
     }
   };
-  if (kk > 0) load_batch(0);
-  for (int i = tid; i < kCosBins; i += kRetThreads) sh.hist[i] = 0;
-  if (tid == 0) sh.cnt = 0;
-  __syncthreads();
-  if (kk > 0) {
-    for (int b = 0; b < n; b += 8 * kRetThreads) {
+  if (reg) {
+    // All n scores and this thread's bins in one round of loads; the bins are
+    // then zeroed for the next call (this CTA is their only reader).
+    uint32_t* hg = a.hist + (size_t)q * kCosBins;
+    load_batch(0);
+#pragma unroll
+    for (int i = 0; i < BPT; ++i) c[i] = __ldcg(hg + hi - i);
+#pragma unroll
+    for (int i = 0; i < BPT; ++i) __stcg(hg + hi - i, 0u);
+    if (tid == 0) sh.cnt = 0;
+  } else {
+    if (kk > 0) load_batch(0);
+    for (int i = tid; i < kCosBins; i += kRetThreads) sh.hist[i] = 0;
+    if (tid == 0) sh.cnt = 0;
+    __syncthreads();
+  }
+  if (kk > 0 && !reg) {
+    for (int b = 0; b < n; b += kRegPer * kRetThreads) {
       if (b > 0) load_batch(b);
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
+      for (int u = 0; u < kRegPer; ++u) {
         const int j = b + u * kRetThreads + tid;
         if (j < n) {
           if (SMEM_KEYS) s_keys[j] = score_key(v[u]);
@@ -140,12 +168,10 @@ __device__ void topk_block(const TopkArgs& a, TopkShared& sh, uint32_t* s_keys, 
   // B: the bins in descending order, BPT per thread in thread order; a block
   // scan of the per-thread counts finds the thread holding the k-th score.
   {
-    constexpr int BPT = kCosBins / kRetThreads;
-    const int hi = kCosBins - 1 - BPT * tid;
-    uint32_t c[BPT], sum = 0;
+    uint32_t sum = 0;
 #pragma unroll
     for (int i = 0; i < BPT; ++i) {
-      c[i] = sh.hist[hi - i];
+      if (!reg) c[i] = sh.hist[hi - i];
       sum += c[i];
     }
     int32_t tot;
@@ -169,7 +195,25 @@ __device__ void topk_block(const TopkArgs& a, TopkShared& sh, uint32_t* s_keys, 
   if (sh.above + sh.eq <= (uint32_t)kCandMax) {
     const int bstar = sh.bstar;
     C = sh.above + sh.eq;
-    if (SMEM_KEYS) {
+    if (reg) {
+      // Scores in registers: mark this thread's candidates, one block scan
+      // gives its first slot.
+      uint32_t take = 0;
+#pragma unroll
+      for (int u = 0; u < kRegPer; ++u) {
+        const int j = u * kRetThreads + tid;
+        if (j < n && cos_bin(v[u]) >= bstar) take |= 1u << u;
+      }
+      int32_t tot;
+      uint32_t slot = (uint32_t)block_exclusive_scan((int32_t)__popc(take), sh.scratch, &tot);
+#pragma unroll
+      for (int u = 0; u < kRegPer; ++u) {
+        if (take & (1u << u)) {
+          sh.sel[slot] = sel_entry(score_key(v[u]), (uint32_t)(u * kRetThreads + tid), slot);
+          ++slot;
+        }
+      }
+    } else if (SMEM_KEYS) {
       // Keys in shared memory: count this thread's candidates, one block scan
       // gives each thread its first slot, then a second pass writes them.
       uint32_t mine = 0;
@@ -265,36 +309,45 @@ __device__ void topk_block(const TopkArgs& a, TopkShared& sh, uint32_t* s_keys, 
   __syncthreads();
 
   if (C <= (uint32_t)kRetThreads) {
-    // Rank selection: thread t owns candidate t; its rank is the number of
-    // candidates above it (entries are unique).  The fact lookup overlaps the
-    // ranking.  The top kk are then placed by rank (fact and length in
-    // sh.cand, store token in sh.rk_tok, key in the histogram's space), so
-    // thread r writes rank r's outputs and one block scan of the lengths gives
-    // the segment offsets.
+    // Rank selection: candidate c's rank is the number of candidates above it
+    // (entries are unique), counted by S neighbouring threads over every S-th
+    // entry and summed by shuffles; S is the largest power of two up to 8
+    // that keeps S threads per candidate.  The fact lookup (by the first of
+    // the S) overlaps the ranking.  The top kk are then placed by rank (fact
+    // and length in sh.cand, store token in sh.rk_tok, key in the histogram's
+    // space), so thread r writes rank r's outputs and one block scan of the
+    // lengths gives the segment offsets.
     const uint32_t t = (uint32_t)tid;
     int64_t* rk_tok = sh.rk_tok;
     uint32_t* rk_key = sh.hist;                                       // free by now
-    if (t < C) {
-      const unsigned long long e = sh.sel[t];
+    uint32_t S = 1;
+    while (S < 8 && C * S * 2 <= (uint32_t)kRetThreads) S <<= 1;
+    const uint32_t cidx = t / S, part = t % S;
+    const bool have = cidx < C;
+    const unsigned long long e = have ? sh.sel[cidx] : 0ull;
+    int32_t f = 0, len = 0;
+    int64_t tok = 0;
+    if (have && part == 0) {
       const uint32_t j = 0xFFFFFu - (uint32_t)((e >> 10) & 0xFFFFFu);
       const int tile = user_tile(a.user_tiles, um, (int)(j / kTile));
       const size_t row = (size_t)tile * kTile + (j % kTile);
-      const int32_t f = a.tile_fact[row];
-      const int32_t len = a.tile_len[row];
-      const int64_t tok = a.tile_tok[row];
-      uint32_t rank = 0;
-      for (uint32_t i = 0; i < C; ++i) rank += sh.sel[i] > e ? 1u : 0u;
-      if (rank < (uint32_t)kk) {
-        sh.cand[rank] = ((unsigned long long)(uint32_t)len << 32) | (uint32_t)f;
-        rk_tok[rank] = tok;
-        rk_key[rank] = (uint32_t)(e >> 32);
-      }
+      f = a.tile_fact[row];
+      len = a.tile_len[row];
+      tok = a.tile_tok[row];
+    }
+    uint32_t rank = 0;
+    if (have)
+      for (uint32_t i = part; i < C; i += S) rank += sh.sel[i] > e ? 1u : 0u;
+    for (uint32_t o = 1; o < S; o <<= 1) rank += __shfl_xor_sync(0xffffffffu, rank, (int)o);
+    if (have && part == 0 && rank < (uint32_t)kk) {
+      sh.cand[rank] = ((unsigned long long)(uint32_t)len << 32) | (uint32_t)f;
+      rk_tok[rank] = tok;
+      rk_key[rank] = (uint32_t)(e >> 32);
     }
     __syncthreads();
     const unsigned long long cv = t < (uint32_t)kk ? sh.cand[t] : 0ull;
-    const int32_t len = (int32_t)(cv >> 32);
     int32_t total;
-    const int32_t off = block_exclusive_scan(len, sh.scratch, &total);
+    const int32_t off = block_exclusive_scan((int32_t)(cv >> 32), sh.scratch, &total);
     if (t < (uint32_t)kk) {
       ids[t] = (int32_t)(uint32_t)cv;
       scs[t] = key_score(rk_key[t]);
