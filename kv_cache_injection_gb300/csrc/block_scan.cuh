@@ -35,4 +35,32 @@ __device__ __forceinline__ I block_exclusive_scan(I x, I* scratch, I* total) {
   return before + inc - x;
 }
 
+// The same sum with one barrier: each warp scans with shuffles and publishes
+// its total; after the barrier every thread adds up the totals of the warps
+// before its own.  `scratch` holds NWARPS ints and is read after the barrier,
+// so it may be written again only once every thread has passed a later
+// barrier: back-to-back calls alternate between two buffers.
+template <int NWARPS, typename I>
+__device__ __forceinline__ I block_exclusive_scan_1bar(I x, I* scratch, I* total) {
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  I inc = x;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const I y = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += y;
+  }
+  if (lane == 31) scratch[warp] = inc;
+  __syncthreads();
+  I before = I(0), tot = I(0);
+#pragma unroll
+  for (int w = 0; w < NWARPS; ++w) {
+    const I t = scratch[w];
+    if (w < warp) before += t;
+    tot += t;
+  }
+  *total = tot;
+  return before + inc - x;
+}
+
 }  // namespace isk

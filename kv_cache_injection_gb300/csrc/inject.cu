@@ -336,12 +336,20 @@ __global__ void __launch_bounds__(kInjectWarpsMax * 32) inject_kernel(const Inje
   }
   __syncwarp();
   warm8(a.seg_len, a.n_ids, a.fact_seg_off, a.fact_src, a.seg_start, a.block_table, a.slot_mapping, a.ids);
+  // What does not depend on the plan is set up before the wait.  Kernel
+  // parameters live in the constant bank: reading the remaining ones here
+  // (the chunk pool's fields, the FP8 scales, this lane's rotation turns)
+  // keeps their first use after the wait from missing there.
+  const int groups = (a.n_layers + G - 1) / G;   // items per token
+  const int fbase = STYLE == 0 ? (lane % a.half_vecs) * VE : (lane % a.head_vecs) * (VE / 2);
+  asm volatile("" ::"r"(a.chunk_items), "l"(a.work_ctr), "l"(a.work_ctr_next), "f"(a.k_inv), "f"(a.v_inv),
+               "r"(a.row_bytes), "r"(a.block_size), "r"(a.num_blocks));
+  asm volatile("" ::"f"(rt.hi[fbase]), "f"(rt.lo[fbase]), "f"(rt.hi[fbase + NF - 1]), "f"(rt.lo[fbase + NF - 1]));
   pdl_wait();                                   // outputs of the planning kernel
 
   const int32_t *s_off, *s_start;
   const int32_t total = segment_prefix(a, off_region, scratch, &s_off, &s_start);
 
-  const int groups = (a.n_layers + G - 1) / G;   // items per token
   const int64_t n_items = (int64_t)total * groups;
   const int64_t warp_id = (int64_t)blockIdx.x * nwarps + warp;
   const int64_t n_warps = (int64_t)gridDim.x * nwarps;
@@ -378,7 +386,6 @@ __global__ void __launch_bounds__(kInjectWarpsMax * 32) inject_kernel(const Inje
   const uint32_t stage0 = smem_addr(stages);
   const int vpl = a.row_bytes >> 9;             // 16-byte vectors per lane per row
   const int hv = a.half_vecs;
-  const int fbase = STYLE == 0 ? (lane % hv) * VE : (lane % a.head_vecs) * (VE / 2);
 
   TokenCursor cur;
 

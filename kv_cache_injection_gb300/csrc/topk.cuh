@@ -43,6 +43,7 @@ struct TopkShared {
   unsigned long long cand[kCandMax];        // (length << 32) | fact id, by slot (by rank on the rank path)
   int64_t rk_tok[kCandMax];                 // rank path: arena token by rank
   int32_t scratch[33];
+  int32_t scratch2[kRetThreads / 32];       // second buffer of the one-barrier scans
   uint32_t bstar, above, eq, digit, cnt;
 };
 
@@ -175,7 +176,7 @@ __device__ void topk_block(const TopkArgs& a, TopkShared& sh, uint32_t* s_keys, 
       sum += c[i];
     }
     int32_t tot;
-    const uint32_t before = (uint32_t)block_exclusive_scan((int32_t)sum, sh.scratch, &tot);
+    const uint32_t before = (uint32_t)block_exclusive_scan_1bar<kRetThreads / 32>((int32_t)sum, sh.scratch, &tot);
     if (before < (uint32_t)kk && before + sum >= (uint32_t)kk) {
       uint32_t run = before;
 #pragma unroll
@@ -205,7 +206,7 @@ __device__ void topk_block(const TopkArgs& a, TopkShared& sh, uint32_t* s_keys, 
         if (j < n && cos_bin(v[u]) >= bstar) take |= 1u << u;
       }
       int32_t tot;
-      uint32_t slot = (uint32_t)block_exclusive_scan((int32_t)__popc(take), sh.scratch, &tot);
+      uint32_t slot = (uint32_t)block_exclusive_scan_1bar<kRetThreads / 32>((int32_t)__popc(take), sh.scratch2, &tot);
 #pragma unroll
       for (int u = 0; u < kRegPer; ++u) {
         if (take & (1u << u)) {
@@ -219,7 +220,7 @@ __device__ void topk_block(const TopkArgs& a, TopkShared& sh, uint32_t* s_keys, 
       uint32_t mine = 0;
       for (int j = tid; j < n; j += kRetThreads) mine += cos_bin(key_score(s_keys[j])) >= bstar ? 1u : 0u;
       int32_t tot;
-      uint32_t slot = (uint32_t)block_exclusive_scan((int32_t)mine, sh.scratch, &tot);
+      uint32_t slot = (uint32_t)block_exclusive_scan_1bar<kRetThreads / 32>((int32_t)mine, sh.scratch2, &tot);
       for (int j = tid; j < n; j += kRetThreads) {
         const uint32_t key = s_keys[j];
         if (cos_bin(key_score(key)) >= bstar) {
@@ -336,8 +337,18 @@ __device__ void topk_block(const TopkArgs& a, TopkShared& sh, uint32_t* s_keys, 
       tok = a.tile_tok[row];
     }
     uint32_t rank = 0;
-    if (have)
-      for (uint32_t i = part; i < C; i += S) rank += sh.sel[i] > e ? 1u : 0u;
+    if (have) {
+      // Four independent counts keep four shared-memory reads in flight.
+      uint32_t r0 = 0, r1 = 0, r2 = 0, r3 = 0, i = part;
+      for (; i + 3 * S < C; i += 4 * S) {
+        r0 += sh.sel[i] > e ? 1u : 0u;
+        r1 += sh.sel[i + S] > e ? 1u : 0u;
+        r2 += sh.sel[i + 2 * S] > e ? 1u : 0u;
+        r3 += sh.sel[i + 3 * S] > e ? 1u : 0u;
+      }
+      for (; i < C; i += S) r0 += sh.sel[i] > e ? 1u : 0u;
+      rank = r0 + r1 + r2 + r3;
+    }
     for (uint32_t o = 1; o < S; o <<= 1) rank += __shfl_xor_sync(0xffffffffu, rank, (int)o);
     if (have && part == 0 && rank < (uint32_t)kk) {
       sh.cand[rank] = ((unsigned long long)(uint32_t)len << 32) | (uint32_t)f;
@@ -347,7 +358,7 @@ __device__ void topk_block(const TopkArgs& a, TopkShared& sh, uint32_t* s_keys, 
     __syncthreads();
     const unsigned long long cv = t < (uint32_t)kk ? sh.cand[t] : 0ull;
     int32_t total;
-    const int32_t off = block_exclusive_scan((int32_t)(cv >> 32), sh.scratch, &total);
+    const int32_t off = block_exclusive_scan_1bar<kRetThreads / 32>((int32_t)(cv >> 32), sh.scratch, &total);
     if (t < (uint32_t)kk) {
       ids[t] = (int32_t)(uint32_t)cv;
       scs[t] = key_score(rk_key[t]);
