@@ -55,8 +55,8 @@ struct InjectArgs {
   int32_t head_vecs;            // 16-byte vectors per head (D / VE)
   int32_t cache_row_bytes;      // H * D * elt of the cache (row_bytes, or H * D for FP8)
   float k_inv, v_inv;           // FP8 cache: fp32(1 / k_scale), fp32(1 / v_scale)
-  uint32_t* work_ctr;           // pool chunks claimed in this launch (zero at its start)
-  uint32_t* work_ctr_next;      // the counter of the next launch, zeroed by this one
+  uint32_t* work_ctr;           // kPoolCtrs counters of pool claims in this launch (zero at its start)
+  uint32_t* work_ctr_next;      // the counters of the next launch, zeroed by this one
   int32_t chunk_items;          // items per pool chunk (set by the launcher)
 };
 
@@ -95,6 +95,13 @@ struct PlanArgs {
   uint32_t* status;
   int32_t R;
 };
+
+// The inject kernel's pool of work chunks is claimed through kPoolCtrs
+// counters, kCtrStride words (one 128-byte line) apart; a launch uses one set
+// of kPoolCtrWords words and zeroes the other for the next launch.
+constexpr int kPoolCtrs = 16;
+constexpr int kCtrStride = 32;
+constexpr int kPoolCtrWords = kPoolCtrs * kCtrStride;
 
 // Uniform bins of the cosine in [-1, 1] used by the top-k's first pass.
 constexpr int kCosBins = 2048;
@@ -234,6 +241,10 @@ __device__ __forceinline__ uint2 to_e4m3x8(const float* x, float r) {
 
 __device__ __forceinline__ void prefetch_l2(const void* p) {
   asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
+__device__ __forceinline__ void prefetch_l1(const void* p) {
+  asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
 }
 
 // Thread i < 8 prefetches the first line of p_i into L2 (null pointers are

@@ -191,6 +191,22 @@ __device__ __forceinline__ int32_t segment_prefix(const InjectArgs& a, int32_t* 
   return total;
 }
 
+// One warp pulls block-table lines into L1: up to kBtLines 128-byte lines in
+// all, split evenly over the requests (at least one each for the first
+// kBtLines), each request's from the line of its first position on.
+constexpr int kBtLines = 128;
+__device__ __forceinline__ void prefetch_block_rows(const InjectArgs& a, int lane) {
+  if (!a.block_table || a.R <= 0) return;
+  const int per = max(1, kBtLines / a.R);
+  const int row_lines = (a.max_blocks + 31) >> 5;
+  for (int i = lane; i < kBtLines && i < a.R * per; i += 32) {
+    const int r = i / per;
+    const int start = a.seg_start[r];
+    const int line = (start >= 0 ? start / a.block_size : 0) / 32 + i % per;
+    if (line < row_lines) prefetch_l1(a.block_table + (size_t)r * a.max_blocks + (size_t)line * 32);
+  }
+}
+
 // Warp-uniform walk from a composed-segment token t (all requests back to
 // back) to its store token, serving position and destination slot.  Tokens a
 // warp visits are consecutive, so the request, fact and block-table entry found
@@ -345,6 +361,10 @@ __global__ void __launch_bounds__(kInjectWarpsMax * 32) inject_kernel(const Inje
   asm volatile("" ::"r"(a.chunk_items), "l"(a.work_ctr), "l"(a.work_ctr_next), "f"(a.k_inv), "f"(a.v_inv),
                "r"(a.row_bytes), "r"(a.block_size), "r"(a.num_blocks));
   asm volatile("" ::"f"(rt.hi[fbase]), "f"(rt.lo[fbase]), "f"(rt.hi[fbase + NF - 1]), "f"(rt.lo[fbase + NF - 1]));
+  // The block table and the starts are the caller's inputs, not the planning
+  // kernel's outputs: bring the rows' first lines, from each request's start
+  // on, into this SM's L1 now, so position lookups after the wait hit there.
+  if (warp == 0) prefetch_block_rows(a, lane);
   pdl_wait();                                   // outputs of the planning kernel
 
   const int32_t *s_off, *s_start;
@@ -355,23 +375,29 @@ __global__ void __launch_bounds__(kInjectWarpsMax * 32) inject_kernel(const Inje
   const int64_t n_warps = (int64_t)gridDim.x * nwarps;
   // Each warp first takes a fixed, contiguous share of kStaticPct % of an even
   // split; the rest of the items form a pool handed out in chunks of CH to
-  // whichever warp asks first (a counter in global memory).  Warps that run
-  // faster take more of the pool, so the launch ends with the work rather
-  // than with its slowest warp, and the claims come late and spread out in
-  // time.  A warp claims its next chunk when its current run is down to its
+  // whichever warp asks first.  Warps on SMs that move data faster (the
+  // spread is systematic, about +-15 %) take more of the pool, so the launch
+  // ends with the work rather than with its slowest warp.  The pool is dealt
+  // round-robin over kPoolCtrs counters (chunk c belongs to counter c %
+  // kPoolCtrs) and each warp claims from one of them only, so no single
+  // address takes every claim and a finished pool costs each warp one failed
+  // claim.  A warp claims its next chunk when its current run is down to its
   // last kClaimAhead items, so the claim's latency hides behind them.  The
-  // counter of this launch was zeroed by the previous one; this launch zeroes
-  // the other counter for the next.
-  // Launches with little work per warp (fewer than kMinShare static items)
-  // split the items evenly and use no pool: their claims would all arrive at
-  // once on one address.
+  // counters of this launch were zeroed by the previous one; this launch
+  // zeroes the other set for the next.  Chunks are at most a quarter of the
+  // static share; launches with fewer than kMinShare static items per warp
+  // split evenly and use no pool.  So do launches into an FP8 cache: their
+  // warps end close together without a pool, and a pool's chunks (a position
+  // lookup and a claim each, a new token's angles) measured slower there.
   constexpr int kClaimAhead = 2;
   constexpr int kStaticPct = 50;
-  constexpr int kMinShare = 64;
-  if (blockIdx.x == 0 && threadIdx.x == 0) *a.work_ctr_next = 0u;
-  const int64_t CH = a.chunk_items;
+  constexpr int kMinShare = 4;
+  if (blockIdx.x == 0 && threadIdx.x < kPoolCtrs) a.work_ctr_next[threadIdx.x * kCtrStride] = 0u;
+  const int home = (int)(warp_id % kPoolCtrs);
+  uint32_t* const home_ctr = a.work_ctr + home * kCtrStride;
   int64_t share = div_nn(n_items * kStaticPct / 100, n_warps);
-  if (share < kMinShare) share = div_nn(n_items + n_warps - 1, n_warps);
+  if (F8 || share < kMinShare) share = div_nn(n_items + n_warps - 1, n_warps);
+  const int64_t CH = min((int64_t)a.chunk_items, max((int64_t)1, share >> 2));
   const int64_t pool0 = min(n_items, share * n_warps);   // first pool item
   const int64_t n_chunks = div_nn(n_items - pool0 + CH - 1, CH);
   int64_t next_claim = 0;                        // lane 0: the pool chunk claimed next
@@ -394,7 +420,7 @@ __global__ void __launch_bounds__(kInjectWarpsMax * 32) inject_kernel(const Inje
   auto next_item = [&](int32_t& t, int32_t& l) -> bool {
     if (left == 0) {
       if (stream_done) return false;
-      if (!claimed && lane == 0) next_claim = (int64_t)atomicAdd(a.work_ctr, 1u);
+      if (!claimed && lane == 0) next_claim = (int64_t)atomicAdd(home_ctr, 1u) * kPoolCtrs + home;
       claimed = false;
       const int64_t c = __shfl_sync(0xffffffffu, next_claim, 0);
       if (c >= n_chunks) {
@@ -410,7 +436,7 @@ __global__ void __launch_bounds__(kInjectWarpsMax * 32) inject_kernel(const Inje
     l = ng * G;
     --left;
     if (left <= kClaimAhead && !claimed) {
-      if (lane == 0) next_claim = (int64_t)atomicAdd(a.work_ctr, 1u);
+      if (lane == 0) next_claim = (int64_t)atomicAdd(home_ctr, 1u) * kPoolCtrs + home;
       claimed = true;
     }
     if (++ng == groups) {
@@ -811,12 +837,14 @@ namespace {
 
 constexpr int kNaRequests = IS_NOALLOC_MAX_REQUESTS;
 constexpr int kNaSegStride = IS_NOALLOC_MAX_FACTS + 1;
-constexpr size_t kNaWords = (size_t)kNaRequests * kNaSegStride + 2 * kNaRequests + 2;
+constexpr size_t kNaCtrOff = ((size_t)kNaRequests * kNaSegStride + 2 * kNaRequests + 31) & ~(size_t)31;
+constexpr size_t kNaWords = kNaCtrOff + 2 * isk::kPoolCtrWords;
 constexpr int kNaMaxDevices = 64;
 
 // [0, R*stride): per-request prefix of fact lengths; then n_ids[R]; then
-// seg_len[R]; then the inject kernel's two chunk counters, used by alternate
-// launches (zero at load; each launch zeroes the other one).
+// seg_len[R]; then, from a 128-byte boundary, the inject kernel's two sets of
+// chunk counters, used by alternate launches (zero at load; each launch
+// zeroes the other set).
 static __device__ __align__(256) int32_t g_noalloc_scratch[kNaWords];
 
 struct NoAllocDevice {
@@ -950,9 +978,9 @@ extern "C" is_status_t is_inject_noalloc(
   a.row_bytes = (int32_t)row_bytes;
   a.cache_row_bytes = (int32_t)row_bytes;
   {
-    uint32_t* ctr = reinterpret_cast<uint32_t*>(d.scratch + (size_t)kNaRequests * kNaSegStride + 2 * kNaRequests);
-    a.work_ctr = ctr + d.parity;
-    a.work_ctr_next = ctr + (d.parity ^ 1);
+    uint32_t* ctr = reinterpret_cast<uint32_t*>(d.scratch + kNaCtrOff);
+    a.work_ctr = ctr + (size_t)d.parity * isk::kPoolCtrWords;
+    a.work_ctr_next = ctr + (size_t)(d.parity ^ 1) * isk::kPoolCtrWords;
     d.parity ^= 1;
   }
   a.half_vecs = head_dim / 2 / ve;

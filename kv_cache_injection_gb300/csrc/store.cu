@@ -139,7 +139,7 @@ struct is_store {
   int64_t cap_src_tokens = 0;
   std::vector<uint8_t> cap_layers;
   int64_t* cap_seg = nullptr;     // [IS_MAX_CAPTURE_FACTS][2] {first source token, first arena token}
-  uint32_t* work_ctr = nullptr;   // [2] the inject kernel's chunk counters, alternate launches
+  uint32_t* work_ctr = nullptr;   // [2][kPoolCtrWords] the inject kernel's chunk counters, alternate launches
   int work_parity = 0;
   PendingFacts cap_pending;
 
@@ -484,7 +484,7 @@ is_status_t is_store_create(const is_store_config_t* config, int device, cudaStr
   ALLOC(groups, Q * sizeof(int4), "query groups");
   ALLOC(counts, 8, "group counts");
   ALLOC(cap_seg, (size_t)std::min<int64_t>(c.max_facts, IS_MAX_CAPTURE_FACTS) * 16, "capture segments");
-  ALLOC(work_ctr, 8, "inject chunk counters");
+  ALLOC(work_ctr, 2 * kPoolCtrWords * 4, "inject chunk counters");
 #undef ALLOC
   s->scratch_bytes = (int64_t)(Q * s->score_stride * 4 + Q * c.max_k * 12 + Q * kCosBins * 4 +
                                R * (s->seg_stride * 4 + 8) + (size_t)c.max_facts * 4 + 4);
@@ -492,7 +492,7 @@ is_status_t is_store_create(const is_store_config_t* config, int device, cudaStr
   if (e == cudaSuccess) e = cudaMemsetAsync(s->user_meta, 0, (size_t)c.max_users * sizeof(int4), stream);
   if (e == cudaSuccess) e = cudaMemsetAsync(s->arrive, 0, Q * 4, stream);
   if (e == cudaSuccess) e = cudaMemsetAsync(s->hist, 0, Q * kCosBins * 4, stream);
-  if (e == cudaSuccess) e = cudaMemsetAsync(s->work_ctr, 0, 8, stream);
+  if (e == cudaSuccess) e = cudaMemsetAsync(s->work_ctr, 0, 2 * kPoolCtrWords * 4, stream);
   if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
   if (e != cudaSuccess) {
     free_store(s);
@@ -914,8 +914,8 @@ static is_status_t launch_injection(is_store_t* s, int32_t R, const int64_t* ids
   a.layer_stride = layer_stride;
   a.row_bytes = (int32_t)s->row_bytes;
   a.cache_row_bytes = (int32_t)cache_row_bytes(s, cache);
-  a.work_ctr = s->work_ctr + s->work_parity;
-  a.work_ctr_next = s->work_ctr + (s->work_parity ^ 1);
+  a.work_ctr = s->work_ctr + (size_t)s->work_parity * kPoolCtrWords;
+  a.work_ctr_next = s->work_ctr + (size_t)(s->work_parity ^ 1) * kPoolCtrWords;
   a.k_inv = (float)(1.0 / (double)cache->k_scale);
   a.v_inv = (float)(1.0 / (double)cache->v_scale);
   const int ve = 16 / s->elt;
