@@ -219,3 +219,99 @@ def test_rope_frequencies_match_oracle(api):
     want = rope.inv_freq(128, r.theta, 1, r.factor, r.low_freq_factor, r.high_freq_factor,
                          r.original_max_pos)
     assert np.allclose(got, want, rtol=1e-14, atol=0)
+
+
+@pytest.mark.parametrize("n", [1, 255, 2047, 2048, 2049])
+def test_topk_around_the_register_path(api, n):
+    """Users of n facts either side of 2048, where the top-k switches from bins
+    counted by the similarity CTAs (kept zeroed between calls) to a shared-memory
+    histogram.  Repeated calls with different k on one store, each against the
+    oracle, and the fused path after them."""
+    import torch
+    spec = SMALL_BF16.with_(n_users=2, facts_per_user=n, n_queries=2, k=min(50, n), seed=40 + n,
+                            length_dist=("uniform", 1, 3), tokens_cap=300 * 3)
+    wl = workloads.generate(spec)
+    store = staging.load_store(wl, api, max_k=300)
+    try:
+        inp = staging.device_inputs(wl)
+        for k in (1, 50, 300, 7, 50):
+            ids = torch.empty((2, k), dtype=torch.int64, device="cuda")
+            sc = torch.empty((2, k), dtype=torch.float32, device="cuda")
+            api.is_retrieve_topk(store, inp["users"], inp["q_emb"], k, ids, sc)
+            g, gs = ids.cpu().numpy(), sc.cpu().numpy()
+            for q in range(2):
+                o_ids, o_sc, score_of = parity.oracle_retrieve(wl, q, k)
+                parity.check_topk(g[q], gs[q], o_ids, o_sc, score_of, k)
+        cache = staging.canary_cache(wl)
+        out = gh.run_fused(api, store, wl, inp, cache)
+        assert out["status"] == 0
+        for q in range(2):
+            o_ids, o_sc, score_of = parity.oracle_retrieve(wl, q, wl.spec.k)
+            parity.check_topk(out["ids"][q], out["scores"][q], o_ids, o_sc, score_of, wl.spec.k)
+        _full_compare(wl, cache, out["ids"], out["seg_len"], out["slot_map"], 0)
+        assert api.is_get_status(store) == 0
+    finally:
+        store.destroy()
+
+
+def test_topk_heavy_ties_on_the_register_path(api):
+    """2000 facts of one user whose embeddings take only 4 values: more than
+    1024 rows share the k-th bin, so the exact radix select takes over from the
+    bins the similarity CTAs counted; ties still go to the lower fact id."""
+    import torch
+    spec = SMALL_BF16.with_(n_users=1, facts_per_user=2000, n_queries=2, k=60, seed=61,
+                            length_dist=("uniform", 1, 2), tokens_cap=60 * 2)
+    wl = workloads.generate(spec)
+    base = wl.emb[:4].copy()
+    wl.emb[:] = base[np.arange(2000) % 4]
+    wl.queries[:] = base[[1, 2]]
+    store = staging.load_store(wl, api, max_k=1024)
+    try:
+        inp = staging.device_inputs(wl)
+        for k in (60, 600, 1024):
+            ids = torch.empty((2, k), dtype=torch.int64, device="cuda")
+            sc = torch.empty((2, k), dtype=torch.float32, device="cuda")
+            api.is_retrieve_topk(store, inp["users"], inp["q_emb"], k, ids, sc)
+            g = ids.cpu().numpy()
+            for q in range(2):
+                o_ids, o_sc, score_of = parity.oracle_retrieve(wl, q, k)
+                head = min(k, 500)                    # the query's own value: 500 exact ties
+                assert np.array_equal(g[q][:head], o_ids[:head]), (k, q)
+                parity.check_topk(g[q], sc.cpu().numpy()[q], o_ids, o_sc, score_of, k)
+        assert api.is_get_status(store) == 0
+    finally:
+        store.destroy()
+
+
+@pytest.mark.parametrize("cache_dtype", [None, "e4m3"])
+def test_chunk_pool_over_consecutive_launches(api, cache_dtype):
+    """A launch with enough items per warp that the inject kernel hands half of
+    them out through its claim counters (about 5600 tokens x 4 layers of 2 KiB
+    rows), run three times: the counters alternate between launches, and every
+    run must write the same cache, equal to the oracle's (an FP8 cache takes
+    the even split instead)."""
+    import torch
+    spec = SMALL_BF16.with_(num_layers=4, num_kv_heads=8, head_dim=128, n_users=1, facts_per_user=400,
+                            length_dist=("uniform", 24, 32), n_queries=1, k=200, tokens_cap=200 * 32,
+                            seed=77)
+    wl = workloads.generate(spec)
+    store = staging.load_store(wl, api)
+    try:
+        inp = staging.device_inputs(wl)
+        caches, outs = [], []
+        for _ in range(3):
+            c = staging.canary_cache(wl, cache_dtype=cache_dtype)
+            outs.append(gh.run_fused(api, store, wl, inp, c, cache_dtype=cache_dtype))
+            caches.append(c)
+        assert all(o["status"] == 0 for o in outs)
+        assert int(outs[0]["seg_len"][0]) * 4 >= 2 * 2432 * 4       # the pool is in use
+        for c in caches[1:]:
+            assert torch.equal(c.view(torch.uint8), caches[0].view(torch.uint8))
+        if cache_dtype is None:
+            _full_compare(wl, caches[0], outs[0]["ids"], outs[0]["seg_len"], outs[0]["slot_map"], 0)
+        else:
+            plans, lens = parity.oracle_plans(wl, outs[0]["ids"])
+            want = np.concatenate([[e[3] for e in pl] for pl in plans]).astype(np.int64)
+            gh.assert_only_slots_changed(caches[0], "e4m3", want)
+    finally:
+        store.destroy()
