@@ -196,10 +196,12 @@ def workload_description(s) -> str:
             f"k={k}, block {s.block_size}")
 
 
-def run_ours(args, rank, world, local_rank):
+def prepare(args, rank, local_rank, extra_facts=0, extra_tokens=0):
+    """Builds the library, the workload's store (with room for extra_facts
+    facts of extra_tokens tokens more) and its device inputs."""
     import torch
 
-    from kv_cache_injection_gb300 import api
+    from kv_cache_injection_gb300 import _lib, api
     from kv_cache_injection_gb300 import build as kbuild
     from synth import staging, workloads
 
@@ -217,12 +219,21 @@ def run_ours(args, rank, world, local_rank):
         overrides["tokens_cap"] = args.k * int(spec.length_dist[2] if spec.length_dist[0] == "uniform"
                                                 else spec.tokens_cap // spec.k)
     wl = workloads.get(args.workload, **overrides)
-    s = wl.spec
-    store = staging.load_store(wl, api, device=local_rank, kv_placement=args.kv_placement)
-    from kv_cache_injection_gb300 import _lib
+    store = staging.load_store(wl, api, device=local_rank, kv_placement=args.kv_placement,
+                               max_facts=wl.spec.n_facts + extra_facts,
+                               max_facts_per_user=wl.spec.facts_per_user + extra_facts,
+                               max_tokens=wl.total_tokens + extra_tokens)
     api.is_set_retrieval_mode(store, {"auto": _lib.IS_RETRIEVAL_AUTO, "per_query": _lib.IS_RETRIEVAL_PER_QUERY,
                                       "batched": _lib.IS_RETRIEVAL_BATCHED}[args.retrieval])
     inp = staging.device_inputs(wl, local_rank)
+    return api, staging, wl, store, inp, dev
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+
+    api, staging, wl, store, inp, dev = prepare(args, rank, local_rank)
+    s = wl.spec
     cache = staging.canary_cache(wl, local_rank, cache_dtype=args.cache_dtype)
     Q, k = s.n_queries, s.k
     ids = torch.empty((Q, k), dtype=torch.int64, device=dev)
@@ -431,6 +442,189 @@ def run_ours(args, rank, world, local_rank):
     return result
 
 
+# ----------------------------------------------------------------------------- other entry points
+
+def _per_launch(events):
+    return [a.elapsed_time(b) for a, b in events]
+
+
+def run_layerwise(args, rank, world, local_rank):
+    """Layer-wise injection as a layer-by-layer KV connector calls it: the ids
+    of one retrieval, then one is_inject_layer call per layer into that layer's
+    own cache tensor (the first call plans the segments, the others reuse the
+    plan).  CUDA events around every call, L2 flushed between steps."""
+    import torch
+
+    api, staging, wl, store, inp, dev = prepare(args, rank, local_rank)
+    s = wl.spec
+    Q, k, L = s.n_queries, s.k, s.num_layers
+    cache_dtype = args.cache_dtype or s.kv_dtype
+    ids = torch.empty((Q, k), dtype=torch.int64, device=dev)
+    scores = torch.empty((Q, k), dtype=torch.float32, device=dev)
+    api.is_retrieve_topk(store, inp["users"], inp["q_emb"], k, ids, scores)
+    n_ids = (ids >= 0).sum(dim=1).to(torch.int32)
+    shape = (2, wl.num_blocks, s.block_size, s.num_kv_heads, s.head_dim)
+    caches = [torch.empty(shape, dtype=staging.torch_dtype(cache_dtype), device=dev) for _ in range(L)]
+    for c in caches:
+        staging.refill_canary(c, cache_dtype)
+    seg_len = torch.empty(Q, dtype=torch.int32, device=dev)
+    rope = staging.rope_params(wl, api)
+    cdesc = api.make_cache_desc(s.block_size, wl.num_blocks, cache_dtype)
+    flush = L2Flush(dev)
+    stream = torch.cuda.current_stream()
+
+    def step(events=None):
+        for l in range(L):
+            if events is not None:
+                events[l][0].record(stream)
+            api.is_inject_layer(store, l, Q, inp["seg_start"], rope, inp["block_table"], cdesc, caches[l],
+                                fact_ids=ids if l == 0 else None, n_ids=n_ids if l == 0 else None,
+                                users=inp["users"] if l == 0 else None,
+                                seg_len_out=seg_len if l == 0 else None, stream=stream)
+            if events is not None:
+                events[l][1].record(stream)
+
+    clocks = ClockSampler(local_rank).__enter__()
+    for _ in range(args.warmup):
+        flush()
+        step()
+    torch.cuda.synchronize()
+    if api.is_get_status(store):
+        raise RuntimeError("device status bits set during warm-up")
+    tokens = int(seg_len.sum().item())
+    # Two passes: "host-paced", the calls submitted as the GPU runs them (each
+    # call's host cost shows); "queued", the stream held by a short GPU delay
+    # while the host submits all L calls, so the events time the GPU side.
+    res = {}
+    for mode in ("host_paced", "queued"):
+        first, later, total = [], [], []
+        for _ in range(args.steps):
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(L)]
+            flush()
+            if mode == "queued":
+                torch.cuda._sleep(int(L * 40e-6 * 2.0e9))          # ~40 us of GPU time per layer call
+            step(ev)
+            torch.cuda.synchronize()
+            d = _per_launch(ev)
+            first.append(d[0])
+            later.extend(d[1:])
+            total.append(ev[0][0].elapsed_time(ev[-1][1]))
+        res[mode] = (first, later, total)
+    clocks.__exit__(None, None, None)
+    first, later, total = res["queued"]
+    if api.is_get_status(store):
+        raise RuntimeError("device status bits set in the timed region")
+    store.destroy()
+    elt = 1 if cache_dtype == "e4m3" else s.elt_bytes
+    layer_bytes = tokens * 2 * s.num_kv_heads * s.head_dim * (s.elt_bytes + elt)   # K+V read and written
+    later_ms = statistics.mean(later) if later else statistics.mean(first)
+    peaks = measured_peaks()
+    achieved = layer_bytes / (later_ms * 1e-3) / 1e9
+    step_ms = statistics.mean(total)
+    return {"metric": "layer-wise injected KV tokens/s (one is_inject_layer call per layer, plan from the first)",
+            "value": tokens / (step_ms * 1e-3), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "dtype": s.kv_dtype,
+            "data": "synthetic (seeded)",
+            "config": {"workload": workload_description(s), "tokens_per_step": tokens, "layers": L,
+                       "cache_dtype": cache_dtype,
+                       "l2": "flushed between steps, outside the events; events around every layer call",
+                       "timing": "queued: a GPU delay holds the stream while the host submits the L calls"},
+            "per_layer_us": {"first_with_plan": statistics.mean(first) * 1e3, "later": later_ms * 1e3},
+            "host_paced": {"ms_per_step": statistics.mean(res["host_paced"][2]),
+                           "per_layer_us": statistics.mean(res["host_paced"][1]) * 1e3,
+                           "value": tokens / (statistics.mean(res["host_paced"][2]) * 1e-3)},
+            "roofline": {"bound": "hbm", "kernel": "inject, one layer per launch", "achieved": achieved,
+                         "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                         "algorithmic_bytes": layer_bytes, "traffic": None},
+            "clocks": clocks.summary()}
+
+
+def run_capture(args, rank, world, local_rank):
+    """Context-Window Encoding capture: per step, is_store_capture_begin for
+    --capture-facts facts (fact lengths from the workload, windows of
+    --window tokens before each), one is_store_capture_layer call per layer
+    from synthetic engine layer buffers, and is_store_capture_abort (so the
+    store does not grow).  CUDA events around every layer call."""
+    import numpy as np
+    import torch
+
+    from synth import workloads
+    n = args.capture_facts
+    lengths = np.resize(workloads.get(args.workload).lengths, n).astype(np.int32)
+    api, staging, wl, store, inp, dev = prepare(args, rank, local_rank, extra_facts=n,
+                                                extra_tokens=int(lengths.sum()))
+    s = wl.spec
+    L = s.num_layers
+    rng = np.random.default_rng(5)
+    window = np.full(n, args.window, dtype=np.int32)
+    src_tokens = int((lengths + window).sum())
+    fact_tokens = int(lengths.sum())
+    row = s.num_kv_heads * s.head_dim
+    tdt = staging.torch_dtype(s.kv_dtype)
+    k_buf = torch.empty(src_tokens * row, dtype=tdt, device=dev)
+    v_buf = torch.empty_like(k_buf)
+    from synth import kvgen
+    staging.fill_kv(k_buf, s.kv_dtype, 99, kvgen.STREAM_K, 0)
+    staging.fill_kv(v_buf, s.kv_dtype, 99, kvgen.STREAM_V, 0)
+    edt = torch.float16 if s.emb_dtype == "f16" else torch.float32
+    emb = torch.from_numpy(rng.standard_normal((n, s.emb_dim))).to(edt).to(dev)
+    flush = L2Flush(dev)
+    stream = torch.cuda.current_stream()
+    clocks = ClockSampler(local_rank).__enter__()
+
+    def step(events=None):
+        api.is_store_capture_begin(store, 0, window, lengths, emb, stream=stream)
+        if events is not None:
+            # hold the stream while the host submits the L calls, so the
+            # events time the GPU side
+            torch.cuda._sleep(int(L * 40e-6 * 2.0e9))
+        for l in range(L):
+            if events is not None:
+                events[l][0].record(stream)
+            api.is_store_capture_layer(store, l, k_buf, v_buf, stream=stream)
+            if events is not None:
+                events[l][1].record(stream)
+        torch.cuda.synchronize()
+        api.is_store_capture_abort(store)
+
+    for _ in range(args.warmup):
+        flush()
+        step()
+    per_layer, layers_ms, wall = [], [], []
+    for _ in range(args.steps):
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(L)]
+        flush()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        step(ev)
+        wall.append(time.perf_counter() - t0)
+        d = _per_launch(ev)
+        per_layer.extend(d)
+        layers_ms.append(ev[0][0].elapsed_time(ev[-1][1]))
+    clocks.__exit__(None, None, None)
+    if api.is_get_status(store):
+        raise RuntimeError("device status bits set during the capture")
+    store.destroy()
+    layer_bytes = fact_tokens * 2 * row * s.elt_bytes * 2     # the facts' K+V rows read and written
+    mean_layer = statistics.mean(per_layer)
+    peaks = measured_peaks()
+    achieved = layer_bytes / (mean_layer * 1e-3) / 1e9
+    return {"metric": "captured KV tokens/s (Context-Window Encoding: fact rows of every layer into the store)",
+            "value": fact_tokens / (statistics.mean(layers_ms) * 1e-3), "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": statistics.mean(layers_ms),
+            "higher_is_better": True, "dtype": s.kv_dtype, "data": "synthetic (seeded)",
+            "config": {"workload": workload_description(s), "facts": n, "window_tokens": args.window,
+                       "fact_tokens": fact_tokens, "source_tokens": src_tokens, "layers": L,
+                       "l2": "flushed between steps, outside the events; events around every layer call",
+                       "timing": "a GPU delay holds the stream while the host submits the L calls"},
+            "per_layer_us": mean_layer * 1e3,
+            "host_wall_ms_per_capture": statistics.mean(wall) * 1e3,
+            "roofline": {"bound": "hbm", "kernel": "capture_layer (one layer per launch)", "achieved": achieved,
+                         "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                         "algorithmic_bytes": layer_bytes, "traffic": None},
+            "clocks": clocks.summary()}
+
+
 # ----------------------------------------------------------------------------- oracle arm
 
 def oracle_step(wl, q: int, max_facts: int | None, kv_cache_fn):
@@ -616,6 +810,11 @@ def main(argv=None):
                     help="paged-cache type when it differs from the store's (e4m3: FP8, scales 1.0)")
     ap.add_argument("--retrieval", choices=["auto", "per_query", "batched"], default="auto",
                     help="similarity path: per-query kernel, tcgen05 batched contraction, or automatic")
+    ap.add_argument("--mode", choices=["step", "layerwise", "capture"], default="step",
+                    help="step: the fused retrieve+inject step (the headline); layerwise: one "
+                         "is_inject_layer call per layer; capture: Context-Window Encoding capture")
+    ap.add_argument("--capture-facts", type=int, default=256, help="facts per capture (--mode capture)")
+    ap.add_argument("--window", type=int, default=64, help="window tokens before each fact (--mode capture)")
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     args = ap.parse_args(argv)
@@ -633,6 +832,10 @@ def main(argv=None):
             dist.init_process_group("nccl")
     if args.impl == "reference":
         out = run_reference(args, rank, world)
+    elif args.mode == "layerwise":
+        out = run_layerwise(args, rank, world, local_rank)
+    elif args.mode == "capture":
+        out = run_capture(args, rank, world, local_rank)
     else:
         out = run_ours(args, rank, world, local_rank)
     if rank == 0 and out is not None:

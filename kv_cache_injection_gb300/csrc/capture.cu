@@ -14,25 +14,51 @@ namespace isk {
 
 constexpr int kCaptureThreads = 256;
 
-// One warp per fact token: its K row and V row of `layer`.
+// One warp per fact token: its K row and V row of `layer`.  The token's fact
+// is found by a 32-way search (each round the lanes probe 32 evenly spaced
+// facts and a ballot keeps the last one that starts at or before the token),
+// so a capture of n facts costs log32(n) rounds of loads, not log2(n).  Each
+// lane then loads up to kCapVecs vectors of the K row and of the V row before
+// storing any, so the loads of a row are in flight together.
+constexpr int kCapVecs = 4;
+
 __global__ void __launch_bounds__(kCaptureThreads) capture_layer_kernel(const CaptureArgs a) {
   const int64_t t = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;   // fact token
   const int lane = threadIdx.x & 31;
-  if (t >= a.tokens) return;
-  // The fact holding t: the last one whose first arena token is <= tok0 + t.
-  int lo = 0, hi = a.n;
+  if (t >= a.tokens) return;                   // whole warps: t is the same for all lanes
+  int lo = 0, hi = a.n;                        // fact lo starts at or before t; facts >= hi start after
   while (hi - lo > 1) {
-    const int mid = (lo + hi) >> 1;
-    if (a.seg[2 * mid + 1] - a.tok0 <= t) lo = mid; else hi = mid;
+    const int stride = (hi - lo + 31) >> 5;
+    const int idx = lo + lane * stride;
+    const bool le = idx < hi && a.seg[2 * idx + 1] - a.tok0 <= t;
+    const unsigned m = __ballot_sync(0xffffffffu, le);   // lane 0 probes lo, which qualifies
+    lo += (31 - __clz(m)) * stride;
+    hi = min(hi, lo + stride);
   }
   const int64_t src = a.seg[2 * lo] + (t - (a.seg[2 * lo + 1] - a.tok0));
   const uint8_t* ks = a.k + (size_t)src * a.row_bytes;
   const uint8_t* vs = a.v + (size_t)src * a.row_bytes;
   uint8_t* dk = a.kv + ((size_t)(a.tok0 + t) * a.L + a.layer) * 2 * (size_t)a.row_bytes;
   uint8_t* dv = dk + a.row_bytes;
-  for (int c = lane; c < a.row_bytes / 16; c += 32) {
-    st_v4(dk + (size_t)c * 16, *reinterpret_cast<const uint4*>(ks + (size_t)c * 16));
-    st_v4(dv + (size_t)c * 16, *reinterpret_cast<const uint4*>(vs + (size_t)c * 16));
+  const int nv = a.row_bytes >> 4;
+  for (int c0 = lane; c0 < nv; c0 += 32 * kCapVecs) {
+    uint4 kx[kCapVecs], vx[kCapVecs];
+#pragma unroll
+    for (int u = 0; u < kCapVecs; ++u) {
+      const int c = c0 + 32 * u;
+      if (c < nv) {
+        kx[u] = *reinterpret_cast<const uint4*>(ks + (size_t)c * 16);
+        vx[u] = *reinterpret_cast<const uint4*>(vs + (size_t)c * 16);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kCapVecs; ++u) {
+      const int c = c0 + 32 * u;
+      if (c < nv) {
+        st_v4(dk + (size_t)c * 16, kx[u]);
+        st_v4(dv + (size_t)c * 16, vx[u]);
+      }
+    }
   }
 }
 
