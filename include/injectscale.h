@@ -324,6 +324,27 @@ is_status_t is_retrieve_and_inject(is_store_t* store, int32_t Q, const int32_t* 
                                    int32_t* seg_len_out, int64_t* slot_mapping_out,
                                    cudaStream_t stream);
 
+/* ---- is_retrieve_and_inject_host --------------------------------------------
+ * is_retrieve_and_inject for a caller whose per-call inputs and outputs are in
+ * host memory (any host memory: the library stages them through its own
+ * page-locked buffer).  users (int32[Q]), q_emb ([Q][E] in emb_dtype),
+ * seg_start (int32[Q]) and block_table (int32[Q][max_blocks_per_seq]) are
+ * copied to the device in one transfer; the path runs on `stream`; ids_out
+ * (int64[Q][k]), scores_out (float[Q][k]) and seg_len_out (int32[Q]), host
+ * arrays that may each be NULL, come back in one transfer.  The store and the
+ * paged cache stay on the device (kv_cache is a device pointer).
+ * Synchronous: returns once the outputs are in host memory.  The staging
+ * buffers belong to the store; a call that needs more than the last one had
+ * grows them (a synchronisation and an allocation; IS_ERR_OOM if that fails).
+ * Errors as is_retrieve_and_inject, detected before anything is enqueued
+ * except device-side ones (read them with is_get_status). */
+is_status_t is_retrieve_and_inject_host(is_store_t* store, int32_t Q, const int32_t* users_host,
+                                        const void* q_emb_host, int32_t k, const int32_t* seg_start_host,
+                                        const is_rope_params_t* rope, const int32_t* block_table_host,
+                                        int32_t max_blocks_per_seq, const is_cache_desc_t* cache,
+                                        void* kv_cache, int64_t* ids_out_host, float* scores_out_host,
+                                        int32_t* seg_len_out_host, cudaStream_t stream);
+
 /* ---- is_inject_noalloc ------------------------------------------------------
  * The paper has no counterpart to this call; it exists for callers that
  * cannot allocate device memory: code whose device memory is all owned by

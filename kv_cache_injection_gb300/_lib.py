@@ -72,6 +72,9 @@ SIGNATURES = {
     "is_retrieve_and_inject": [c_void_p, c_int32, c_void_p, c_void_p, c_int32, c_void_p,
                                POINTER(RopeParams), c_void_p, c_int32, POINTER(CacheDesc),
                                c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p],
+    "is_retrieve_and_inject_host": [c_void_p, c_int32, c_void_p, c_void_p, c_int32, c_void_p,
+                                    POINTER(RopeParams), c_void_p, c_int32, POINTER(CacheDesc),
+                                    c_void_p, c_void_p, c_void_p, c_void_p, c_void_p],
     "is_inject_noalloc": [c_void_p, c_void_p, c_void_p, c_int64, c_int32, c_int32, c_int32,
                           c_int32, c_int32, c_int32, c_void_p, c_void_p, c_int32, c_void_p,
                           POINTER(RopeParams), c_void_p, c_int32, POINTER(CacheDesc), c_void_p,

@@ -206,6 +206,48 @@ def prepare_retrieve_and_inject(store: Store, users, q_emb, k: int, seg_start, r
     return call
 
 
+def _hptr(a) -> int | None:
+    """Address of a host array (numpy array or CPU tensor), which must be contiguous."""
+    if a is None:
+        return None
+    if hasattr(a, "data_ptr"):
+        if a.is_cuda or not a.is_contiguous():
+            raise ValueError("host tensor arguments must be contiguous CPU tensors")
+        return a.data_ptr()
+    if not a.flags["C_CONTIGUOUS"]:
+        raise ValueError("host array arguments must be C-contiguous")
+    return a.ctypes.data
+
+
+def prepare_retrieve_and_inject_host(store: Store, users, q_emb, k: int, seg_start, rope: RopeParams,
+                                     block_table, cache: CacheDesc, kv_cache, ids_out=None, scores_out=None,
+                                     seg_len_out=None, stream=None):
+    """is_retrieve_and_inject_host with every argument marshalled once: inputs
+    and outputs are host arrays (numpy or CPU tensors; contents may change
+    between calls), kv_cache a device tensor.  Returns a callable; each call is
+    synchronous and raises ISError on a non-OK status."""
+    fn = _lib.load().is_retrieve_and_inject_host
+    args = (c_void_p(store.handle), int(users.shape[0]), _hptr(users), _hptr(q_emb), int(k), _hptr(seg_start),
+            byref(rope), _hptr(block_table), int(block_table.shape[1]), byref(cache), _ptr(kv_cache),
+            _hptr(ids_out), _hptr(scores_out), _hptr(seg_len_out), _stream(stream))
+    keep = (rope, cache, users, q_emb, seg_start, block_table, ids_out, scores_out, seg_len_out)
+
+    def call():
+        st = fn(*args)
+        if st != _lib.IS_OK:
+            _check(st)
+        return keep is not None
+    return call
+
+
+def is_retrieve_and_inject_host(store: Store, users, q_emb, k: int, seg_start, rope: RopeParams, block_table,
+                                cache: CacheDesc, kv_cache, ids_out=None, scores_out=None, seg_len_out=None,
+                                stream=None) -> None:
+    """The fused call with host inputs and outputs (see the prepared form)."""
+    prepare_retrieve_and_inject_host(store, users, q_emb, k, seg_start, rope, block_table, cache, kv_cache,
+                                     ids_out, scores_out, seg_len_out, stream)()
+
+
 def is_inject_noalloc(kv_arena, fact_tok, fact_len, max_fact_len: int, num_layers: int,
                       num_kv_heads: int, head_dim: int, kv_dtype, fact_ids, n_ids, seg_start,
                       rope: RopeParams, block_table, cache: CacheDesc, kv_cache, status_out,

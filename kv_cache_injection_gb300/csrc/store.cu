@@ -143,6 +143,12 @@ struct is_store {
   int work_parity = 0;
   PendingFacts cap_pending;
 
+  // staging of is_retrieve_and_inject_host: one page-locked host buffer and
+  // one device buffer, inputs then outputs, grown on demand
+  uint8_t* stage_h = nullptr;
+  uint8_t* stage_d = nullptr;
+  size_t stage_bytes = 0;
+
   bool timing = false;
   std::vector<EventPair> pending[IS_NUM_STAGES];
   std::vector<cudaEvent_t> event_pool;
@@ -191,6 +197,9 @@ void free_store(is_store_t* s) {
     cudaFreeHost(s->kv);
     s->kv = nullptr;
   }
+  if (s->stage_h) cudaFreeHost(s->stage_h);
+  if (s->stage_d) cudaFree(s->stage_d);
+  s->stage_h = s->stage_d = nullptr;
   void* ptrs[] = {s->kv, s->fact_tok, s->fact_len, s->fact_user, s->emb, s->emb_inv_norm,
                   s->tile_fact, s->tile_len, s->user_meta, s->tile_tok, s->fact_src, s->user_tiles, s->scores,
                   s->ids_tmp, s->scores_tmp, s->fact_seg_off, s->n_ids, s->seg_len_tmp,
@@ -1056,6 +1065,71 @@ is_status_t is_retrieve_and_inject(is_store_t* s, int32_t Q, const int32_t* user
   return launch_injection(s, Q, ids, k, seg_len, seg_start, rope, block_table, max_blocks, cache,
                           kv_cache, slot_mapping_out, stream, 0, s->cfg.num_layers,
                           cache_layer_bytes(s, cache));
+}
+
+is_status_t is_retrieve_and_inject_host(is_store_t* s, int32_t Q, const int32_t* users, const void* q_emb,
+                                        int32_t k, const int32_t* seg_start, const is_rope_params_t* rope,
+                                        const int32_t* block_table, int32_t max_blocks,
+                                        const is_cache_desc_t* cache, void* kv_cache, int64_t* ids_out,
+                                        float* scores_out, int32_t* seg_len_out, cudaStream_t stream) {
+  if (!s) return fail(IS_ERR_INVALID_ARG, "NULL store");
+  if (Q < 1 || Q > s->cfg.max_queries)
+    return fail(IS_ERR_INVALID_ARG, "Q=%d outside [1, %d]", Q, s->cfg.max_queries);
+  if (k < 1 || k > s->cfg.max_k) return fail(IS_ERR_OUT_OF_RANGE, "k=%d outside [1, %d]", k, s->cfg.max_k);
+  if (!users || !q_emb || !seg_start || !block_table)
+    return fail(IS_ERR_INVALID_ARG, "users, q_emb, seg_start or block_table is NULL");
+  if (max_blocks < 1) return fail(IS_ERR_INVALID_ARG, "max_blocks_per_seq=%d must be >= 1", max_blocks);
+  auto up = [](size_t b) { return (b + 255) & ~(size_t)255; };
+  const size_t emb_elt = s->cfg.emb_dtype == IS_F16 ? 2 : 4;
+  const size_t b_users = up((size_t)Q * 4), b_q = up((size_t)Q * s->cfg.emb_dim * emb_elt);
+  const size_t b_start = up((size_t)Q * 4), b_bt = up((size_t)Q * max_blocks * 4);
+  const size_t b_ids = up((size_t)Q * k * 8), b_sc = up((size_t)Q * k * 4), b_len = up((size_t)Q * 4);
+  const size_t in_bytes = b_users + b_q + b_start + b_bt, out_bytes = b_ids + b_sc + b_len;
+  DeviceGuard g(s->device);
+  if (in_bytes + out_bytes > s->stage_bytes) {
+    CUDA_TRY(cudaStreamSynchronize(stream));
+    if (s->stage_h) cudaFreeHost(s->stage_h);
+    if (s->stage_d) cudaFree(s->stage_d);
+    s->stage_h = s->stage_d = nullptr;
+    s->stage_bytes = 0;
+    void* h = nullptr;
+    void* d = nullptr;
+    if (cudaHostAlloc(&h, in_bytes + out_bytes, cudaHostAllocPortable) != cudaSuccess) {
+      cudaGetLastError();
+      return fail(IS_ERR_OOM, "cudaHostAlloc(%zu bytes) for host staging failed", in_bytes + out_bytes);
+    }
+    if (cudaMalloc(&d, in_bytes + out_bytes) != cudaSuccess) {
+      cudaGetLastError();
+      cudaFreeHost(h);
+      return fail(IS_ERR_OOM, "cudaMalloc(%zu bytes) for device staging failed", in_bytes + out_bytes);
+    }
+    s->stage_h = static_cast<uint8_t*>(h);
+    s->stage_d = static_cast<uint8_t*>(d);
+    s->stage_bytes = in_bytes + out_bytes;
+  }
+  uint8_t* h = s->stage_h;
+  uint8_t* d = s->stage_d;
+  std::memcpy(h, users, (size_t)Q * 4);
+  std::memcpy(h + b_users, q_emb, (size_t)Q * s->cfg.emb_dim * emb_elt);
+  std::memcpy(h + b_users + b_q, seg_start, (size_t)Q * 4);
+  std::memcpy(h + b_users + b_q + b_start, block_table, (size_t)Q * max_blocks * 4);
+  CUDA_TRY(cudaMemcpyAsync(d, h, in_bytes, cudaMemcpyHostToDevice, stream));
+  uint8_t* dout = d + in_bytes;
+  is_status_t st = is_retrieve_and_inject(
+      s, Q, reinterpret_cast<const int32_t*>(d), d + b_users, k, reinterpret_cast<const int32_t*>(d + b_users + b_q),
+      rope, reinterpret_cast<const int32_t*>(d + b_users + b_q + b_start), max_blocks, cache, kv_cache,
+      reinterpret_cast<int64_t*>(dout), reinterpret_cast<float*>(dout + b_ids),
+      reinterpret_cast<int32_t*>(dout + b_ids + b_sc), nullptr, stream);
+  if (st != IS_OK) {
+    cudaStreamSynchronize(stream);              // the staged inputs stay in use until the copy ran
+    return st;
+  }
+  CUDA_TRY(cudaMemcpyAsync(h + in_bytes, dout, out_bytes, cudaMemcpyDeviceToHost, stream));
+  CUDA_TRY(cudaStreamSynchronize(stream));
+  if (ids_out) std::memcpy(ids_out, h + in_bytes, (size_t)Q * k * 8);
+  if (scores_out) std::memcpy(scores_out, h + in_bytes + b_ids, (size_t)Q * k * 4);
+  if (seg_len_out) std::memcpy(seg_len_out, h + in_bytes + b_ids + b_sc, (size_t)Q * 4);
+  return IS_OK;
 }
 
 is_status_t is_get_status(is_store_t* s, cudaStream_t stream, uint32_t* bits_out) {

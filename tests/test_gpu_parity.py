@@ -315,3 +315,41 @@ def test_chunk_pool_over_consecutive_launches(api, cache_dtype):
             gh.assert_only_slots_changed(caches[0], "e4m3", want)
     finally:
         store.destroy()
+
+
+def test_host_buffer_call_equals_device_call(api):
+    """is_retrieve_and_inject_host (host inputs and outputs, staged through the
+    library's page-locked buffer) gives the device call's ids, scores, segment
+    lengths and cache, on repeated calls and after its staging has grown."""
+    import torch
+    wl = workloads.generate(SMALL_BF16)
+    s = wl.spec
+    store = staging.load_store(wl, api)
+    try:
+        inp = staging.device_inputs(wl)
+        dev_cache = staging.canary_cache(wl)
+        out = gh.run_fused(api, store, wl, inp, dev_cache)
+        assert out["status"] == 0
+        rope = staging.rope_params(wl, api)
+        cd = api.make_cache_desc(s.block_size, wl.num_blocks, s.kv_dtype)
+        edt = np.float16 if s.emb_dtype == "f16" else np.float32
+        users = np.ascontiguousarray(wl.users, dtype=np.int32)
+        q = np.ascontiguousarray(wl.queries, dtype=edt)
+        start = np.ascontiguousarray(wl.seg_start, dtype=np.int32)
+        Q = len(users)
+        for k, bt in ((s.k, np.ascontiguousarray(wl.block_table, dtype=np.int32)),
+                      (s.k, np.ascontiguousarray(np.pad(wl.block_table, ((0, 0), (0, 64)))).astype(np.int32))):
+            host_cache = staging.canary_cache(wl)
+            ids = np.full((Q, k), -5, dtype=np.int64)
+            sc = np.zeros((Q, k), dtype=np.float32)
+            ln = np.full(Q, -5, dtype=np.int32)
+            api.is_retrieve_and_inject_host(store, users, q, k, start, rope, bt, cd, host_cache, ids, sc, ln)
+            assert np.array_equal(ids, out["ids"])
+            assert np.array_equal(sc.view(np.uint32), out["scores"].view(np.uint32))
+            assert np.array_equal(ln, out["seg_len"])
+            assert torch.equal(host_cache.view(torch.int16), dev_cache.view(torch.int16))
+        assert api.is_get_status(store) == 0
+        with pytest.raises(api.ISError):
+            api.is_retrieve_and_inject_host(store, users, q, 0, start, rope, bt, cd, host_cache)
+    finally:
+        store.destroy()
