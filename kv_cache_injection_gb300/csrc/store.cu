@@ -894,7 +894,7 @@ static is_status_t launch_injection(is_store_t* s, int32_t R, const int64_t* ids
                                     const is_rope_params_t* rope, const int32_t* block_table,
                                     int32_t max_blocks, const is_cache_desc_t* cache, void* kv_cache,
                                     int64_t* slot_mapping, cudaStream_t stream, int32_t layer0,
-                                    int32_t n_layers, int64_t layer_stride) {
+                                    int32_t n_layers, int64_t layer_stride, bool after_plan) {
   InjectArgs a{};
   a.kv = s->kv;
   a.fact_tok = s->fact_tok;
@@ -938,7 +938,12 @@ static is_status_t launch_injection(is_store_t* s, int32_t R, const int64_t* ids
     s->turns_valid = true;
   }
   const RopeTurns& rt = s->turns;
-  const LaunchCfg cfg{stream, s->num_sms, true};      // follows the planning kernel
+  // A programmatic dependent launch only right after this call's own planning
+  // (or retrieval) kernel: the inject kernel reads the caller's starts and
+  // block table before its dependency wait, which is safe only when the
+  // kernel before it does not write them.  A call that reuses an earlier plan
+  // follows whatever the caller queued, so it launches in plain stream order.
+  const LaunchCfg cfg{stream, s->num_sms, after_plan};
   StageTimer tm(s, IS_STAGE_INJECT, stream);
   CUDA_TRY(launch_inject(a, rt, s->cfg.kv_dtype, rope->style, s->cfg.kv_placement == IS_KV_HOST,
                          cache->dtype == IS_FP8_E4M3, cfg));
@@ -998,7 +1003,7 @@ is_status_t is_inject(is_store_t* s, int32_t R, const int64_t* fact_ids, const i
   s->plan_seg_len = seg_len;
   return launch_injection(s, R, fact_ids, ids_stride, seg_len, seg_start, rope, block_table, max_blocks,
                           cache, kv_cache, slot_mapping_out, stream, 0, s->cfg.num_layers,
-                          cache_layer_bytes(s, cache));
+                          cache_layer_bytes(s, cache), true);
 }
 
 is_status_t is_inject_layer(is_store_t* s, int32_t layer, int32_t R, const int64_t* fact_ids,
@@ -1038,7 +1043,7 @@ is_status_t is_inject_layer(is_store_t* s, int32_t layer, int32_t R, const int64
     seg_len = s->plan_seg_len;
   }
   return launch_injection(s, R, nullptr, 0, seg_len, seg_start, rope, block_table, max_blocks, cache,
-                          layer_cache, slot_mapping_out, stream, layer, 1, 0);
+                          layer_cache, slot_mapping_out, stream, layer, 1, 0, fact_ids != nullptr);
 }
 
 is_status_t is_retrieve_and_inject(is_store_t* s, int32_t Q, const int32_t* users, const void* q_emb,
@@ -1064,7 +1069,7 @@ is_status_t is_retrieve_and_inject(is_store_t* s, int32_t Q, const int32_t* user
   s->plan_seg_len = seg_len;
   return launch_injection(s, Q, ids, k, seg_len, seg_start, rope, block_table, max_blocks, cache,
                           kv_cache, slot_mapping_out, stream, 0, s->cfg.num_layers,
-                          cache_layer_bytes(s, cache));
+                          cache_layer_bytes(s, cache), true);
 }
 
 is_status_t is_retrieve_and_inject_host(is_store_t* s, int32_t Q, const int32_t* users, const void* q_emb,
