@@ -114,8 +114,10 @@ __device__ void topk_block(const TopkArgs& a, TopkShared& sh, uint32_t* s_keys, 
   // Read now, used at the very end: its latency hides under the selection.
   const int32_t start_q = (a.fact_seg_off && tid == 0) ? a.seg_start[q] : 0;
 
-  // The first batch of scores is requested before the histogram is cleared,
-  // so their latency overlaps the clearing and the barrier.
+  // Either path issues its score loads first: with bins counted by the
+  // similarity CTAs, all n scores and the thread's bins in one round; without,
+  // the first batch of scores before the shared histogram is cleared, so
+  // their latency overlaps the clearing and the barrier.
   constexpr int BPT = kCosBins / kRetThreads;
   const int hi = kCosBins - 1 - BPT * tid;     // this thread's bins: hi, hi - 1, .., hi - BPT + 1
   float v[kRegPer];
