@@ -387,6 +387,9 @@ def run_ours(args, rank, world, local_rank):
             "steps": args.steps,
             "warmup": args.warmup,
             "ms_per_step": total_ms / args.steps,
+            "step_ms_distribution": {"median": statistics.median(step_ms),
+                                     "p10": float(np.percentile(step_ms, 10)),
+                                     "p90": float(np.percentile(step_ms, 90))},
             "higher_is_better": True,
             "scaling": "weak",
             "vs_baseline": None,
