@@ -333,7 +333,8 @@ is_status_t is_retrieve_and_inject(is_store_t* store, int32_t Q, const int32_t* 
  * (int64[Q][k]), scores_out (float[Q][k]) and seg_len_out (int32[Q]), host
  * arrays that may each be NULL, come back in one transfer.  The store and the
  * paged cache stay on the device (kv_cache is a device pointer).
- * Synchronous: returns once the outputs are in host memory.  The staging
+ * Synchronous: returns once the outputs are in host memory, waiting by
+ * polling the stream (the calling thread spins meanwhile).  The staging
  * buffers belong to the store; a call that needs more than the last one had
  * grows them (a synchronisation and an allocation; IS_ERR_OOM if that fails).
  * Errors as is_retrieve_and_inject, detected before anything is enqueued
