@@ -680,6 +680,31 @@ void prefer_max_shared(const void* kern) {
   }
 }
 
+cudaError_t ensure_dynamic_smem(const void* kern, size_t bytes) {
+  static std::mutex mu;
+  static const void* kern_set[64];
+  static int dev_set[64];
+  static size_t bytes_set[64];
+  static int n_set = 0;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  int slot = -1;
+  for (int i = 0; i < n_set; ++i)
+    if (kern_set[i] == kern && dev_set[i] == dev) slot = i;
+  if (slot >= 0 && bytes_set[slot] >= bytes) return cudaSuccess;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e != cudaSuccess) return e;
+  if (slot < 0 && n_set < 64) slot = n_set++;
+  if (slot >= 0) {
+    kern_set[slot] = kern;
+    dev_set[slot] = dev;
+    bytes_set[slot] = bytes;
+  }
+  return cudaSuccess;
+}
+
 // Shared memory plan of one inject launch: warps per CTA, stages per warp and
 // layers per work item.
 struct InjectShape {
@@ -858,6 +883,7 @@ std::mutex g_na_mu;
 
 is_status_t na_fail(is_status_t st, const char* msg) {
   isk::set_last_error_message(msg);
+  if (st == IS_ERR_CUDA) cudaGetLastError();   // a failed launch is reported here, not by a later call
   return st;
 }
 

@@ -19,6 +19,11 @@ struct LaunchCfg {
 // memory carve-out, so consecutive kernels do not reconfigure L1/shared.
 void prefer_max_shared(const void* kern);   // once per (kernel, device)
 
+// Raises a kernel's dynamic shared-memory limit on the current device to at
+// least `bytes` (the default stops at 48 KB minus the kernel's static shared
+// memory); remembered per kernel and device.
+cudaError_t ensure_dynamic_smem(const void* kern, size_t bytes);
+
 template <typename... KArgs, typename... Args>
 cudaError_t launch_ex(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
                       bool pdl, Args... args) {

@@ -175,6 +175,8 @@ static cudaError_t launch_retrieve_t(const SimArgs& sa, const TopkArgs& ta, int 
                                      int64_t max_user_facts, int32_t* arrive, const LaunchCfg& cfg) {
   if (max_user_facts <= kSmemKeysMax) {
     const size_t smem = (size_t)std::max<int64_t>(max_user_facts, 1) * sizeof(uint32_t);
+    const cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(retrieve_kernel<E, true>), smem);
+    if (e != cudaSuccess) return e;
     return launch_ex(retrieve_kernel<E, true>, grid, dim3(kRetThreads), smem, cfg.stream, cfg.pdl, sa,
                      ta, n_sub, arrive);
   }

@@ -410,6 +410,8 @@ cudaError_t launch_topk_batched(const TopkArgs& ta, int Q, int32_t max_users, in
                                 const LaunchCfg& cfg) {
   if (max_user_facts <= kSmemKeysMax) {
     const size_t ks = (size_t)std::max<int64_t>(max_user_facts, 1) * sizeof(uint32_t);
+    const cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(topk_kernel<true>), ks);
+    if (e != cudaSuccess) return e;
     return launch_ex(topk_kernel<true>, dim3(Q), dim3(kRetThreads), ks, cfg.stream, cfg.pdl, ta, max_users);
   }
   return launch_ex(topk_kernel<false>, dim3(Q), dim3(kRetThreads), 0, cfg.stream, cfg.pdl, ta, max_users);

@@ -27,11 +27,15 @@ is_status_t fail(is_status_t s, const char* fmt, ...) {
   return s;
 }
 
+// On failure the runtime's pending error is read and cleared too, so that a
+// failed launch is reported by this call and not again by a later one.
 #define CUDA_TRY(expr)                                                                  \
   do {                                                                                  \
     cudaError_t e_ = (expr);                                                            \
-    if (e_ != cudaSuccess)                                                              \
+    if (e_ != cudaSuccess) {                                                            \
+      cudaGetLastError();                                                               \
       return fail(IS_ERR_CUDA, "%s failed: %s", #expr, cudaGetErrorString(e_));         \
+    }                                                                                   \
   } while (0)
 
 int dtype_bytes(int dt) { return dt == IS_F32 ? 4 : 2; }

@@ -353,3 +353,30 @@ def test_host_buffer_call_equals_device_call(api):
             api.is_retrieve_and_inject_host(store, users, q, 0, start, rope, bt, cd, host_cache)
     finally:
         store.destroy()
+
+
+@pytest.mark.parametrize("n", [4096, 4097, 6000])
+def test_per_query_topk_on_large_users(api, n):
+    """The per-query retrieval kernel on users of 4096 facts (keys staged in
+    shared memory) and more (keys read back from global memory), with the
+    tensor-core path switched off, against the oracle for several k."""
+    import torch
+    from kv_cache_injection_gb300 import _lib
+    spec = SMALL_BF16.with_(num_layers=1, n_users=2, facts_per_user=n, n_queries=2, k=50,
+                            seed=90 + n % 7, length_dist=("uniform", 1, 2), tokens_cap=300 * 2)
+    wl = workloads.generate(spec)
+    store = staging.load_store(wl, api, max_k=300)
+    try:
+        api.is_set_retrieval_mode(store, _lib.IS_RETRIEVAL_PER_QUERY)
+        inp = staging.device_inputs(wl)
+        for k in (1, 50, 300):
+            ids = torch.empty((2, k), dtype=torch.int64, device="cuda")
+            sc = torch.empty((2, k), dtype=torch.float32, device="cuda")
+            api.is_retrieve_topk(store, inp["users"], inp["q_emb"], k, ids, sc)
+            g, gs = ids.cpu().numpy(), sc.cpu().numpy()
+            for q in range(2):
+                o_ids, o_sc, score_of = parity.oracle_retrieve(wl, q, k)
+                parity.check_topk(g[q], gs[q], o_ids, o_sc, score_of, k)
+        assert api.is_get_status(store) == 0
+    finally:
+        store.destroy()
