@@ -78,7 +78,7 @@ def build(verbose: bool = False, force: bool = False, extra_flags: list[str] | N
         for f in futs:
             f.result()
     if jobs or _stale(LIB, objs):
-        _run([nv] + ARCH + ["-shared", "-o", LIB] + objs, verbose)
+        _run([nv] + ARCH + ["-shared", "-Xlinker", "--no-undefined", "-o", LIB] + objs, verbose)
     return LIB
 
 

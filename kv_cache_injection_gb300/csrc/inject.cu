@@ -661,50 +661,6 @@ cudaError_t launch_plan(const PlanArgs& a, const LaunchCfg& cfg) {
   return launch_ex(plan_kernel, dim3(a.R), dim3(256), 0, cfg.stream, cfg.pdl, a);
 }
 
-void prefer_max_shared(const void* kern) {
-  static std::mutex mu;
-  static const void* done_kern[64];
-  static int done_dev[64];
-  static int n_done = 0;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return;
-  std::lock_guard<std::mutex> lock(mu);
-  for (int i = 0; i < n_done; ++i)
-    if (done_kern[i] == kern && done_dev[i] == dev) return;
-  cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
-                       (int)cudaSharedmemCarveoutMaxShared);
-  if (n_done < 64) {
-    done_kern[n_done] = kern;
-    done_dev[n_done] = dev;
-    ++n_done;
-  }
-}
-
-cudaError_t ensure_dynamic_smem(const void* kern, size_t bytes) {
-  static std::mutex mu;
-  static const void* kern_set[64];
-  static int dev_set[64];
-  static size_t bytes_set[64];
-  static int n_set = 0;
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  std::lock_guard<std::mutex> lock(mu);
-  int slot = -1;
-  for (int i = 0; i < n_set; ++i)
-    if (kern_set[i] == kern && dev_set[i] == dev) slot = i;
-  if (slot >= 0 && bytes_set[slot] >= bytes) return cudaSuccess;
-  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
-  if (e != cudaSuccess) return e;
-  if (slot < 0 && n_set < 64) slot = n_set++;
-  if (slot >= 0) {
-    kern_set[slot] = kern;
-    dev_set[slot] = dev;
-    bytes_set[slot] = bytes;
-  }
-  return cudaSuccess;
-}
-
 // Shared memory plan of one inject launch: warps per CTA, stages per warp and
 // layers per work item.
 struct InjectShape {
