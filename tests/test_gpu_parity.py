@@ -380,3 +380,39 @@ def test_per_query_topk_on_large_users(api, n):
         assert api.is_get_status(store) == 0
     finally:
         store.destroy()
+
+
+def test_prepared_device_call_equals_direct_call(api, tiny):
+    """api.prepare_retrieve_and_inject marshals once and reissues the call on
+    the same buffers; after the inputs change in place, it must give what a
+    direct call gives on the new inputs."""
+    import torch
+    wl, store = tiny
+    s = wl.spec
+    inp = staging.device_inputs(wl)
+    Q, k = s.n_queries, s.k
+    rope = staging.rope_params(wl, api)
+    cd = api.make_cache_desc(s.block_size, wl.num_blocks, s.kv_dtype)
+    outs = []
+    for prepared in (True, False):
+        cache = staging.canary_cache(wl)
+        ids = torch.empty((Q, k), dtype=torch.int64, device="cuda")
+        sc = torch.empty((Q, k), dtype=torch.float32, device="cuda")
+        ln = torch.empty(Q, dtype=torch.int32, device="cuda")
+        start = inp["seg_start"].clone()
+        if prepared:
+            call = api.prepare_retrieve_and_inject(store, inp["users"], inp["q_emb"], k, start, rope,
+                                                   inp["block_table"], cd, cache, ids, sc, ln)
+            call()
+            start.add_(3)                              # new starts, same buffer
+            staging.refill_canary(cache, s.kv_dtype)
+            call()
+        else:
+            start.add_(3)
+            api.is_retrieve_and_inject(store, inp["users"], inp["q_emb"], k, start, rope, inp["block_table"],
+                                       cd, cache, ids, sc, ln)
+        torch.cuda.synchronize()
+        outs.append((ids.cpu(), ln.cpu(), cache.view(torch.int32).cpu()))
+    assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
+    assert torch.equal(outs[0][2], outs[1][2])
+    assert api.is_get_status(store) == 0
