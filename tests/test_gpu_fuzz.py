@@ -233,3 +233,54 @@ def test_random_capture_equals_add_facts(api, i):
     finally:
         a.destroy()
         b.destroy()
+
+
+def _topk_case(i):
+    rng = np.random.default_rng(5000 + i)
+    n_users = int(rng.integers(1, 4))
+    n = int(rng.choice([int(rng.integers(1, 300)), int(rng.integers(1500, 2600)), int(rng.integers(3900, 6200))]))
+    k = int(rng.choice([1, 5, 50, 64, 65, 200, 257, 1024]))
+    n_q = int(rng.integers(1, 9))
+    spec = workloads.WorkloadSpec(
+        name=f"fuzz_topk{i}", num_layers=1, num_kv_heads=4, head_dim=64, kv_dtype="bf16",
+        rope=workloads.RopeSpec(theta=1e4), n_users=n_users, facts_per_user=n,
+        length_dist=("uniform", 1, 2), emb_dim=int(rng.choice([64, 128, 1024])), emb_dtype="f16",
+        n_queries=n_q, k=min(k, 1024), query_kind="planted", start=("uniform", 0, 50), block_size=16,
+        tokens_cap=64, block_layout="free_list", queries_share_user=True, seed=6000 + i)
+    dup = int(rng.choice([0, 0, 3, 40]))        # embeddings drawn from this many distinct rows (0: all distinct)
+    return spec, rng, dup
+
+
+@pytest.mark.parametrize("i", range(24))
+def test_random_topk(api, i):
+    """Retrieval alone on random user sizes either side of the kernels' internal
+    limits (2048 rows for bins counted by the similarity CTAs, 4096 for keys
+    staged in shared memory), k across the rank (<= 256 candidates), bitonic and
+    radix-select paths, several queries and, in some draws, many exact ties
+    (embeddings repeated).  Per-query path, every top-k against the oracle."""
+    import torch
+    from kv_cache_injection_gb300 import _lib
+    spec, rng, dup = _topk_case(i)
+    wl = workloads.generate(spec)
+    wl.users[:] = rng.integers(0, spec.n_users, size=spec.n_queries).astype(np.int32)
+    dup = min(dup, len(wl.emb))
+    if dup:
+        base = wl.emb[:dup].copy()
+        wl.emb[:] = base[rng.integers(0, dup, size=len(wl.emb))]
+        wl.queries[:] = base[rng.integers(0, dup, size=len(wl.queries))]
+    store = staging.load_store(wl, api, max_k=1024)
+    try:
+        api.is_set_retrieval_mode(store, _lib.IS_RETRIEVAL_PER_QUERY)
+        inp = staging.device_inputs(wl)
+        k = spec.k
+        for rep in range(2):                    # twice: the bins must be left zeroed
+            ids = torch.empty((spec.n_queries, k), dtype=torch.int64, device="cuda")
+            sc = torch.empty((spec.n_queries, k), dtype=torch.float32, device="cuda")
+            api.is_retrieve_topk(store, inp["users"], inp["q_emb"], k, ids, sc)
+            g, gs = ids.cpu().numpy(), sc.cpu().numpy()
+            for q in range(spec.n_queries):
+                o_ids, o_sc, score_of = parity.oracle_retrieve(wl, q, k)
+                parity.check_topk(g[q], gs[q], o_ids, o_sc, score_of, k)
+        assert api.is_get_status(store) == 0
+    finally:
+        store.destroy()
