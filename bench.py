@@ -89,16 +89,19 @@ def inject_source_hash() -> str:
         return hashlib.sha256(f.read()).hexdigest()[:16]
 
 
-def ncu_traffic_per_token():
-    """DRAM bytes per injected token from the committed ncu summary, if it was
-    taken on the current inject kernel source."""
+def ncu_traffic_per_token_layer(key: str):
+    """DRAM bytes per injected token and layer from the committed ncu summary
+    for this workload, cache type and placement (key "workload/cache
+    dtype/placement"), if it was taken on the current inject kernel source;
+    else None."""
     if not os.path.exists(TRAFFIC_FILE):
         return None
     with open(TRAFFIC_FILE) as f:
         d = json.load(f)
     if d.get("inject_cu_sha256_16") != inject_source_hash():
         return None
-    return float(d["dram_bytes_per_token"])
+    c = d.get("captures", {}).get(key)
+    return float(c["dram_bytes_per_token_layer"]) if c else None
 
 
 class L2Flush:
@@ -339,7 +342,7 @@ def run_ours(args, rank, world, local_rank):
         inject_bytes = (per_tok + per_tok_w) * tokens_per_step  # read + write per launch
         inject_ms = stage_ms["inject"] / max(1, stage_n["inject"])
         achieved = inject_bytes / (inject_ms * 1e-3) / 1e9
-        traffic_tok = ncu_traffic_per_token()
+        traffic_tl = ncu_traffic_per_token_layer(f"{s.name}/{cache_dtype}/{args.kv_placement}")
         emb_bytes = 0
         for u in np.unique(wl.users):
             emb_bytes += int((wl.fact_user == u).sum()) * s.emb_dim * (2 if s.emb_dtype == "f16" else 4)
@@ -372,7 +375,7 @@ def run_ours(args, rank, world, local_rank):
                 "unit": "GB/s",
                 "frac": achieved / peaks["hbm_gbs"],
                 "frac_of_nominal_8tbs": achieved / 8000.0,
-                "traffic": (traffic_tok * tokens_per_step) if traffic_tok and cache_dtype == s.kv_dtype else None,
+                "traffic": (traffic_tl * tokens_per_step * s.num_layers) if traffic_tl else None,
                 "algorithmic_bytes": inject_bytes,
                 "avg_launch_ms": inject_ms,
             }
