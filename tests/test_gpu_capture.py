@@ -14,6 +14,7 @@ import pytest
 from oracle import cwe, model, numerics
 from oracle import inject as oinject
 from oracle import rope
+from synth import staging
 from tests import gpu_helpers as gh
 from tests import parity
 
@@ -202,3 +203,61 @@ def test_capture_protocol_errors(api):
         assert api.is_store_info(store)["n_facts"] == n
     finally:
         store.destroy()
+
+
+def test_large_capture_equals_add_facts():
+    """A capture of 2000 facts (the fact search takes three 32-way rounds) with
+    random windows stores exactly the fact rows: injecting all 2000 facts from
+    it and from a store built by is_store_add_facts of the same rows gives the
+    same cache byte for byte."""
+    import torch
+    gh.ensure_built()
+    from kv_cache_injection_gb300 import api
+    rng = np.random.default_rng(77)
+    L, H, D, dt = 2, 4, 64, "bf16"
+    tdt = staging.torch_dtype(dt)
+    n = 2000
+    lengths = rng.integers(1, 9, size=n).astype(np.int32)
+    windows = rng.integers(0, 21, size=n).astype(np.int32)
+    total = int((lengths + windows).sum())
+    gen = torch.Generator(device="cuda").manual_seed(5)
+    layers = [(torch.randn(total, H, D, device="cuda", generator=gen).to(tdt),
+               torch.randn(total, H, D, device="cuda", generator=gen).to(tdt)) for _ in range(L)]
+    emb = torch.nn.functional.normalize(torch.randn(n, 64, device="cuda", generator=gen), dim=1).half()
+
+    def store():
+        cfg = api.make_config(num_layers=L, num_kv_heads=H, head_dim=D, emb_dim=64, kv_dtype=dt,
+                              emb_dtype="f16", max_facts=n, max_tokens=int(lengths.sum()), max_users=1,
+                              max_queries=1, max_k=n // 2, max_requests=2)
+        return api.is_store_create(cfg, 0)
+    a, b = store(), store()
+    try:
+        api.is_store_capture_begin(a, 0, windows, lengths, emb)
+        for l in range(L):
+            api.is_store_capture_layer(a, l, layers[l][0], layers[l][1])
+        assert np.array_equal(api.is_store_capture_end(a, n), np.arange(n))
+        starts = np.cumsum(np.concatenate([[0], lengths + windows]))[:-1] + windows
+        idx = torch.from_numpy(np.concatenate([np.arange(st, st + ln) for st, ln in zip(starts, lengths)])).cuda()
+        k = torch.stack([layers[l][0].index_select(0, idx) for l in range(L)], 1).contiguous()
+        v = torch.stack([layers[l][1].index_select(0, idx) for l in range(L)], 1).contiguous()
+        api.is_store_add_facts(b, 0, lengths, k, v, emb)
+        bs = 16
+        order = rng.permutation(n).astype(np.int64).reshape(2, n // 2)
+        seg = [int(lengths[order[r]].sum()) for r in range(2)]
+        nbr = max(seg) // bs + 2
+        nb = 2 * nbr
+        bt = torch.arange(nb, dtype=torch.int32, device="cuda").reshape(2, nbr).flip(1).contiguous()
+        rope = api.make_rope(1e4, 0)
+        cd = api.make_cache_desc(bs, nb, dt)
+        outs = []
+        for st in (a, b):
+            cache = torch.zeros((L, 2, nb, bs, H, D), dtype=tdt, device="cuda")
+            api.is_inject(st, torch.from_numpy(order).cuda(), torch.full((2,), n // 2, dtype=torch.int32, device="cuda"),
+                          torch.zeros(2, dtype=torch.int32, device="cuda"), rope, bt, cd, cache)
+            assert api.is_get_status(st) == 0
+            outs.append(cache)
+        assert torch.equal(outs[0].view(torch.uint8), outs[1].view(torch.uint8))
+        assert bool(outs[0].view(torch.int16).ne(0).any())
+    finally:
+        a.destroy()
+        b.destroy()
