@@ -55,6 +55,7 @@ extern "C" {
 #define IS_MAX_POSITION   (1 << 24)  /* positions must stay below 2^24 */
 #define IS_EMB_TILE       128    /* embedding rows per store tile (one user per tile) */
 #define IS_MAX_FACTS_PER_USER (1 << 20)  /* facts of one user (retrieval row index width) */
+#define IS_MAX_LAYERS_PER_CALL 128  /* per-layer cache tensors one is_inject_layers call writes */
 
 typedef enum {
   IS_OK = 0,
@@ -309,6 +310,24 @@ is_status_t is_inject_layer(is_store_t* store, int32_t layer, int32_t R, const i
                             const int32_t* block_table, int32_t max_blocks_per_seq,
                             const is_cache_desc_t* cache, void* layer_cache, int32_t* seg_len_out,
                             int64_t* slot_mapping_out, cudaStream_t stream);
+
+/* ---- is_inject_layers -------------------------------------------------------
+ * is_inject_layer for the layers layer0 .. layer0 + n_layers - 1 in one launch,
+ * each into its own cache tensor: layer_caches is a host array of n_layers
+ * device pointers, entry i being layer (layer0 + i)'s
+ * [2][num_blocks][block_size][H][D] tensor, at any addresses (16-byte
+ * aligned).  This is how an engine that keeps one KV tensor per layer (vLLM)
+ * injects a group of layers, or the whole model (layer0 = 0, n_layers = L),
+ * at the cost of one launch.  1 <= n_layers <= IS_MAX_LAYERS_PER_CALL and
+ * layer0 + n_layers <= the store's layers (IS_ERR_OUT_OF_RANGE otherwise).
+ * Planning (fact_ids != NULL) and plan reuse (fact_ids == NULL), the other
+ * arguments and the errors are as is_inject_layer. */
+is_status_t is_inject_layers(is_store_t* store, int32_t layer0, int32_t n_layers, int32_t R,
+                             const int64_t* fact_ids, const int32_t* n_ids, int32_t ids_stride,
+                             const int32_t* users, const int32_t* seg_start, const is_rope_params_t* rope,
+                             const int32_t* block_table, int32_t max_blocks_per_seq,
+                             const is_cache_desc_t* cache, void* const* layer_caches, int32_t* seg_len_out,
+                             int64_t* slot_mapping_out, cudaStream_t stream);
 
 /* ---- is_retrieve_and_inject -------------------------------------------------
  * is_retrieve_topk followed by is_inject of each query's k facts in

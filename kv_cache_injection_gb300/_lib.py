@@ -19,6 +19,7 @@ IS_STAGE_SIMILARITY, IS_STAGE_TOPK, IS_STAGE_PLAN, IS_STAGE_INJECT = 0, 1, 2, 3
 IS_MAX_K, IS_MAX_QUERIES, IS_MAX_REQUESTS, IS_EMB_TILE = 1024, 1024, 4096, 128
 IS_NOALLOC_MAX_REQUESTS, IS_NOALLOC_MAX_FACTS = 256, 256
 IS_MAX_CAPTURE_FACTS = 65536
+IS_MAX_LAYERS_PER_CALL = 128
 IS_RETRIEVAL_AUTO, IS_RETRIEVAL_PER_QUERY, IS_RETRIEVAL_BATCHED = 0, 1, 2
 IS_KV_DEVICE, IS_KV_HOST = 0, 1
 
@@ -69,6 +70,9 @@ SIGNATURES = {
     "is_inject_layer": [c_void_p, c_int32, c_int32, c_void_p, c_void_p, c_int32, c_void_p, c_void_p,
                         POINTER(RopeParams), c_void_p, c_int32, POINTER(CacheDesc), c_void_p,
                         c_void_p, c_void_p, c_void_p],
+    "is_inject_layers": [c_void_p, c_int32, c_int32, c_int32, c_void_p, c_void_p, c_int32, c_void_p,
+                         c_void_p, POINTER(RopeParams), c_void_p, c_int32, POINTER(CacheDesc), c_void_p,
+                         c_void_p, c_void_p, c_void_p],
     "is_retrieve_and_inject": [c_void_p, c_int32, c_void_p, c_void_p, c_int32, c_void_p,
                                POINTER(RopeParams), c_void_p, c_int32, POINTER(CacheDesc),
                                c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p],

@@ -175,6 +175,20 @@ def is_inject_layer(store: Store, layer: int, R: int, seg_start, rope: RopeParam
         _ptr(layer_cache), _ptr(seg_len_out), _ptr(slot_mapping_out), _stream(stream)))
 
 
+def is_inject_layers(store: Store, layer0: int, R: int, seg_start, rope: RopeParams, block_table,
+                     cache: CacheDesc, layer_caches, fact_ids=None, n_ids=None, users=None,
+                     seg_len_out=None, slot_mapping_out=None, stream=None) -> None:
+    """Layers layer0 .. layer0 + len(layer_caches) - 1 in one launch, each into its
+    own cache tensor (a list of device tensors); fact_ids=None reuses the last plan."""
+    n = len(layer_caches)
+    ptrs = (c_void_p * max(n, 1))(*[_ptr(t) for t in layer_caches])
+    stride = int(fact_ids.shape[1]) if fact_ids is not None else 0
+    _check(_lib.load().is_inject_layers(
+        c_void_p(store.handle), int(layer0), n, int(R), _ptr(fact_ids), _ptr(n_ids), stride, _ptr(users),
+        _ptr(seg_start), byref(rope), _ptr(block_table), int(block_table.shape[1]), byref(cache),
+        ctypes.cast(ptrs, c_void_p), _ptr(seg_len_out), _ptr(slot_mapping_out), _stream(stream)))
+
+
 def is_retrieve_and_inject(store: Store, users, q_emb, k: int, seg_start, rope: RopeParams,
                            block_table, cache: CacheDesc, kv_cache, ids_out=None, scores_out=None,
                            seg_len_out=None, slot_mapping_out=None, stream=None) -> None:

@@ -58,6 +58,8 @@ struct InjectArgs {
   uint32_t* work_ctr;           // kPoolCtrs counters of pool claims in this launch (zero at its start)
   uint32_t* work_ctr_next;      // the counters of the next launch, zeroed by this one
   int32_t chunk_items;          // items per pool chunk (set by the launcher)
+  int32_t per_layer;            // 1: layer l of this call is written to layer_cache[l]
+  uint8_t* layer_cache[IS_MAX_LAYERS_PER_CALL];   // per_layer: each layer's own [2][nb][bs][H][D]
 };
 
 // One layer of a Context-Window Encoding capture (is_store_capture_layer).

@@ -207,6 +207,12 @@ __device__ __forceinline__ void prefetch_block_rows(const InjectArgs& a, int lan
   }
 }
 
+// K block of layer l (counted from the call's first layer) in the
+// destination: its own tensor, or l layer strides into one cache.
+__device__ __forceinline__ uint8_t* layer_base(const InjectArgs& a, int l) {
+  return a.per_layer ? a.layer_cache[l] : a.cache + (size_t)l * a.layer_stride;
+}
+
 // Warp-uniform walk from a composed-segment token t (all requests back to
 // back) to its store token, serving position and destination slot.  Tokens a
 // warp visits are consecutive, so the request, fact and block-table entry found
@@ -509,7 +515,7 @@ __global__ void __launch_bounds__(kInjectWarpsMax * 32) inject_kernel(const Inje
       }
       for (int gl = 0; gl < m.nl; ++gl) {
         const uint32_t kst = stage0 + (uint32_t)s * item_bytes + (uint32_t)gl * 2u * (uint32_t)a.row_bytes;
-        uint8_t* dk = a.cache + (size_t)(m.l + gl) * a.layer_stride + (size_t)m.slot * a.cache_row_bytes;
+        uint8_t* dk = layer_base(a, m.l + gl) + (size_t)m.slot * a.cache_row_bytes;
         uint8_t* dv = dk + (size_t)a.num_blocks * a.block_size * a.cache_row_bytes;
         if (!F8 && lane == 0) bulk_store(dv, kst + a.row_bytes, a.row_bytes);
         for (int c = 0; c < vpl; ++c) {
@@ -623,7 +629,7 @@ __global__ void __launch_bounds__(kHostWarps * 32) inject_host_kernel(const Inje
       }
     }
     const uint8_t* src = a.kv + ((size_t)cur.src * a.L + a.layer0 + l) * 2 * (size_t)a.row_bytes;
-    uint8_t* dk = a.cache + (size_t)l * a.layer_stride + (size_t)cur.slot * a.cache_row_bytes;
+    uint8_t* dk = layer_base(a, l) + (size_t)cur.slot * a.cache_row_bytes;
     uint8_t* dv = dk + plane;
     for (int c0 = 0; c0 < vpl; c0 += kHostChunk) {
       uint4 kx[kHostChunk], vx[kHostChunk];

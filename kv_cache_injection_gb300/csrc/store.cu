@@ -948,7 +948,8 @@ static is_status_t launch_injection(is_store_t* s, int32_t R, const int64_t* ids
                                     const is_rope_params_t* rope, const int32_t* block_table,
                                     int32_t max_blocks, const is_cache_desc_t* cache, void* kv_cache,
                                     int64_t* slot_mapping, cudaStream_t stream, int32_t layer0,
-                                    int32_t n_layers, int64_t layer_stride, bool after_plan) {
+                                    int32_t n_layers, int64_t layer_stride, bool after_plan,
+                                    void* const* layer_caches = nullptr) {
   InjectArgs a{};
   a.kv = s->kv;
   a.fact_tok = s->fact_tok;
@@ -966,6 +967,10 @@ static is_status_t launch_injection(is_store_t* s, int32_t R, const int64_t* ids
   a.block_table = block_table;
   a.max_blocks = max_blocks;
   a.cache = static_cast<uint8_t*>(kv_cache);
+  if (layer_caches) {
+    a.per_layer = 1;
+    for (int i = 0; i < n_layers; ++i) a.layer_cache[i] = static_cast<uint8_t*>(layer_caches[i]);
+  }
   a.block_size = cache->block_size;
   a.num_blocks = cache->num_blocks;
   a.slot_mapping = slot_mapping;
@@ -1060,21 +1065,27 @@ is_status_t is_inject(is_store_t* s, int32_t R, const int64_t* fact_ids, const i
                           cache_layer_bytes(s, cache), true);
 }
 
-is_status_t is_inject_layer(is_store_t* s, int32_t layer, int32_t R, const int64_t* fact_ids,
-                            const int32_t* n_ids, int32_t ids_stride, const int32_t* users,
-                            const int32_t* seg_start, const is_rope_params_t* rope,
-                            const int32_t* block_table, int32_t max_blocks, const is_cache_desc_t* cache,
-                            void* layer_cache, int32_t* seg_len_out, int64_t* slot_mapping_out,
-                            cudaStream_t stream) {
+is_status_t is_inject_layers(is_store_t* s, int32_t layer0, int32_t n_layers, int32_t R,
+                             const int64_t* fact_ids, const int32_t* n_ids, int32_t ids_stride,
+                             const int32_t* users, const int32_t* seg_start, const is_rope_params_t* rope,
+                             const int32_t* block_table, int32_t max_blocks, const is_cache_desc_t* cache,
+                             void* const* layer_caches, int32_t* seg_len_out, int64_t* slot_mapping_out,
+                             cudaStream_t stream) {
   if (!s) return fail(IS_ERR_INVALID_ARG, "NULL store");
-  if (layer < 0 || layer >= s->cfg.num_layers)
-    return fail(IS_ERR_OUT_OF_RANGE, "layer %d outside [0, %d)", layer, s->cfg.num_layers);
+  if (n_layers < 1 || n_layers > IS_MAX_LAYERS_PER_CALL)
+    return fail(IS_ERR_OUT_OF_RANGE, "n_layers=%d outside [1, %d]", n_layers, IS_MAX_LAYERS_PER_CALL);
+  if (layer0 < 0 || (int64_t)layer0 + n_layers > s->cfg.num_layers)
+    return fail(IS_ERR_OUT_OF_RANGE, "layers [%d, %lld) outside [0, %d)", layer0,
+                (long long)layer0 + n_layers, s->cfg.num_layers);
   if (R < 1 || R > s->cfg.max_requests)
     return fail(IS_ERR_INVALID_ARG, "R=%d outside [1, %d]", R, s->cfg.max_requests);
+  if (!layer_caches) return fail(IS_ERR_INVALID_ARG, "layer_caches is NULL");
   const int32_t stride_for_bound = fact_ids ? ids_stride : s->cfg.max_k;
-  is_status_t st = check_inject_common(s, R, seg_start, rope, block_table, max_blocks, cache, layer_cache,
+  is_status_t st = check_inject_common(s, R, seg_start, rope, block_table, max_blocks, cache, layer_caches[0],
                                        stride_for_bound);
   if (st != IS_OK) return st;
+  for (int i = 1; i < n_layers; ++i)
+    if ((st = check_cache(s, cache, layer_caches[i])) != IS_OK) return st;
   DeviceGuard g(s->device);
   const int32_t* seg_len = nullptr;
   if (fact_ids) {
@@ -1097,7 +1108,21 @@ is_status_t is_inject_layer(is_store_t* s, int32_t layer, int32_t R, const int64
     seg_len = s->plan_seg_len;
   }
   return launch_injection(s, R, nullptr, 0, seg_len, seg_start, rope, block_table, max_blocks, cache,
-                          layer_cache, slot_mapping_out, stream, layer, 1, 0, fact_ids != nullptr);
+                          layer_caches[0], slot_mapping_out, stream, layer0, n_layers, 0, fact_ids != nullptr,
+                          layer_caches);
+}
+
+is_status_t is_inject_layer(is_store_t* s, int32_t layer, int32_t R, const int64_t* fact_ids,
+                            const int32_t* n_ids, int32_t ids_stride, const int32_t* users,
+                            const int32_t* seg_start, const is_rope_params_t* rope,
+                            const int32_t* block_table, int32_t max_blocks, const is_cache_desc_t* cache,
+                            void* layer_cache, int32_t* seg_len_out, int64_t* slot_mapping_out,
+                            cudaStream_t stream) {
+  if (s && (layer < 0 || layer >= s->cfg.num_layers))
+    return fail(IS_ERR_OUT_OF_RANGE, "layer %d outside [0, %d)", layer, s->cfg.num_layers);
+  void* const caches[1] = {layer_cache};
+  return is_inject_layers(s, layer, 1, R, fact_ids, n_ids, ids_stride, users, seg_start, rope, block_table,
+                          max_blocks, cache, caches, seg_len_out, slot_mapping_out, stream);
 }
 
 is_status_t is_retrieve_and_inject(is_store_t* s, int32_t Q, const int32_t* users, const void* q_emb,

@@ -84,3 +84,19 @@ def test_rope_frequencies_host_side(lib):
         api.is_rope_frequencies(api.make_rope(0.5), 64)
     with pytest.raises(api.ISError):
         api.is_rope_frequencies(api.make_rope(1e4, style=3), 64)
+
+
+def test_binding_constants_match_the_header():
+    """Every integer IS_* constant the binding defines equals the header's #define."""
+    text = open(HEADER).read()
+    defines = {}
+    for name, val in re.findall(r"#define\s+(IS_[A-Z0-9_]+)\s+(\(1 << \d+\)|0x[0-9a-fA-F]+|\d+)u?\b", text):
+        m = re.match(r"\(1 << (\d+)\)", val)
+        defines[name] = (1 << int(m.group(1))) if m else int(val, 0)
+    assert len(defines) >= 8
+    checked = 0
+    for name, value in defines.items():
+        if hasattr(_lib, name):
+            assert getattr(_lib, name) == value, name
+            checked += 1
+    assert checked >= 6

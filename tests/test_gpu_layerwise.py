@@ -119,3 +119,40 @@ def test_reuse_needs_a_plan_of_the_same_size(env):
     with pytest.raises(api.ISError) as e:
         api.is_inject_layer(store, s.num_layers, 2, inp["seg_start"], rope, inp["block_table"], cd, layers[0])
     assert e.value.status == 4
+
+
+def test_layer_groups_equal_the_fused_call(env):
+    """is_inject_layers: all layers into per-layer tensors in one launch (with
+    planning), then groups of layers reusing the plan, each equal byte for byte
+    to the fused call's layers.  The per-layer tensors are allocated one by one
+    (arbitrary addresses, the way an engine keeps them)."""
+    import torch
+    api, wl, store = env
+    s = wl.spec
+    inp = staging.device_inputs(wl)
+    k = s.k
+    fused = staging.canary_cache(wl)
+    out = gh.run_fused(api, store, wl, inp, fused)
+    assert out["status"] == 0
+    ids = torch.empty((2, k), dtype=torch.int64, device="cuda")
+    sc = torch.empty((2, k), dtype=torch.float32, device="cuda")
+    api.is_retrieve_topk(store, inp["users"], inp["q_emb"], k, ids, sc)
+    n_ids = (ids >= 0).sum(1).to(torch.int32)
+    rope = staging.rope_params(wl, api)
+    cd = api.make_cache_desc(s.block_size, wl.num_blocks, "bf16")
+    layers = _layer_caches(wl)
+    api.is_inject_layers(store, 0, 2, inp["seg_start"], rope, inp["block_table"], cd, layers,
+                         fact_ids=ids, n_ids=n_ids)
+    assert api.is_get_status(store) == 0
+    for l in range(s.num_layers):
+        assert torch.equal(fused[l].view(torch.int16), layers[l].view(torch.int16)), f"layer {l}"
+    groups = _layer_caches(wl)
+    for l0, l1 in ((0, 2), (2, 3), (3, s.num_layers)):
+        api.is_inject_layers(store, l0, 2, inp["seg_start"], rope, inp["block_table"], cd, groups[l0:l1])
+    assert api.is_get_status(store) == 0
+    for l in range(s.num_layers):
+        assert torch.equal(fused[l].view(torch.int16), groups[l].view(torch.int16)), f"group layer {l}"
+    with pytest.raises(api.ISError):
+        api.is_inject_layers(store, 1, 2, inp["seg_start"], rope, inp["block_table"], cd, groups)   # past L
+    with pytest.raises(api.ISError):
+        api.is_inject_layers(store, 0, 2, inp["seg_start"], rope, inp["block_table"], cd, [])
