@@ -306,9 +306,11 @@ def run_ours(args, rank, world, local_rank):
 
     # End to end through the public API with host buffers: the C-ABI call
     # that takes the step's inputs (users, queries, starts, block table) in
-    # host memory, stages them through the library's page-locked buffer in one
-    # host-to-device copy, runs the path and returns the ids, scores and
-    # segment lengths in one device-to-host copy (synchronous).
+    # host memory, copies them into the library's page-locked buffer, runs the
+    # path and returns the ids, scores and segment lengths in host memory
+    # (synchronous).  Up to 16 KiB of inputs the kernels read them, and write
+    # the outputs, over the host link; larger inputs go in one host-to-device
+    # copy and the outputs return in one device-to-host copy.
     edt = np.float16 if s.emb_dtype == "f16" else np.float32
     h_users = np.ascontiguousarray(wl.users, dtype=np.int32)
     h_q = np.ascontiguousarray(wl.queries, dtype=edt)

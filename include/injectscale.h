@@ -346,16 +346,19 @@ is_status_t is_retrieve_and_inject(is_store_t* store, int32_t Q, const int32_t* 
 /* ---- is_retrieve_and_inject_host --------------------------------------------
  * is_retrieve_and_inject for a caller whose per-call inputs and outputs are in
  * host memory (any host memory: the library stages them through its own
- * page-locked buffer).  users (int32[Q]), q_emb ([Q][E] in emb_dtype),
- * seg_start (int32[Q]) and block_table (int32[Q][max_blocks_per_seq]) are
- * copied to the device in one transfer; the path runs on `stream`; ids_out
- * (int64[Q][k]), scores_out (float[Q][k]) and seg_len_out (int32[Q]), host
- * arrays that may each be NULL, come back in one transfer.  The store and the
- * paged cache stay on the device (kv_cache is a device pointer).
- * Synchronous: returns once the outputs are in host memory, waiting by
- * polling the stream (the calling thread spins meanwhile).  The staging
- * buffers belong to the store; a call that needs more than the last one had
- * grows them (a synchronisation and an allocation; IS_ERR_OOM if that fails).
+ * page-locked buffer, mapped into the device's address space).  users
+ * (int32[Q]), q_emb ([Q][E] in emb_dtype), seg_start (int32[Q]) and
+ * block_table (int32[Q][max_blocks_per_seq]) are copied into that buffer,
+ * where the kernels read them over the host link; the path runs on `stream`;
+ * the kernels write ids_out (int64[Q][k]), scores_out (float[Q][k]) and
+ * seg_len_out (int32[Q]) into the buffer, and the call copies them to the
+ * caller's host arrays, which may each be NULL.  The store and the paged
+ * cache stay on the device (kv_cache is a device pointer).  Synchronous:
+ * returns once the outputs are in host memory, waiting by polling the stream
+ * (the calling thread spins meanwhile).  The staging buffer belongs to the
+ * store; a call that needs more than the last one had grows it (a
+ * synchronisation and an allocation; IS_ERR_OOM if that fails,
+ * IS_ERR_UNSUPPORTED if the device cannot address it at its host address).
  * Errors as is_retrieve_and_inject, detected before anything is enqueued
  * except device-side ones (read them with is_get_status). */
 is_status_t is_retrieve_and_inject_host(is_store_t* store, int32_t Q, const int32_t* users_host,

@@ -142,6 +142,7 @@ struct TopkArgs {
   int64_t* fact_src;            // [Q][seg_stride] or null
   int32_t seg_stride;
   int32_t* seg_len;             // [Q] or null
+  int32_t* seg_len_copy;        // [Q] or null: a second destination of seg_len (may be mapped host memory)
   const int32_t* block_table;   // [Q][max_blocks] or null (prefetched into L2)
   int32_t max_blocks;
   uint32_t* hist;               // [Q][kCosBins] cosine-bin counts filled by the similarity CTAs, or null

@@ -84,6 +84,7 @@ __device__ __forceinline__ void plan_tail(const TopkArgs& a, int q, int nn, int3
   off[nn] = total;
   a.n_ids_out[q] = nn;
   a.seg_len[q] = total;
+  if (a.seg_len_copy) a.seg_len_copy[q] = total;
 }
 
 // The top-k of query q by the whole CTA (kRetThreads threads):

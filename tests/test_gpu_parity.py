@@ -320,7 +320,10 @@ def test_chunk_pool_over_consecutive_launches(api, cache_dtype):
 def test_host_buffer_call_equals_device_call(api):
     """is_retrieve_and_inject_host (host inputs and outputs, staged through the
     library's page-locked buffer) gives the device call's ids, scores, segment
-    lengths and cache, on repeated calls and after its staging has grown."""
+    lengths and cache, on repeated calls and after its staging has grown: small
+    inputs that the kernels read from the mapped buffer, inputs above 16 KiB
+    (a block table padded by 1024 unused columns) that go over in one copy,
+    then small inputs again."""
     import torch
     wl = workloads.generate(SMALL_BF16)
     s = wl.spec
@@ -337,8 +340,10 @@ def test_host_buffer_call_equals_device_call(api):
         q = np.ascontiguousarray(wl.queries, dtype=edt)
         start = np.ascontiguousarray(wl.seg_start, dtype=np.int32)
         Q = len(users)
-        for k, bt in ((s.k, np.ascontiguousarray(wl.block_table, dtype=np.int32)),
-                      (s.k, np.ascontiguousarray(np.pad(wl.block_table, ((0, 0), (0, 64)))).astype(np.int32))):
+        bt0 = np.ascontiguousarray(wl.block_table, dtype=np.int32)
+        padded = [np.ascontiguousarray(np.pad(bt0, ((0, 0), (0, p)))) for p in (64, 1024)]
+        assert Q * padded[1].shape[1] * 4 > 16384
+        for k, bt in ((s.k, bt0), (s.k, padded[0]), (s.k, padded[1]), (s.k, bt0)):
             host_cache = staging.canary_cache(wl)
             ids = np.full((Q, k), -5, dtype=np.int64)
             sc = np.zeros((Q, k), dtype=np.float32)
