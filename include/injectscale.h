@@ -291,13 +291,14 @@ is_status_t is_inject(is_store_t* store, int32_t R, const int64_t* fact_ids,
 /* ---- is_inject_layer --------------------------------------------------------
  * is_inject for one layer, into that layer's own cache tensor
  * layer_cache [2][num_blocks][block_size][H][D] (K at [0], V at [1]), so an
- * engine can inject layer l while it works on another layer: the pages
- * integrate through vLLM's KV-connector interface ("Méthodologie"), which
+ * engine can inject layer l while it works on another layer: InferScale
+ * ("Méthodologie") integrates through vLLM's KV-connector interface, which
  * saves and loads KV layer by layer.
  *   fact_ids != NULL   plan the segments (as is_inject) and inject `layer`;
  *   fact_ids == NULL   reuse the segment plan of the store's previous
- *                      is_inject, is_inject_layer or is_retrieve_and_inject
- *                      call, which must have had the same R (n_ids, users and
+ *                      is_inject, is_inject_layer(s) or
+ *                      is_retrieve_and_inject(_host) call, which must have
+ *                      had the same R (n_ids, users and
  *                      ids_stride are then ignored); the plan stays valid
  *                      until the next planning call on the store.
  * seg_start and block_table must be the ones the plan was made with.
@@ -316,7 +317,8 @@ is_status_t is_inject_layer(is_store_t* store, int32_t layer, int32_t R, const i
  * each into its own cache tensor: layer_caches is a host array of n_layers
  * device pointers, entry i being layer (layer0 + i)'s
  * [2][num_blocks][block_size][H][D] tensor, at any addresses (16-byte
- * aligned).  This is how an engine that keeps one KV tensor per layer (vLLM)
+ * aligned).  This is how an engine that keeps one KV tensor per layer (vLLM,
+ * whose KV-connector interface InferScale integrates through, "Méthodologie")
  * injects a group of layers, or the whole model (layer0 = 0, n_layers = L),
  * at the cost of one launch.  1 <= n_layers <= IS_MAX_LAYERS_PER_CALL and
  * layer0 + n_layers <= the store's layers (IS_ERR_OUT_OF_RANGE otherwise).
