@@ -301,7 +301,10 @@ is_status_t is_inject(is_store_t* store, int32_t R, const int64_t* fact_ids,
  *                      had the same R (n_ids, users and
  *                      ids_stride are then ignored); the plan stays valid
  *                      until the next planning call on the store.
- * seg_start and block_table must be the ones the plan was made with.
+ * seg_start and block_table must be the ones the plan was made with.  A plan
+ * made by is_inject or is_inject_layer(s) with seg_len_out != NULL keeps its
+ * segment lengths in that array: it must stay allocated and unchanged while
+ * the plan is reused.
  * slot_mapping_out (if given) is written again for this call.  Errors as
  * is_inject, plus IS_ERR_OUT_OF_RANGE for a bad layer and
  * IS_ERR_INVALID_ARG when there is no plan of R requests to reuse. */
@@ -336,7 +339,9 @@ is_status_t is_inject_layers(is_store_t* store, int32_t layer0, int32_t n_layers
  * descending-score order, with no host synchronisation between the stages
  * (the ids never leave the device).  Arguments as in those calls; ids_out,
  * scores_out (device [Q][k]), seg_len_out (device int32[Q]) and
- * slot_mapping_out may each be NULL. */
+ * slot_mapping_out may each be NULL.  The store keeps its own copy of the
+ * segment plan, so a later layer call may reuse it whatever becomes of these
+ * arrays. */
 is_status_t is_retrieve_and_inject(is_store_t* store, int32_t Q, const int32_t* users,
                                    const void* q_emb, int32_t k, const int32_t* seg_start,
                                    const is_rope_params_t* rope, const int32_t* block_table,

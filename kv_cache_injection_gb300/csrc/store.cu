@@ -1134,15 +1134,12 @@ is_status_t is_inject_layer(is_store_t* s, int32_t layer, int32_t R, const int64
                           max_blocks, cache, caches, seg_len_out, slot_mapping_out, stream);
 }
 
-// The fused call.  seg_len_copy (or null) receives the segment lengths a
-// second time; the inject kernel reads them from seg_len_out (or the store's
-// own array), so seg_len_copy may live in mapped host memory.
-static is_status_t retrieve_and_inject(is_store_t* s, int32_t Q, const int32_t* users, const void* q_emb,
-                                       int32_t k, const int32_t* seg_start, const is_rope_params_t* rope,
-                                       const int32_t* block_table, int32_t max_blocks,
-                                       const is_cache_desc_t* cache, void* kv_cache, int64_t* ids_out,
-                                       float* scores_out, int32_t* seg_len_out, int32_t* seg_len_copy,
-                                       int64_t* slot_mapping_out, cudaStream_t stream) {
+is_status_t is_retrieve_and_inject(is_store_t* s, int32_t Q, const int32_t* users, const void* q_emb,
+                                   int32_t k, const int32_t* seg_start, const is_rope_params_t* rope,
+                                   const int32_t* block_table, int32_t max_blocks,
+                                   const is_cache_desc_t* cache, void* kv_cache, int64_t* ids_out,
+                                   float* scores_out, int32_t* seg_len_out, int64_t* slot_mapping_out,
+                                   cudaStream_t stream) {
   is_status_t st = check_retrieve(s, Q, users, q_emb, k);
   if (st != IS_OK) return st;
   if (Q > s->cfg.max_requests && Q > s->cfg.max_queries)
@@ -1152,25 +1149,18 @@ static is_status_t retrieve_and_inject(is_store_t* s, int32_t Q, const int32_t* 
   DeviceGuard g(s->device);
   int64_t* ids = ids_out ? ids_out : s->ids_tmp;
   float* scores = scores_out ? scores_out : s->scores_tmp;
-  int32_t* seg_len = seg_len_out ? seg_len_out : s->seg_len_tmp;
+  // The plan's segment lengths stay in the store, so a later layer call can
+  // reuse the plan whatever becomes of the caller's arrays; the top-k writes
+  // them to seg_len_out as well (device or mapped host memory).
+  int32_t* seg_len = s->seg_len_tmp;
   st = run_retrieval(s, Q, users, q_emb, k, ids, scores, seg_start, seg_len, block_table, max_blocks,
-                     stream, seg_len_copy);
+                     stream, seg_len_out);
   if (st != IS_OK) return st;
   s->plan_R = Q;
   s->plan_seg_len = seg_len;
   return launch_injection(s, Q, ids, k, seg_len, seg_start, rope, block_table, max_blocks, cache,
                           kv_cache, slot_mapping_out, stream, 0, s->cfg.num_layers,
                           cache_layer_bytes(s, cache), true);
-}
-
-is_status_t is_retrieve_and_inject(is_store_t* s, int32_t Q, const int32_t* users, const void* q_emb,
-                                   int32_t k, const int32_t* seg_start, const is_rope_params_t* rope,
-                                   const int32_t* block_table, int32_t max_blocks,
-                                   const is_cache_desc_t* cache, void* kv_cache, int64_t* ids_out,
-                                   float* scores_out, int32_t* seg_len_out, int64_t* slot_mapping_out,
-                                   cudaStream_t stream) {
-  return retrieve_and_inject(s, Q, users, q_emb, k, seg_start, rope, block_table, max_blocks, cache, kv_cache,
-                             ids_out, scores_out, seg_len_out, nullptr, slot_mapping_out, stream);
 }
 
 is_status_t is_retrieve_and_inject_host(is_store_t* s, int32_t Q, const int32_t* users, const void* q_emb,
@@ -1241,14 +1231,11 @@ is_status_t is_retrieve_and_inject_host(is_store_t* s, int32_t Q, const int32_t*
   if (!mapped) CUDA_TRY(cudaMemcpyAsync(d, h, in_bytes, cudaMemcpyHostToDevice, stream));
   uint8_t* hout = h + in_bytes;
   uint8_t* dout = d + in_bytes;
-  // On the mapped path the inject kernel reads the segment lengths from the
-  // store's device array and the top-k writes them into the buffer as well.
-  is_status_t st = retrieve_and_inject(
+  is_status_t st = is_retrieve_and_inject(
       s, Q, reinterpret_cast<const int32_t*>(d), d + b_users, k, reinterpret_cast<const int32_t*>(d + b_users + b_q),
       rope, reinterpret_cast<const int32_t*>(d + b_users + b_q + b_start), max_blocks, cache, kv_cache,
       reinterpret_cast<int64_t*>(dout), reinterpret_cast<float*>(dout + b_ids),
-      mapped ? nullptr : reinterpret_cast<int32_t*>(dout + b_ids + b_sc),
-      mapped ? reinterpret_cast<int32_t*>(dout + b_ids + b_sc) : nullptr, nullptr, stream);
+      reinterpret_cast<int32_t*>(dout + b_ids + b_sc), nullptr, stream);
   if (st != IS_OK) {
     cudaStreamSynchronize(stream);              // the staged inputs stay in use until the kernels ran
     return st;

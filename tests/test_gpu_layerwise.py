@@ -156,3 +156,40 @@ def test_layer_groups_equal_the_fused_call(env):
         api.is_inject_layers(store, 1, 2, inp["seg_start"], rope, inp["block_table"], cd, groups)   # past L
     with pytest.raises(api.ISError):
         api.is_inject_layers(store, 0, 2, inp["seg_start"], rope, inp["block_table"], cd, [])
+
+
+def test_reuse_after_fused_and_host_calls(env):
+    """A layer call may reuse the plan of is_retrieve_and_inject and of
+    is_retrieve_and_inject_host, on its mapped path (small inputs) and on its
+    copy path (a block table padded past 16 KiB): each reuse puts every layer
+    byte for byte where the fused call put it."""
+    import torch
+    api, wl, store = env
+    s = wl.spec
+    inp = staging.device_inputs(wl)
+    fused = staging.canary_cache(wl)
+    out = gh.run_fused(api, store, wl, inp, fused)
+    assert out["status"] == 0
+    rope = staging.rope_params(wl, api)
+    cd = api.make_cache_desc(s.block_size, wl.num_blocks, "bf16")
+    Q = len(wl.users)
+    users = np.ascontiguousarray(wl.users, dtype=np.int32)
+    q = np.ascontiguousarray(wl.queries, dtype=np.float16)
+    start = np.ascontiguousarray(wl.seg_start, dtype=np.int32)
+    bt0 = np.ascontiguousarray(wl.block_table, dtype=np.int32)
+    bt_big = np.ascontiguousarray(np.pad(bt0, ((0, 0), (0, 2048))))
+    assert Q * bt_big.shape[1] * 4 > 16384
+    for planner in ("fused", "host mapped", "host copy"):
+        if planner == "fused":
+            gh.run_fused(api, store, wl, inp, staging.canary_cache(wl))
+        else:
+            bt = bt0 if planner == "host mapped" else bt_big
+            ln = np.empty(Q, dtype=np.int32)
+            api.is_retrieve_and_inject_host(store, users, q, s.k, start, rope, bt, cd, staging.canary_cache(wl),
+                                            seg_len_out=ln)
+            assert np.array_equal(ln, out["seg_len"]), planner
+        layers = _layer_caches(wl)
+        api.is_inject_layers(store, 0, Q, inp["seg_start"], rope, inp["block_table"], cd, layers)
+        assert api.is_get_status(store) == 0
+        for l in range(s.num_layers):
+            assert torch.equal(fused[l].view(torch.int16), layers[l].view(torch.int16)), f"{planner}, layer {l}"
