@@ -8,7 +8,7 @@ import numpy as np
 import pytest
 
 import tests.test_oracle_pins as pins
-from oracle import inject, numerics, retrieval, rope
+from oracle import attention, inject, model, numerics, retrieval, rope
 
 
 def _fails(fn, *args):
@@ -191,3 +191,81 @@ def test_mutation_fp8_value_scale_multiplied(monkeypatch):
     orig = inject.e4m3_value
     monkeypatch.setattr(inject, "e4m3_value", lambda v, dt, s: orig(v, dt, 1.0 / s))
     assert _fails(pins.test_inject_fp8_cache_quantises_scaled_values)
+
+
+def _attention_variant(mask, scale, weights, head_of):
+    """causal_attention with one step replaced: the mask test, the logit scale,
+    the softmax weights or the query-head -> KV-head map."""
+    def fn(q_rot, q_pos, k_rot, k_pos, v):
+        Tq, Hq, D = q_rot.shape
+        Hk = k_rot.shape[1]
+        out = np.zeros((Tq, Hq, D))
+        for i in range(Tq):
+            visible = mask(np.asarray(k_pos), q_pos[i])
+            for h in range(Hq):
+                g = head_of(h, Hq, Hk)
+                logits = k_rot[visible, g, :] @ q_rot[i, h, :] * scale(D)
+                w = weights(logits)
+                out[i, h] = w @ v[visible, g, :]
+        return out
+    return fn
+
+
+def _softmax(z):
+    w = np.exp(z - z.max())
+    return w / w.sum()
+
+
+_MASK = lambda kp, qp: kp <= qp                                      # noqa: E731
+_SCALE = lambda D: 1.0 / np.sqrt(D)                                  # noqa: E731
+_HEAD = lambda h, Hq, Hk: h // (Hq // Hk)                            # noqa: E731
+
+
+@pytest.mark.parametrize("mistake", ["strict_mask", "index_mask", "no_scale", "uniform", "head_mod"])
+def test_mutation_causal_attention(monkeypatch, mistake):
+    mask, scale, weights, head_of = _MASK, _SCALE, _softmax, _HEAD
+    if mistake == "strict_mask":
+        mask = lambda kp, qp: kp < qp                                 # noqa: E731
+    elif mistake == "index_mask":                                     # key index read as its position
+        mask = lambda kp, qp: np.arange(len(kp)) <= qp                # noqa: E731
+    elif mistake == "no_scale":
+        scale = lambda D: 1.0                                         # noqa: E731
+    elif mistake == "uniform":
+        weights = lambda z: np.full(z.shape, 1.0 / z.size)           # noqa: E731
+    else:
+        head_of = lambda h, Hq, Hk: h % Hk                            # noqa: E731
+    monkeypatch.setattr(attention, "causal_attention", _attention_variant(mask, scale, weights, head_of))
+    assert (_fails(pins.test_causal_attention_hand_weights)
+            or _fails(pins.test_causal_attention_grouped_query_heads))
+
+
+def test_mutation_causal_attention_unmutated_passes(monkeypatch):
+    """The variant builder with no mistake passes both pins (so the cases above
+    fail because of their one change)."""
+    monkeypatch.setattr(attention, "causal_attention", _attention_variant(_MASK, _SCALE, _softmax, _HEAD))
+    assert not _fails(pins.test_causal_attention_hand_weights)
+    assert not _fails(pins.test_causal_attention_grouped_query_heads)
+
+
+@pytest.mark.parametrize("mistake", ["sum", "eps_outside", "no_sqrt"])
+def test_mutation_rmsnorm(monkeypatch, mistake):
+    def wrong(x, eps=1e-6):
+        x = np.asarray(x, dtype=np.float64)
+        ms = np.mean(x * x, axis=-1, keepdims=True)
+        if mistake == "sum":
+            return x / np.sqrt(np.sum(x * x, axis=-1, keepdims=True) + eps)
+        if mistake == "eps_outside":
+            return x / (np.sqrt(ms) + eps)
+        return x / (ms + eps)
+    monkeypatch.setattr(model, "rmsnorm", wrong)
+    assert _fails(pins.test_rmsnorm_hand_values)
+
+
+@pytest.mark.parametrize("mistake", ["negated", "no_x"])
+def test_mutation_silu(monkeypatch, mistake):
+    if mistake == "negated":
+        wrong = lambda x: x / (1.0 + np.exp(x))                       # noqa: E731  x·sigmoid(-x)
+    else:
+        wrong = lambda x: 1.0 / (1.0 + np.exp(-x))                    # noqa: E731  sigmoid alone
+    monkeypatch.setattr(model, "silu", wrong)
+    assert _fails(pins.test_silu_hand_values)

@@ -13,7 +13,7 @@ import os
 import numpy as np
 import pytest
 
-from oracle import attention, inject, numerics, retrieval, rope
+from oracle import attention, inject, model, numerics, retrieval, rope
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 
@@ -363,6 +363,68 @@ def test_inject_tiny_canaries_and_copies(dtype):
         assert np.array_equal(cache[:, 0, blk, off], numerics.encode(krot, dtype))
     same = (cache.view(np.uint8) == before.view(np.uint8)).reshape(cache.shape + (-1,)).all(-1)
     assert same[~touched].all()
+
+
+# ---------------------------------------------------------------- attention, RMSNorm, SiLU by hand
+
+def test_causal_attention_hand_weights():
+    """Softmax attention (Vaswani et al., scaled dot product) worked by hand.
+
+    D = 2, one head.  q = (sqrt(2)·ln 2, 0) and k_s = (s, 0), so after the
+    1/sqrt(D) scale the logit of key s is s·ln 2 and its softmax weight is
+    proportional to 2^s: a query that sees keys 0, 1, 2 weighs them 1/7, 2/7,
+    4/7.  Keys sit at positions 5, 7, 9 and queries at 5, 8, 9, so the causal
+    mask has to compare positions (key position <= query position), not
+    indices: the query at 8 sees keys 0 and 1 only (weights 1/3, 2/3)."""
+    a = math.sqrt(2.0) * math.log(2.0)
+    q = np.array([[a, 0.0], [a, 0.0], [a, 0.0]])[:, None, :]
+    k = np.array([[0.0, 0.0], [1.0, 0.0], [2.0, 0.0]])[:, None, :]
+    v = np.array([[1.0, 0.0], [0.0, 1.0], [1.0, 1.0]])[:, None, :]
+    out = attention.causal_attention(q, np.array([5, 8, 9]), k, np.array([5, 7, 9]), v)
+    want = np.array([[1.0, 0.0], [1 / 3, 2 / 3], [5 / 7, 6 / 7]])
+    assert np.max(np.abs(out[:, 0, :] - want)) < 1e-15
+
+
+def test_causal_attention_grouped_query_heads():
+    """Grouped-query attention: with 4 query heads over 2 KV heads, query heads
+    0 and 1 read KV head 0 and heads 2 and 3 read KV head 1.  Every key gets the
+    same logit (zero query), so each output is the plain mean of the visible
+    values of its KV head."""
+    q = np.zeros((2, 4, 2))
+    k = np.ones((2, 2, 2))
+    v = np.array([[[1.0, 2.0], [10.0, 20.0]],
+                  [[3.0, 4.0], [30.0, 40.0]]])                  # [token][kv head][D]
+    out = attention.causal_attention(q, np.array([0, 1]), k, np.array([0, 1]), v)
+    for h in range(4):
+        g = h // 2
+        assert np.array_equal(out[0, h], v[0, g])
+        assert np.max(np.abs(out[1, h] - (v[0, g] + v[1, g]) / 2)) < 1e-15
+
+
+def test_rmsnorm_hand_values():
+    """RMSNorm without gain (Zhang and Sennrich): x / sqrt(mean(x²) + eps).
+    (3, 4): mean square 12.5, so the result is (3, 4)/sqrt(12.5); a constant
+    vector c·1 maps to 1 (up to eps); the scale of x does not matter."""
+    y = model.rmsnorm(np.array([3.0, 4.0]), eps=0.0)
+    assert np.max(np.abs(y - np.array([3.0, 4.0]) / math.sqrt(12.5))) < 1e-15
+    assert abs(y[0] - 0.848528137423857) < 1e-14 and abs(y[1] - 1.131370849898476) < 1e-14
+    assert np.max(np.abs(model.rmsnorm(np.full(7, -2.5), eps=0.0) + 1.0)) < 1e-15
+    x = np.random.default_rng(3).standard_normal((4, 9))
+    assert np.max(np.abs(model.rmsnorm(x * 1e3, eps=0.0) - model.rmsnorm(x, eps=0.0))) < 1e-13
+    # eps sits under the square root: (3, 4) with eps = 12.5 halves the mean square's root.
+    y = model.rmsnorm(np.array([3.0, 4.0]), eps=12.5)
+    assert np.max(np.abs(y - np.array([3.0, 4.0]) / 5.0)) < 1e-15
+
+
+def test_silu_hand_values():
+    """SiLU(x) = x·sigmoid(x) (Elfwing et al.; Hendrycks and Gimpel).
+    SiLU(0) = 0; SiLU(ln 3) = ln 3 · 3/4; SiLU(-ln 3) = -ln 3 · 1/4;
+    SiLU(x) -> x as x -> +inf and -> 0 as x -> -inf."""
+    ln3 = math.log(3.0)
+    y = model.silu(np.array([0.0, ln3, -ln3, 40.0, -40.0]))
+    assert y[0] == 0.0
+    assert abs(y[1] - 0.75 * ln3) < 1e-15 and abs(y[2] + 0.25 * ln3) < 1e-15
+    assert abs(y[3] - 40.0) < 1e-12 and abs(y[4]) < 1e-14
 
 
 # ---------------------------------------------------------------- Theorem 3 / 6 on tiny attention
