@@ -72,11 +72,45 @@ def assert_only_slots_changed(cache, dtype: str, slots) -> None:
         f"{int((ch != exp).sum())} cache rows differ from the expected set"
 
 
+class DeviceFactCache:
+    """Whole facts' K and V (storage encoding, [len][L][H][D]) drawn by the
+    device copy of the seeded input generator, which is bit-equal to
+    ``synth.kvgen`` (``test_device_generator_matches_host``): the same inputs
+    as ``parity.FactCache``, regenerated in milliseconds instead of seconds."""
+
+    def __init__(self, wl):
+        self.wl = wl
+        self._m = {}
+
+    def __call__(self, f: int):
+        import torch
+        from synth import kvgen
+        f = int(f)
+        if f not in self._m:
+            s = self.wl.spec
+            n = int(self.wl.lengths[f])
+            first = int(self.wl.tok_base[f]) * s.token_elems
+            out = []
+            for stream in (kvgen.STREAM_K, kvgen.STREAM_V):
+                t = torch.empty(n * s.token_elems, dtype=staging.torch_dtype(s.kv_dtype), device="cuda")
+                staging.fill_kv(t, s.kv_dtype, s.seed, stream, first)
+                out.append(staging.cache_bits(t).reshape(n, s.num_layers, s.num_kv_heads, s.head_dim))
+            self._m[f] = tuple(out)
+        return self._m[f]
+
+    def token(self, f: int, t: int):
+        K, V = self(f)
+        return K[int(t)], V[int(t)]
+
+
 def check_fused_workload(api, wl, store, k=None, sample_tokens=160, seed=0, cache_dtype=None,
-                         k_scale=1.0, v_scale=1.0):
+                         k_scale=1.0, v_scale=1.0, all_tokens=False):
     """Fused retrieve + inject of ``wl`` through ``store`` against the oracle:
-    every top-k, segment length and slot; a sample of injected tokens; and
-    that exactly the targeted cache rows changed.  Returns the cache too."""
+    every top-k, segment length and slot; the injected tokens; and that
+    exactly the targeted cache rows changed.  ``all_tokens`` (True, or a list
+    of query indices) compares every injected token of those queries, all
+    layers and heads; the other queries' tokens are sampled (first and last of
+    every segment plus ``sample_tokens`` random ones).  Returns the cache too."""
     inp = staging.device_inputs(wl)
     cache = staging.canary_cache(wl, cache_dtype=cache_dtype)
     k = wl.spec.k if k is None else k
@@ -93,21 +127,40 @@ def check_fused_workload(api, wl, store, k=None, sample_tokens=160, seed=0, cach
     assert np.array_equal(out["slot_map"][: len(want_slots)], want_slots)
     assert len(np.unique(want_slots)) == len(want_slots)
     assert_only_slots_changed(cache, cache_dtype or wl.spec.kv_dtype, want_slots)
-    # sampled tokens: first and last token of every segment, plus random ones
-    entries = [e for pl in plans for e in pl]
-    rng = np.random.default_rng(seed)
-    pick = set(rng.choice(len(entries), size=min(sample_tokens, len(entries)), replace=False).tolist())
-    off = 0
-    for pl in plans:
-        if pl:
-            pick.update([off, off + len(pl) - 1])
-        off += len(pl)
-    sample = [entries[i] for i in sorted(pick)]
-    gk, gv = gather_rows(cache, [e[3] for e in sample])
-    if cache_dtype == "e4m3":
-        stats = parity.compare_tokens_fp8(wl, gk, gv, sample, parity.oracle_freqs(wl), wl.spec.rope.style,
-                                          parity.FactCache(wl), k_scale, v_scale)
-    else:
-        stats = parity.compare_tokens(wl, gk, gv, sample, parity.oracle_freqs(wl), wl.spec.rope.style,
-                                      parity.FactCache(wl))
-    return {"tokens": int(lens.sum()), "swapped": swapped, "cache": cache, **stats}
+    full_q = (set(range(len(plans))) if all_tokens is True
+              else set(int(q) for q in all_tokens) if all_tokens else set())
+    freqs, style = parity.oracle_freqs(wl), wl.spec.rope.style
+    stats = {"n": 0, "within_1ulp": 0, "floor_only": 0, "saturated": 0, "v_saturated": 0}
+    # every token of the queries in full_q, one request at a time
+    dfacts = DeviceFactCache(wl)
+    n_full = 0
+    for q in sorted(full_q):
+        if not plans[q]:
+            continue
+        gk, gv = gather_rows(cache, [e[3] for e in plans[q]])
+        st = parity.compare_runs(wl, gk, gv, plans[q], freqs, style, dfacts,
+                                 (k_scale, v_scale) if cache_dtype == "e4m3" else None)
+        for key, val in st.items():
+            stats[key] += val
+        n_full += len(plans[q])
+    # the other queries: first and last token of every segment, plus random ones
+    entries, ends = [], set()
+    for q, pl in enumerate(plans):
+        if q not in full_q:
+            if pl:
+                ends.update([len(entries), len(entries) + len(pl) - 1])
+            entries.extend(pl)
+    if entries:
+        rng = np.random.default_rng(seed)
+        pick = set(rng.choice(len(entries), size=min(sample_tokens, len(entries)), replace=False).tolist())
+        sample = [entries[i] for i in sorted(pick | ends)]
+        gk, gv = gather_rows(cache, [e[3] for e in sample])
+        if cache_dtype == "e4m3":
+            st = parity.compare_tokens_fp8(wl, gk, gv, sample, freqs, style, parity.FactCache(wl),
+                                           k_scale, v_scale)
+        else:
+            st = parity.compare_tokens(wl, gk, gv, sample, freqs, style, parity.FactCache(wl))
+        for key, val in st.items():
+            stats[key] += val
+    return {"tokens": int(lens.sum()), "tokens_compared_in_full": n_full, "swapped": swapped,
+            "cache": cache, **stats}

@@ -132,6 +132,48 @@ def compare_tokens(wl, gathered_k, gathered_v, entries, freqs, style: int, facts
     return stats
 
 
+def fact_runs(entries):
+    """Split plan entries (fact, t, p, slot) into runs of consecutive tokens of
+    one fact: yields (i0, i1, fact, t array, p array)."""
+    i = 0
+    while i < len(entries):
+        f, t0 = entries[i][0], entries[i][1]
+        j = i + 1
+        while j < len(entries) and entries[j][0] == f and entries[j][1] == t0 + (j - i):
+            j += 1
+        yield (i, j, int(f), np.array([e[1] for e in entries[i:j]]),
+               np.array([e[2] for e in entries[i:j]], dtype=np.int64))
+        i = j
+
+
+def compare_runs(wl, gathered_k, gathered_v, entries, freqs, style: int, facts,
+                 fp8_scales=None) -> dict:
+    """compare_tokens (or compare_tokens_fp8 when ``fp8_scales`` = (k_scale,
+    v_scale)) over every entry, one fact run at a time: the same checks,
+    vectorised over the run's tokens.  ``facts(f)`` returns the whole fact's
+    (K, V) [len][L][H][D] in storage encoding."""
+    dtype = wl.spec.kv_dtype
+    stats = {"n": 0, "within_1ulp": 0, "floor_only": 0, "saturated": 0, "v_saturated": 0}
+    for i0, i1, f, ts, ps in fact_runs(entries):
+        K, V = facts(f)
+        Kt, Vt = K[ts], V[ts]
+        o = oinject.rotated_key_rows(Kt, ps[:, None, None], freqs, style, dtype)
+        x = numerics.decode(Kt, dtype)
+        if fp8_scales is None:
+            assert np.array_equal(np.asarray(gathered_v[i0:i1]).view(np.uint8), Vt.view(np.uint8)), \
+                f"V of fact {f} differs"
+            st = check_rotated(gathered_k[i0:i1], o, x, style, dtype)
+        else:
+            k_scale, v_scale = fp8_scales
+            want_v = oinject.e4m3_value(Vt, dtype, v_scale)
+            assert np.array_equal(np.asarray(gathered_v[i0:i1]), want_v), f"FP8 V of fact {f} differs"
+            stats["v_saturated"] += int((np.abs(numerics.e4m3_bits_to_f64(want_v)) == numerics.E4M3_MAX).sum())
+            st = check_rotated_e4m3(gathered_k[i0:i1], o, x, style, k_scale)
+        for key, val in st.items():
+            stats[key] += val
+    return stats
+
+
 def oracle_freqs(wl):
     r = wl.spec.rope
     return rope.inv_freq(wl.spec.head_dim, r.theta, r.scaling, r.factor, r.low_freq_factor,

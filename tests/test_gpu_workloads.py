@@ -2,10 +2,11 @@
 times (the fused is_retrieve_and_inject).
 
 At these sizes the oracle checks every query's top-k, every request's segment
-length and every slot of the slot mapping, and rotates/compares a sample of
-the injected tokens (all layers and heads of the sampled tokens); every
-cache row is checked on the device to have changed exactly when its slot was
-targeted.
+length and every slot of the slot mapping; every cache row is checked on the
+device to have changed exactly when its slot was targeted.  The injected
+tokens are compared element by element with the oracle: all of them for the
+Llama-3.1-8B request and for one Qwen2.5-7B user, a sample (first and last
+token of every segment plus random ones, all layers and heads) elsewhere.
 """
 import pytest
 
@@ -33,8 +34,9 @@ class TestLlama31:
 
     def test_fused_parity(self, api, loaded):
         wl, store = loaded
-        st = gh.check_fused_workload(api, wl, store)
+        st = gh.check_fused_workload(api, wl, store, all_tokens=True)
         assert st["tokens"] > 40 * 10
+        assert st["n"] == st["tokens"] * wl.spec.token_elems      # every injected key element
 
     def test_planted_fact_is_retrieved(self, api, loaded):
         import torch
@@ -73,8 +75,9 @@ class TestQwen100Users:
 
     def test_fused_parity(self, api, loaded):
         wl, store = loaded
-        st = gh.check_fused_workload(api, wl, store, sample_tokens=300)
+        st = gh.check_fused_workload(api, wl, store, sample_tokens=300, all_tokens=[0])
         assert st["tokens"] > 100 * 50 * 10
+        assert st["tokens_compared_in_full"] >= 50 * 10
 
     def test_fused_parity_tensor_core_similarity(self, api, loaded):
         """The same 100 queries with the similarity as tcgen05 contractions
