@@ -383,11 +383,16 @@ is_status_t is_retrieve_and_inject_host(is_store_t* store, int32_t Q, const int3
  * keeps facts in its own buffers and still wants the gather + Chunked RoPE +
  * paged scatter.  This call creates no store and allocates nothing: the
  * per-request segment plan lives in a static device array of the library
- * (about 265 KB, held on every device that loads the library until exit).
- *   kv_arena             device, token-major [tokens][L][2][H][D] in kv_dtype
+ * (about 269 KB, held on every device that loads the library until exit).
+ *   kv_arena             device, token-major [arena_tokens][L][2][H][D] in kv_dtype
  *                        (per token and layer: K row then V row, K before RoPE)
+ *   arena_tokens         tokens in kv_arena, >= 1
  *   fact_tok, fact_len   device int64[n_facts] first arena token, int32[n_facts]
- *                        length (each in [1, max_fact_len])
+ *                        length.  They are checked on the device: a fact whose
+ *                        length is outside [1, max_fact_len] or whose tokens leave
+ *                        [0, arena_tokens) latches IS_ST_FACT_RANGE and is left
+ *                        out of its segment (length 0), like an id outside
+ *                        [0, n_facts); nothing is read for it
  *   R                    1 <= R <= IS_NOALLOC_MAX_REQUESTS
  *   ids_stride           1 <= ids_stride <= IS_NOALLOC_MAX_FACTS
  *   status_out           device uint32, caller-owned: IS_ST_* bits are OR-ed in
@@ -398,14 +403,15 @@ is_status_t is_retrieve_and_inject_host(is_store_t* store, int32_t Q, const int3
  * return IS_ERR_UNSUPPORTED before anything is enqueued.  The first call on a
  * device looks up the static array's device address (once per device, under
  * a lock); make that first call before any stream capture.  Every call uses
- * the same static array and overwrites the entries it reads, so nothing has
- * to start at zero, but two calls whose kernels overlap on the GPU (different
- * streams, no ordering between them) race on it. */
+ * the same static array: its planning kernel writes the plan entries and
+ * zeroes the work counters its injection kernel then uses, so a call depends
+ * on nothing an earlier call left there, but two calls whose kernels overlap
+ * on the GPU (different streams, no ordering between them) race on it. */
 #define IS_NOALLOC_MAX_REQUESTS 256
 #define IS_NOALLOC_MAX_FACTS    256
-is_status_t is_inject_noalloc(const void* kv_arena, const int64_t* fact_tok,
-                              const int32_t* fact_len, int64_t n_facts, int32_t max_fact_len,
-                              int32_t num_layers, int32_t num_kv_heads, int32_t head_dim,
+is_status_t is_inject_noalloc(const void* kv_arena, int64_t arena_tokens,
+                              const int64_t* fact_tok, const int32_t* fact_len, int64_t n_facts,
+                              int32_t max_fact_len, int32_t num_layers, int32_t num_kv_heads, int32_t head_dim,
                               int32_t kv_dtype, int32_t R, const int64_t* fact_ids,
                               const int32_t* n_ids, int32_t ids_stride, const int32_t* seg_start,
                               const is_rope_params_t* rope, const int32_t* block_table,
@@ -429,6 +435,21 @@ is_status_t is_inject_noalloc(const void* kv_arena, const int64_t* fact_tok,
 #define IS_RETRIEVAL_PER_QUERY 1
 #define IS_RETRIEVAL_BATCHED   2
 is_status_t is_set_retrieval_mode(is_store_t* store, int32_t mode);
+
+/* ---- is_set_wait_budget ---------------------------------------------------------
+ * Every wait inside the store's kernels is bounded: a wait for data that does
+ * not arrive gives up, latches IS_ST_TIMEOUT, lets the copies it already
+ * started land and ends its kernel, so a stalled GPU memory system cannot
+ * hang the caller, and is_get_status then returns IS_ERR_TIMEOUT.  This sets
+ * the budget, in nanoseconds, of each wait in the injection pipeline and in
+ * the batched (tensor-core) similarity: 0 <= budget_ns <= 2 s, default 2 s.
+ * With 0 a wait looks once and gives up at once if its data has not landed,
+ * which is how the tests exercise the time-out path.  The waits that let
+ * copies in flight land before a kernel ends always keep 2 s.  After a time-out
+ * the call's outputs are undefined, except that every cache row is either
+ * left as it was or holds what the call would have written there.
+ * Errors: IS_ERR_INVALID_ARG for a budget outside that range. */
+is_status_t is_set_wait_budget(is_store_t* store, int64_t budget_ns);
 
 /* ---- status / diagnostics ---------------------------------------------------
  * is_get_status: synchronise `stream`, read the device status word into

@@ -79,7 +79,7 @@ SIGNATURES = {
     "is_retrieve_and_inject_host": [c_void_p, c_int32, c_void_p, c_void_p, c_int32, c_void_p,
                                     POINTER(RopeParams), c_void_p, c_int32, POINTER(CacheDesc),
                                     c_void_p, c_void_p, c_void_p, c_void_p, c_void_p],
-    "is_inject_noalloc": [c_void_p, c_void_p, c_void_p, c_int64, c_int32, c_int32, c_int32,
+    "is_inject_noalloc": [c_void_p, c_int64, c_void_p, c_void_p, c_int64, c_int32, c_int32, c_int32,
                           c_int32, c_int32, c_int32, c_void_p, c_void_p, c_int32, c_void_p,
                           POINTER(RopeParams), c_void_p, c_int32, POINTER(CacheDesc), c_void_p,
                           c_void_p, c_void_p, c_void_p, c_void_p],
@@ -88,6 +88,7 @@ SIGNATURES = {
     "is_status_string": [c_int],
     "is_rope_frequencies": [POINTER(RopeParams), c_int32, POINTER(c_double)],
     "is_set_retrieval_mode": [c_void_p, c_int32],
+    "is_set_wait_budget": [c_void_p, c_int64],
     "is_set_timing": [c_void_p, c_int32],
     "is_get_timing": [c_void_p, c_int32, POINTER(c_double), POINTER(c_int64)],
     "is_reset_timing": [c_void_p],

@@ -262,17 +262,18 @@ def is_retrieve_and_inject_host(store: Store, users, q_emb, k: int, seg_start, r
                                      ids_out, scores_out, seg_len_out, stream)()
 
 
-def is_inject_noalloc(kv_arena, fact_tok, fact_len, max_fact_len: int, num_layers: int,
-                      num_kv_heads: int, head_dim: int, kv_dtype, fact_ids, n_ids, seg_start,
-                      rope: RopeParams, block_table, cache: CacheDesc, kv_cache, status_out,
+def is_inject_noalloc(kv_arena, arena_tokens: int, fact_tok, fact_len, max_fact_len: int,
+                      num_layers: int, num_kv_heads: int, head_dim: int, kv_dtype, fact_ids, n_ids,
+                      seg_start, rope: RopeParams, block_table, cache: CacheDesc, kv_cache, status_out,
                       seg_len_out=None, slot_mapping_out=None, stream=None) -> None:
-    """Store-free injection from a caller-owned token-major K/V arena; the
-    library allocates nothing (its plan scratch is a static device array)."""
+    """Store-free injection from a caller-owned token-major K/V arena of
+    ``arena_tokens`` tokens; the library allocates nothing (its plan scratch
+    is a static device array)."""
     dt = DTYPE_CODES[kv_dtype] if isinstance(kv_dtype, str) else int(kv_dtype)
     R, stride = int(fact_ids.shape[0]), int(fact_ids.shape[1])
     _check(_lib.load().is_inject_noalloc(
-        _ptr(kv_arena), _ptr(fact_tok), _ptr(fact_len), int(fact_len.shape[0]), int(max_fact_len),
-        int(num_layers), int(num_kv_heads), int(head_dim), dt, R, _ptr(fact_ids), _ptr(n_ids),
+        _ptr(kv_arena), int(arena_tokens), _ptr(fact_tok), _ptr(fact_len), int(fact_len.shape[0]),
+        int(max_fact_len), int(num_layers), int(num_kv_heads), int(head_dim), dt, R, _ptr(fact_ids), _ptr(n_ids),
         stride, _ptr(seg_start), byref(rope), _ptr(block_table), int(block_table.shape[1]),
         byref(cache), _ptr(kv_cache), _ptr(seg_len_out), _ptr(slot_mapping_out), _ptr(status_out),
         _stream(stream)))
@@ -296,6 +297,10 @@ def is_rope_frequencies(rope: RopeParams, head_dim: int) -> np.ndarray:
 
 def is_set_retrieval_mode(store: Store, mode: int) -> None:
     _check(_lib.load().is_set_retrieval_mode(c_void_p(store.handle), int(mode)))
+
+
+def is_set_wait_budget(store: Store, budget_ns: int) -> None:
+    _check(_lib.load().is_set_wait_budget(c_void_p(store.handle), int(budget_ns)))
 
 
 def is_set_timing(store: Store, enable: bool) -> None:

@@ -55,6 +55,7 @@ struct InjectArgs {
   int32_t head_vecs;            // 16-byte vectors per head (D / VE)
   int32_t cache_row_bytes;      // H * D * elt of the cache (row_bytes, or H * D for FP8)
   float k_inv, v_inv;           // FP8 cache: fp32(1 / k_scale), fp32(1 / v_scale)
+  uint64_t wait_ns;             // budget of each pipeline wait (the drain of copies in flight keeps 2 s)
   uint32_t* work_ctr;           // kPoolCtrs counters of pool claims in this launch (zero at its start)
   uint32_t* work_ctr_next;      // the counters of the next launch, zeroed by this one
   int32_t chunk_items;          // items per pool chunk (set by the launcher)
@@ -96,6 +97,15 @@ struct PlanArgs {
   int32_t* seg_len;             // [R]
   uint32_t* status;
   int32_t R;
+  // Caller-owned fact tables (is_inject_noalloc) are checked here, since no
+  // store checked them when the facts were added: with arena_tokens > 0 a
+  // fact whose length lies outside [1, max_fact_len] or whose tokens leave
+  // [0, arena_tokens) latches IS_ST_FACT_RANGE and counts as length 0.
+  int64_t arena_tokens;
+  int32_t max_fact_len;
+  // If set, CTA 0 zeroes these kPoolCtrs chunk counters (kCtrStride words
+  // apart) for the inject launch that follows this plan in the stream.
+  uint32_t* zero_ctr;
 };
 
 // The inject kernel's pool of work chunks is claimed through kPoolCtrs
@@ -181,6 +191,7 @@ struct GemmArgs {
   int64_t score_stride;
   int32_t E;
   uint32_t* status;
+  uint64_t wait_ns;             // budget of each pipeline wait (drains keep 2 s)
 };
 
 // ------------------------------------------------------------------ device helpers
@@ -348,9 +359,28 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
   return t;
 }
 
+// Default and largest budget of a bounded wait; waits that drain copies
+// already in flight before a kernel exits always use it.
+constexpr uint64_t kWaitBudgetNs = 2000000000ull;   // 2 s
+
+// Non-blocking test of an mbarrier phase.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Bounded wait for an mbarrier phase: gives up after `budget_ns` of wall time
-// (or 2^26 polls) and returns false.
+// (or 2^26 polls) and returns false.  A zero budget looks once, without
+// waiting.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, uint64_t budget_ns) {
+  if (budget_ns == 0) return mbar_test_wait(bar, parity);
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   for (uint32_t it = 0; it < (1u << 26); ++it) {

@@ -31,6 +31,7 @@ __global__ void __launch_bounds__(256) plan_kernel(const PlanArgs a) {
   }
   const int32_t user = a.users ? a.users[r] : -1;
   int32_t* off = a.fact_seg_off + (size_t)r * a.seg_stride;
+  if (a.zero_ctr && r == 0 && threadIdx.x < kPoolCtrs) a.zero_ctr[threadIdx.x * kCtrStride] = 0u;
   if (a.block_table) prefetch_row_l2(a.block_table + (size_t)r * a.max_blocks, a.max_blocks, threadIdx.x, blockDim.x);
   int32_t carry = 0;
   for (int base = 0; base < n; base += blockDim.x) {
@@ -44,6 +45,13 @@ __global__ void __launch_bounds__(256) plan_kernel(const PlanArgs a) {
         latch(a.status, IS_ST_FACT_USER);
       } else {
         len = a.fact_len[f];
+        if (a.arena_tokens > 0) {
+          const int64_t tok = a.fact_tok[f];
+          if (len < 1 || len > a.max_fact_len || tok < 0 || tok > a.arena_tokens - len) {
+            latch(a.status, IS_ST_FACT_RANGE);
+            len = 0;
+          }
+        }
         if (a.fact_src) a.fact_src[(size_t)r * a.seg_stride + i] = a.fact_tok[f];
       }
     }
@@ -84,10 +92,11 @@ __global__ void __launch_bounds__(256) plan_kernel(const PlanArgs a) {
 // stores.  NeoX pairs (i, i + D/2) lie in vectors v and v ^ half_vecs of the
 // row, interleaved pairs inside one vector; either way the frequencies a lane
 // needs depend only on its lane index, so it computes VE (or VE/2) sin/cos
-// once per position.  Every mbarrier wait is bounded: on time-out the warp
-// latches IS_ST_TIMEOUT, stops issuing, drains its copies and returns.
+// once per position.  Every mbarrier wait is bounded (a.wait_ns, 2 s unless
+// the store was told otherwise): on time-out the warp latches IS_ST_TIMEOUT,
+// stops issuing, waits up to kWaitBudgetNs for each of its loads in flight to
+// land, waits for its bulk stores and returns.
 constexpr int kInjectWarpsMax = 8;
-constexpr uint64_t kWaitBudgetNs = 2000000000ull;   // 2 s per wait
 
 struct StageMeta {
   int64_t slot;     // destination slot, -1 = nothing to do
@@ -248,8 +257,11 @@ struct TokenCursor {
       o[e] = in ? off[idx] : 0;
       sv[e] = (in && fsrc) ? fsrc[idx] : 0;
     }
-    // Offsets strictly increase, so "offset <= ts" holds for a prefix of the
-    // facts; its last entry is the fact holding ts (off[0] = 0 <= ts).
+    // Offsets never decrease, so "offset <= ts" holds for a prefix of the
+    // facts; its last entry is the fact holding ts (off[0] = 0 <= ts).  A
+    // fact the plan left out has length 0: the entry after it has the same
+    // offset (or it is the last, whose offset is the segment length > ts), so
+    // it is never that last entry.
     int best = -1;
 #pragma unroll
     for (int e = 0; e < kPer; ++e) {
@@ -496,7 +508,7 @@ __global__ void __launch_bounds__(kInjectWarpsMax * 32) inject_kernel(const Inje
     const StageMeta m = meta[s];
     if (m.slot >= 0) {
       const uint32_t bar = smem_addr(&bars[s]);
-      const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar, (phase >> s) & 1u, kWaitBudgetNs));
+      const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar, (phase >> s) & 1u, a.wait_ns));
       if (!ok) {
         if (lane == 0) latch(a.status, IS_ST_TIMEOUT);
         aborted = true;
@@ -829,14 +841,15 @@ constexpr size_t kNaWords = kNaCtrOff + 2 * isk::kPoolCtrWords;
 constexpr int kNaMaxDevices = 64;
 
 // [0, R*stride): per-request prefix of fact lengths; then n_ids[R]; then
-// seg_len[R]; then, from a 128-byte boundary, the inject kernel's two sets of
-// chunk counters, used by alternate launches (zero at load; each launch
-// zeroes the other set).
+// seg_len[R]; then, from a 128-byte boundary, two sets of the inject kernel's
+// chunk counters.  Every call's planning kernel zeroes the first set, which
+// that call's inject kernel then claims from; the inject kernel zeroes the
+// second set as it would for a following launch, and nothing reads it.  So
+// a call depends on no state a previous call left, on the host or the device.
 static __device__ __align__(256) int32_t g_noalloc_scratch[kNaWords];
 
 struct NoAllocDevice {
   bool ready = false;
-  int parity = 0;               // which of the two chunk counters the next launch uses
   int32_t* scratch = nullptr;   // device address of g_noalloc_scratch on this device
   int num_sms = 0;
 };
@@ -852,7 +865,7 @@ is_status_t na_fail(is_status_t st, const char* msg) {
 }  // namespace
 
 extern "C" is_status_t is_inject_noalloc(
-    const void* kv_arena, const int64_t* fact_tok, const int32_t* fact_len, int64_t n_facts,
+    const void* kv_arena, int64_t arena_tokens, const int64_t* fact_tok, const int32_t* fact_len, int64_t n_facts,
     int32_t max_fact_len, int32_t num_layers, int32_t num_kv_heads, int32_t head_dim,
     int32_t kv_dtype, int32_t R, const int64_t* fact_ids, const int32_t* n_ids, int32_t ids_stride,
     const int32_t* seg_start, const is_rope_params_t* rope, const int32_t* block_table,
@@ -866,8 +879,9 @@ extern "C" is_status_t is_inject_noalloc(
     return na_fail(IS_ERR_UNSUPPORTED, "R must be in [1, IS_NOALLOC_MAX_REQUESTS]");
   if (ids_stride < 1 || ids_stride > IS_NOALLOC_MAX_FACTS)
     return na_fail(IS_ERR_UNSUPPORTED, "ids_stride must be in [1, IS_NOALLOC_MAX_FACTS]");
-  if (n_facts < 1 || max_fact_len < 1 || max_blocks_per_seq < 1)
-    return na_fail(IS_ERR_INVALID_ARG, "n_facts, max_fact_len, max_blocks_per_seq must be >= 1");
+  if (n_facts < 1 || max_fact_len < 1 || max_blocks_per_seq < 1 || arena_tokens < 1)
+    return na_fail(IS_ERR_INVALID_ARG,
+                   "arena_tokens, n_facts, max_fact_len, max_blocks_per_seq must be >= 1");
   if ((int64_t)R * ids_stride * max_fact_len >= (int64_t)INT32_MAX)
     return na_fail(IS_ERR_UNSUPPORTED, "R * ids_stride * max_fact_len must stay below 2^31");
   if (kv_dtype != IS_F32 && kv_dtype != IS_BF16 && kv_dtype != IS_F16)
@@ -934,6 +948,10 @@ extern "C" is_status_t is_inject_noalloc(
   p.seg_len = seg_len;
   p.status = status_out;
   p.R = R;
+  p.arena_tokens = arena_tokens;
+  p.max_fact_len = max_fact_len;
+  uint32_t* ctr = reinterpret_cast<uint32_t*>(d.scratch + kNaCtrOff);
+  p.zero_ctr = ctr;
   const LaunchCfg cfg{stream, d.num_sms, false};
   if (launch_plan(p, cfg) != cudaSuccess) return na_fail(IS_ERR_CUDA, "plan launch failed");
 
@@ -965,12 +983,9 @@ extern "C" is_status_t is_inject_noalloc(
   a.layer_stride = 2LL * cache->num_blocks * cache->block_size * row_bytes;
   a.row_bytes = (int32_t)row_bytes;
   a.cache_row_bytes = (int32_t)row_bytes;
-  {
-    uint32_t* ctr = reinterpret_cast<uint32_t*>(d.scratch + kNaCtrOff);
-    a.work_ctr = ctr + (size_t)d.parity * isk::kPoolCtrWords;
-    a.work_ctr_next = ctr + (size_t)(d.parity ^ 1) * isk::kPoolCtrWords;
-    d.parity ^= 1;
-  }
+  a.wait_ns = kWaitBudgetNs;
+  a.work_ctr = ctr;                              // zeroed by this call's plan kernel
+  a.work_ctr_next = ctr + isk::kPoolCtrWords;     // zeroed by the inject kernel, unused
   a.half_vecs = head_dim / 2 / ve;
   a.head_vecs = head_dim / ve;
   RopeTurns rt;

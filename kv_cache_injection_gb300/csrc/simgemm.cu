@@ -31,7 +31,6 @@ constexpr uint32_t kATile = 128 * kChunkK * 2;      // 16 KiB
 constexpr uint32_t kBTile = kGroupN * kChunkK * 2;  // 8 KiB
 constexpr uint32_t kStageBytes = kATile + kBTile;
 constexpr uint32_t kTmemCols = 64;
-constexpr uint64_t kGemmWaitNs = 2000000000ull;
 // kind::f16 instruction descriptor: D fp32 (bits 4-5 = 1), A and B fp16
 // (bits 7-9, 10-12 = 0), both K-major (bits 15, 16 = 0), N >> 3 at bits
 // 17-22, M >> 4 at bits 24-28.
@@ -98,14 +97,16 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
   return d;
 }
 
-// Bounded mbarrier wait that also gives up when another thread of the CTA
-// has flagged an abort.
-__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+// Bounded mbarrier wait (budget_ns; zero looks once) that also gives up when
+// another thread of the CTA has flagged an abort.
+__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                              uint64_t budget_ns) {
+  if (budget_ns == 0) return mbar_test_wait(bar, parity);
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   for (uint32_t it = 0; it < (1u << 26); ++it) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 255u) == 255u && (*abort_flag || global_timer_ns() - t0 > kGemmWaitNs)) return false;
+    if ((it & 255u) == 255u && (*abort_flag || global_timer_ns() - t0 > budget_ns)) return false;
   }
   return false;
 }
@@ -226,6 +227,8 @@ __global__ void __launch_bounds__(128, 1) sim_gemm_kernel(const __grid_constant_
   __shared__ __align__(8) uint64_t bar_done;
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
+  __shared__ int s_tile_full;                        // the MMA thread issued every chunk of this tile
+  __shared__ uint32_t s_kc_mma;                      // chunks the MMA thread has consumed so far
   __shared__ int s_tile, s_ti, s_pos, s_cnt, s_rows;
 
   pdl_wait();                                        // groups of the grouping kernel
@@ -279,7 +282,7 @@ __global__ void __launch_bounds__(128, 1) sim_gemm_kernel(const __grid_constant_
     if (warp == 0 && lane == 0) {                    // TMA producer
       for (int kc = 0; kc < nk; ++kc, ++kc_prod) {
         const uint32_t s = kc_prod % kGemmStages, ph = (kc_prod / kGemmStages) & 1u;
-        if (!wait_or_abort(smem_addr(&bar_empty[s]), ph ^ 1u, abort_flag)) {
+        if (!wait_or_abort(smem_addr(&bar_empty[s]), ph ^ 1u, abort_flag, g.wait_ns)) {
           *abort_flag = 1;
           break;
         }
@@ -289,9 +292,10 @@ __global__ void __launch_bounds__(128, 1) sim_gemm_kernel(const __grid_constant_
         tma_load_2d(sbase + s * kStageBytes + kATile, &tm_q, kc * kChunkK, pos, bar);
       }
     } else if (warp == 1 && lane == 0) {             // MMA issuer
+      const uint32_t kc_mma0 = kc_mma;
       for (int kc = 0; kc < nk; ++kc, ++kc_mma) {
         const uint32_t s = kc_mma % kGemmStages, ph = (kc_mma / kGemmStages) & 1u;
-        if (!wait_or_abort(smem_addr(&bar_full[s]), ph, abort_flag)) {
+        if (!wait_or_abort(smem_addr(&bar_full[s]), ph, abort_flag, g.wait_ns)) {
           *abort_flag = 1;
           break;
         }
@@ -302,19 +306,29 @@ __global__ void __launch_bounds__(128, 1) sim_gemm_kernel(const __grid_constant_
           mma_f16(tmem, sw128_desc(a0 + 32u * k), sw128_desc(b0 + 32u * k), (kc | k) != 0 ? 1u : 0u);
         mma_commit(smem_addr(&bar_empty[s]));
       }
+      // Arrives once every MMA issued so far has completed, whether or not
+      // the loop ran to the end.
       mma_commit(smem_addr(&bar_done));
+      s_tile_full = kc_mma == kc_mma0 + (uint32_t)nk;
+      s_kc_mma = kc_mma;
     }
     __syncwarp();
+    __syncthreads();
 
-    // Epilogue: warp w reads TMEM lanes 32w .. 32w+31 = tile rows.
-    const bool ok = wait_or_abort(smem_addr(&bar_done), n_done & 1u, abort_flag);
+    // Epilogue: warp w reads TMEM lanes 32w .. 32w+31 = tile rows.  The wait
+    // for the MMAs drains the tensor core before TMEM is read (or, after an
+    // abort, released), so it keeps the full budget and ignores the flag.
+    const bool done = __syncthreads_and(mbar_wait_bounded(smem_addr(&bar_done), n_done & 1u, kWaitBudgetNs));
     ++n_done;
     tc_fence_after();
+    const bool ok = done && s_tile_full;             // the same in every thread
     uint32_t acc[64];
-    tmem_ld_32x32b_x64(tmem + ((uint32_t)(32 * warp) << 16), acc);
-    tmem_wait_ld();
+    if (ok) {
+      tmem_ld_32x32b_x64(tmem + ((uint32_t)(32 * warp) << 16), acc);
+      tmem_wait_ld();
+    }
     const int r = 32 * warp + lane;
-    if (ok && !*abort_flag && r < nrows) {
+    if (ok && r < nrows) {
       const float inv_e = g.emb_inv_norm[(size_t)tile * 128 + r];
       float* out = g.scores + (size_t)ti * 128 + r;
 #pragma unroll
@@ -328,7 +342,15 @@ __global__ void __launch_bounds__(128, 1) sim_gemm_kernel(const __grid_constant_
     if (!ok && threadIdx.x == 0) latch(g.status, IS_ST_TIMEOUT);
     tc_fence_before();
     __syncthreads();
-    if (*abort_flag) break;
+    if (!ok || *abort_flag) break;
+  }
+  // After an abort the producer may have loads in flight that no MMA
+  // consumed (chunks s_kc_mma .. kc_prod - 1): they land before shared
+  // memory is released.
+  __syncthreads();
+  if (warp == 0 && lane == 0) {
+    for (uint32_t c = s_kc_mma; c < kc_prod; ++c)
+      mbar_wait_bounded(smem_addr(&bar_full[c % kGemmStages]), (c / kGemmStages) & 1u, kWaitBudgetNs);
   }
   __syncthreads();
   if (warp == 0) tmem_dealloc(tmem, kTmemCols);

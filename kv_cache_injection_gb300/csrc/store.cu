@@ -175,6 +175,7 @@ struct is_store {
   alignas(64) unsigned char map_q[128];
   bool batched_ok = false;
   int32_t retrieval_mode = IS_RETRIEVAL_AUTO;
+  uint64_t wait_ns = kWaitBudgetNs;   // budget of each pipeline wait (is_set_wait_budget)
   // segment plan of the last injecting call (reused by is_inject_layer)
   int32_t plan_R = 0;
   const int32_t* plan_seg_len = nullptr;
@@ -908,6 +909,7 @@ static is_status_t run_retrieval(is_store_t* s, int32_t Q, const int32_t* users,
   gg.score_stride = s->score_stride;
   gg.E = s->cfg.emb_dim;
   gg.status = s->status;
+  gg.wait_ns = s->wait_ns;
   const LaunchCfg dep{stream, s->num_sms, true};
   {
     StageTimer tm(s, IS_STAGE_PLAN, stream);
@@ -991,6 +993,7 @@ static is_status_t launch_injection(is_store_t* s, int32_t R, const int64_t* ids
   a.layer_stride = layer_stride;
   a.row_bytes = (int32_t)s->row_bytes;
   a.cache_row_bytes = (int32_t)cache_row_bytes(s, cache);
+  a.wait_ns = s->wait_ns;
   a.work_ctr = s->work_ctr + (size_t)s->work_parity * kPoolCtrWords;
   a.work_ctr_next = s->work_ctr + (size_t)(s->work_parity ^ 1) * kPoolCtrWords;
   a.k_inv = (float)(1.0 / (double)cache->k_scale);
@@ -1274,6 +1277,14 @@ is_status_t is_set_retrieval_mode(is_store_t* s, int32_t mode) {
   if (mode == IS_RETRIEVAL_BATCHED && !s->batched_ok)
     return fail(IS_ERR_UNSUPPORTED, "the batched path needs fp16 embeddings and tensor maps");
   s->retrieval_mode = mode;
+  return IS_OK;
+}
+
+is_status_t is_set_wait_budget(is_store_t* s, int64_t budget_ns) {
+  if (!s) return fail(IS_ERR_INVALID_ARG, "NULL store");
+  if (budget_ns < 0 || budget_ns > (int64_t)kWaitBudgetNs)
+    return fail(IS_ERR_INVALID_ARG, "budget_ns must be in [0, %llu]", (unsigned long long)kWaitBudgetNs);
+  s->wait_ns = (uint64_t)budget_ns;
   return IS_OK;
 }
 
