@@ -113,93 +113,57 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, vol
 
 // ---- query grouping -------------------------------------------------------------
 
-// One CTA of 1024 threads: sorts (user, query) pairs, cuts each user's run of
-// queries into groups of at most kGroupN, numbers the (group, tile) work
-// items, packs the queries in group order and computes their inverse norms.
-__global__ void __launch_bounds__(1024) group_kernel(const GroupArgs a) {
-  __shared__ unsigned long long key[IS_MAX_QUERIES];
+// The call's queries in (user, query index) order, cut into groups of at most
+// kGroupN queries of one user, with the (group, tile) work items numbered.
+// Grid of ceil(Q / 32) CTAs of 1024 threads, one warp per query: every CTA
+// stages the validated user of each of the Q queries in shared memory, and a
+// warp finds its query's position in that order by counting the queries that
+// precede it (a rank, no sort), then packs the query's fp16 row there and
+// computes its inverse norm.  CTA 0 also places each query's user at its
+// position and, one thread per position, finds where each user's run starts
+// and ends and writes the group table.  The row copies of all warps and the
+// user records of all group starts are loaded in parallel, so the grouping
+// costs a few load latencies, not a pass over the rows.
+constexpr int kGroupThreads = 1024;
+constexpr int kGroupWarps = kGroupThreads / 32;
+static_assert(kGroupThreads >= IS_MAX_QUERIES, "CTA 0 takes one thread per query position");
+
+__global__ void __launch_bounds__(kGroupThreads) group_kernel(const GroupArgs a) {
+  __shared__ uint32_t s_user[IS_MAX_QUERIES];      // validated user of query i; 0xFFFFFFFF = unknown
+  __shared__ uint32_t s_sorted[IS_MAX_QUERIES];    // CTA 0: user at each position of the order
   __shared__ int32_t scratch[33];
   pdl_trigger();
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int Q = a.Q;
-  // The query rows are packed after the sort: pull them into L2 now, one
-  // 128-byte line per thread and pass, so their latency hides under the sort.
-  {
-    const size_t lines = ((size_t)Q * a.E * 2 + 127) / 128;
-    const uint8_t* base = reinterpret_cast<const uint8_t*>(a.q_emb);
-    for (size_t i = tid; i < lines; i += blockDim.x) prefetch_l2(base + i * 128);
-  }
-  int P = 1;
-  while (P < Q) P <<= 1;
-  for (int i = tid; i < P; i += blockDim.x) {
-    uint32_t u = 0xFFFFFFFFu;                        // unknown users sort last, form no group
-    if (i < Q) {
-      const int32_t uu = a.users[i];
-      if (uu >= 0 && uu < a.max_users) {
-        u = (uint32_t)uu;
-        prefetch_l2(a.user_meta + uu);               // read after the sort
-      } else {
-        latch(a.status, IS_ST_USER_RANGE);
-      }
+  const int q = blockIdx.x * kGroupWarps + warp;
+  // The query row does not depend on the order: start pulling it now.
+  const __half* src_row = reinterpret_cast<const __half*>(a.q_emb) + (size_t)(q < Q ? q : 0) * a.E;
+  if (q < Q && lane * 64 < a.E * 2) prefetch_l2(reinterpret_cast<const uint8_t*>(src_row) + lane * 64);
+  for (int i = tid; i < Q; i += kGroupThreads) {
+    const int32_t uu = a.users[i];
+    const bool ok = uu >= 0 && uu < a.max_users;
+    if (ok) {
+      if (blockIdx.x == 0) prefetch_l2(a.user_meta + uu);   // CTA 0 reads it after the order
+    } else if (blockIdx.x == 0) {
+      latch(a.status, IS_ST_USER_RANGE);
     }
-    key[i] = i < Q ? (((unsigned long long)u << 32) | (uint32_t)i) : ~0ull;
+    s_user[i] = ok ? (uint32_t)uu : 0xFFFFFFFFu;   // unknown users sort last and form no group
   }
   __syncthreads();
-  for (int size = 2; size <= P; size <<= 1) {
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      for (int i = tid; i < P / 2; i += blockDim.x) {
-        const int lo = 2 * i - (i & (stride - 1));
-        const int hi = lo + stride;
-        const bool asc = (lo & size) == 0;
-        const unsigned long long x = key[lo], y = key[hi];
-        if ((x > y) == asc) {
-          key[lo] = y;
-          key[hi] = x;
-        }
-      }
-      __syncthreads();
+  auto rank_of = [&](int i, uint32_t ui) {          // whole warp; every lane returns the rank
+    uint32_t r = 0;
+    for (int j = lane; j < Q; j += 32) {
+      const uint32_t uj = s_user[j];
+      r += (uj < ui || (uj == ui && j < i)) ? 1u : 0u;
     }
-  }
-  // Thread p looks at sorted position p (Q <= blockDim).
-  const int p = tid;
-  const uint32_t u = p < Q ? (uint32_t)(key[p] >> 32) : 0xFFFFFFFFu;
-  int32_t is_start = 0, count = 0, ntiles = 0;
-  if (u != 0xFFFFFFFFu) {
-    // first and one-past-last positions of user u's run (binary searches)
-    const unsigned long long lo_key = (unsigned long long)u << 32;
-    int lo = 0, hi = p;
-    while (lo < hi) {
-      const int mid = (lo + hi) >> 1;
-      if (key[mid] < lo_key) lo = mid + 1; else hi = mid;
-    }
-    const int first = lo;
-    lo = p;
-    hi = Q;
-    while (lo < hi) {
-      const int mid = (lo + hi) >> 1;
-      if ((uint32_t)(key[mid] >> 32) == u) lo = mid + 1; else hi = mid;
-    }
-    const int end = lo;
-    if ((p - first) % kGroupN == 0) {
-      is_start = 1;
-      count = min(kGroupN, end - p);
-      ntiles = a.user_meta[u].y;
-    }
-  }
-  int32_t n_groups, n_items;
-  const int32_t gidx = block_exclusive_scan(is_start, scratch, &n_groups);
-  const int32_t item_base = block_exclusive_scan(ntiles, scratch, &n_items);
-  if (is_start) a.groups[gidx] = make_int4((int32_t)u, p, count, item_base);
-  if (p < Q) a.qperm[p] = (int32_t)(key[p] & 0xFFFFFFFFu);
-  if (tid == 0) {
-    a.counts[0] = n_groups;
-    a.counts[1] = n_items;
-  }
-  // Pack the queries in group order with their inverse norms (a warp per query).
-  const int warp = tid >> 5, lane = tid & 31, nwarps = blockDim.x >> 5;
-  for (int pp = warp; pp < Q; pp += nwarps) {
-    const int q = (int)(key[pp] & 0xFFFFFFFFu);
-    const uint4* src = reinterpret_cast<const uint4*>(reinterpret_cast<const __half*>(a.q_emb) + (size_t)q * a.E);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) r += __shfl_xor_sync(0xffffffffu, r, o);
+    return (int)r;
+  };
+  if (q < Q) {
+    const int pp = rank_of(q, s_user[q]);
+    if (blockIdx.x == 0 && lane == 0) s_sorted[pp] = s_user[q];
+    const uint4* src = reinterpret_cast<const uint4*>(src_row);
     uint4* dst = reinterpret_cast<uint4*>(a.qg + (size_t)pp * a.E);
     float ss = 0.f;
     for (int c = lane; c < a.E / 8; c += 32) {
@@ -212,7 +176,48 @@ __global__ void __launch_bounds__(1024) group_kernel(const GroupArgs a) {
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-    if (lane == 0) a.q_inv[pp] = ss > 0.f ? 1.0f / sqrtf(ss) : 0.f;
+    if (lane == 0) {
+      a.q_inv[pp] = ss > 0.f ? 1.0f / sqrtf(ss) : 0.f;
+      a.qperm[pp] = q;
+    }
+  }
+  if (blockIdx.x != 0) return;
+
+  // CTA 0: the users of the queries the other CTAs packed, in position order ...
+  for (int i = kGroupWarps + warp; i < Q; i += kGroupWarps) {
+    const uint32_t ui = s_user[i];
+    const int r = rank_of(i, ui);
+    if (lane == 0) s_sorted[r] = ui;
+  }
+  __syncthreads();
+  // ... then thread p looks at position p.
+  const int p = tid;
+  const uint32_t u = p < Q ? s_sorted[p] : 0xFFFFFFFFu;
+  int32_t is_start = 0, count = 0, ntiles = 0;
+  if (u != 0xFFFFFFFFu) {
+    int lo = 0, hi = p;                             // first position of u's run
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (s_sorted[mid] < u) lo = mid + 1; else hi = mid;
+    }
+    if ((p - lo) % kGroupN == 0) {
+      int end = p, ehi = Q;                         // one past the run's last position
+      while (end < ehi) {
+        const int mid = (end + ehi) >> 1;
+        if (s_sorted[mid] == u) end = mid + 1; else ehi = mid;
+      }
+      is_start = 1;
+      count = min(kGroupN, end - p);
+      ntiles = a.user_meta[u].y;
+    }
+  }
+  int32_t n_groups, n_items;
+  const int32_t gidx = block_exclusive_scan(is_start, scratch, &n_groups);
+  const int32_t item = block_exclusive_scan(ntiles, scratch, &n_items);
+  if (is_start) a.groups[gidx] = make_int4((int32_t)u, p, count, item);
+  if (tid == 0) {
+    a.counts[0] = n_groups;
+    a.counts[1] = n_items;
   }
 }
 
@@ -406,7 +411,8 @@ bool make_operand_map(void* map_out, const void* base, int E, int64_t rows, int 
 size_t operand_map_bytes() { return sizeof(CUtensorMap); }
 
 cudaError_t launch_group(const GroupArgs& ga, const LaunchCfg& cfg) {
-  return launch_ex(group_kernel, dim3(1), dim3(1024), 0, cfg.stream, cfg.pdl, ga);
+  const int grid = std::max(1, (ga.Q + kGroupWarps - 1) / kGroupWarps);
+  return launch_ex(group_kernel, dim3(grid), dim3(kGroupThreads), 0, cfg.stream, cfg.pdl, ga);
 }
 
 cudaError_t launch_sim_gemm(const GemmArgs& gg, const void* map_emb, const void* map_q, int Q,
