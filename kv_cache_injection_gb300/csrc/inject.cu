@@ -202,16 +202,23 @@ __device__ __forceinline__ int32_t segment_prefix(const InjectArgs& a, int32_t* 
 
 // One warp pulls block-table lines into L1: up to kBtLines 128-byte lines in
 // all, split evenly over the requests (at least one each for the first
-// kBtLines), each request's from the line of its first position on.
+// kBtLines).  Rows that fit their share are taken whole; longer ones from the
+// line of the request's first position on, which costs the warp a dependent
+// read of the start first (a delay of its own first item when no dependency
+// wait hides it).
 constexpr int kBtLines = 128;
 __device__ __forceinline__ void prefetch_block_rows(const InjectArgs& a, int lane) {
   if (!a.block_table || a.R <= 0) return;
   const int per = max(1, kBtLines / a.R);
   const int row_lines = (a.max_blocks + 31) >> 5;
+  const bool whole = row_lines <= per;
   for (int i = lane; i < kBtLines && i < a.R * per; i += 32) {
     const int r = i / per;
-    const int start = a.seg_start[r];
-    const int line = (start >= 0 ? start / a.block_size : 0) / 32 + i % per;
+    int line = i % per;
+    if (!whole) {
+      const int start = a.seg_start[r];
+      line += (start >= 0 ? start / a.block_size : 0) / 32;
+    }
     if (line < row_lines) prefetch_l1(a.block_table + (size_t)r * a.max_blocks + (size_t)line * 32);
   }
 }
