@@ -89,11 +89,23 @@ def inject_source_hash() -> str:
         return hashlib.sha256(f.read()).hexdigest()[:16]
 
 
+def library_source_hash() -> str:
+    """Hash of every source file the library is built from, and of this file."""
+    h = hashlib.sha256()
+    csrc = os.path.dirname(INJECT_SRC)
+    files = sorted(os.path.join(csrc, f) for f in os.listdir(csrc)) + [
+        os.path.join(ROOT, "include", "injectscale.h"), os.path.abspath(__file__)]
+    for path in files:
+        with open(path, "rb") as f:
+            h.update(os.path.basename(path).encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
 def ncu_traffic_per_token_layer(key: str):
     """DRAM bytes per injected token and layer from the committed ncu summary
-    for this workload, cache type and placement (key "workload/cache
-    dtype/placement"), if it was taken on the current inject kernel source;
-    else None."""
+    for this workload, budget k, cache type and placement (key
+    "workload/k<k>/cache dtype/placement"), if it was taken on the current
+    inject kernel source; else None."""
     if not os.path.exists(TRAFFIC_FILE):
         return None
     with open(TRAFFIC_FILE) as f:
@@ -344,7 +356,7 @@ def run_ours(args, rank, world, local_rank):
         inject_bytes = (per_tok + per_tok_w) * tokens_per_step  # read + write per launch
         inject_ms = stage_ms["inject"] / max(1, stage_n["inject"])
         achieved = inject_bytes / (inject_ms * 1e-3) / 1e9
-        traffic_tl = ncu_traffic_per_token_layer(f"{s.name}/{cache_dtype}/{args.kv_placement}")
+        traffic_tl = ncu_traffic_per_token_layer(f"{s.name}/k{s.k}/{cache_dtype}/{args.kv_placement}")
         emb_bytes = 0
         for u in np.unique(wl.users):
             emb_bytes += int((wl.fact_user == u).sum()) * s.emb_dim * (2 if s.emb_dtype == "f16" else 4)
@@ -381,6 +393,14 @@ def run_ours(args, rank, world, local_rank):
                 "algorithmic_bytes": inject_bytes,
                 "avg_launch_ms": inject_ms,
             }
+            if roofline["traffic"]:
+                # What DRAM saw during the launch: writes still in L2 when the
+                # launch ends are written back later (during the flush), so
+                # this is below the algorithmic rate whenever the cache tail
+                # fits in L2.
+                dram = roofline["traffic"] / (inject_ms * 1e-3) / 1e9
+                roofline["dram_achieved"] = dram
+                roofline["dram_frac"] = dram / peaks["hbm_gbs"]
         roofline["timing"] = (f"CUDA events around each inject launch over {stage_steps} steps of the "
                               "same workload right after the timed region (events between kernels "
                               "disable launch overlap, so this duration includes the launch gap)")
@@ -423,9 +443,11 @@ def run_ours(args, rank, world, local_rank):
                     "d2h_bytes_per_step": d2h},
             "gpu_launches": gpu_launches,
             "clocks": clocks.summary(),
+            "source_sha16": library_source_hash(),
         }
         if args.cpu_baseline:
-            result["cpu_baseline"] = cpu_baseline(wl, budget_s=args.cpu_budget)
+            result["cpu_baseline"] = cpu_baseline(wl, budget_s=args.cpu_budget,
+                                                  tokens_per_step=tokens_per_step)
     store.destroy()
     return result
 
@@ -538,7 +560,10 @@ def run_layerwise(args, rank, world, local_rank):
             "roofline": {"bound": "hbm", "kernel": f"inject, {G} layer(s) per launch", "achieved": achieved,
                          "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
                          "algorithmic_bytes": layer_bytes, "traffic": None},
-            "clocks": clocks.summary()}
+            "clocks": clocks.summary(),
+            "source_sha16": library_source_hash(),
+            "cpu_baseline": (cpu_baseline(wl, budget_s=args.cpu_budget, tokens_per_step=tokens)
+                             if args.cpu_baseline and rank == 0 else None)}
 
 
 def run_capture(args, rank, world, local_rank):
@@ -624,7 +649,10 @@ def run_capture(args, rank, world, local_rank):
             "roofline": {"bound": "hbm", "kernel": "capture_layer (one layer per launch)", "achieved": achieved,
                          "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
                          "algorithmic_bytes": layer_bytes, "traffic": None},
-            "clocks": clocks.summary()}
+            "clocks": clocks.summary(),
+            "source_sha16": library_source_hash(),
+            "cpu_baseline": (cpu_baseline_capture(s, lengths, args.window, fact_tokens, budget_s=args.cpu_budget)
+                             if args.cpu_baseline and rank == 0 else None)}
 
 
 # ----------------------------------------------------------------------------- oracle arm
@@ -683,26 +711,28 @@ def _host_cache(wl):
 _ONE_THREAD = ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS")
 
 
-def _oracle_worker(spec, max_facts, warmup, steps, budget_s, barrier, out_q):
+def _oracle_worker(spec, max_facts, warmup, steps, budget_s, barrier, out_q, queries=(0,)):
     """One oracle process: build the workload from its spec, warm up, wait for
-    the others, then run ``steps`` oracle steps (or until ``budget_s``)."""
+    the others, then run ``steps`` oracle steps (or until ``budget_s``), step i
+    on query queries[i % len(queries)]."""
     from synth import workloads
     wl = workloads.generate(spec)
-    _prefetch_facts(wl, 0, max_facts)
+    for q in queries:
+        _prefetch_facts(wl, q, max_facts)
     cache = _host_cache(wl)()
-    for _ in range(warmup):
-        oracle_step(wl, 0, max_facts, lambda: cache)
+    for i in range(warmup):
+        oracle_step(wl, queries[i % len(queries)], max_facts, lambda: cache)
     barrier.wait()
     t0 = time.monotonic()
     tokens = reps = 0
     while reps < steps and (budget_s is None or time.monotonic() - t0 < budget_s):
-        tokens += oracle_step(wl, 0, max_facts, lambda: cache)
+        tokens += oracle_step(wl, queries[reps % len(queries)], max_facts, lambda: cache)
         reps += 1
     out_q.put((tokens, reps, t0, time.monotonic()))
 
 
 def oracle_pool(spec, max_facts: int, workers: int, steps: list[int], warmup: int = 1,
-                budget_s: float | None = None) -> dict:
+                budget_s: float | None = None, queries=(0,)) -> dict:
     """Run the oracle in ``workers`` spawned processes at once (each with its
     BLAS held to one thread, so ``workers`` is the number of threads used).
     Worker i runs ``steps[i]`` steps; the rate is all tokens over the span from
@@ -714,7 +744,8 @@ def oracle_pool(spec, max_facts: int, workers: int, steps: list[int], warmup: in
     os.environ.update({v: "1" for v in _ONE_THREAD})
     try:
         procs = [ctx.Process(target=_oracle_worker,
-                             args=(spec, max_facts, warmup, steps[i], budget_s, barrier, out_q))
+                             args=(spec, max_facts, warmup, steps[i], budget_s, barrier, out_q,
+                                   tuple(queries)))
                  for i in range(workers)]
         for p in procs:
             p.start()
@@ -742,24 +773,75 @@ def host_cores() -> int:
         return os.cpu_count() or 1
 
 
-def cpu_baseline(wl, budget_s: float = 20.0, max_facts: int = 10) -> dict:
-    """Time the oracle, as it stands, on a bounded sample of the workload: the
-    retrieval of query 0 over its user's store plus rotation and scatter of its
-    first ``max_facts`` retrieved facts, repeated (at most 50 times or about
-    ``budget_s``) in one process with one thread, then in one process per host
-    core at once."""
-    n_user = int((wl.fact_user == wl.users[0]).sum())
-    what = (f"cosine top-{wl.spec.k} over {n_user} facts + fp64 RoPE/scatter of the first "
-            f"{max_facts} retrieved facts")
-    one = oracle_pool(wl.spec, max_facts, 1, [50], budget_s=budget_s)
+def cpu_baseline(wl, budget_s: float = 20.0, max_facts: int = 10, tokens_per_step: int | None = None,
+                 n_sample_queries: int = 4) -> dict:
+    """Time the oracle, as it stands, on a bounded sample of the workload: per
+    sampled query, the retrieval over its user's store plus rotation and
+    scatter of its first ``max_facts`` retrieved facts, repeated (at most 50
+    times or about ``budget_s``) in one process with one thread, then in one
+    process per host core at once.  A workload of one query samples that
+    query; with more, a seeded random subset of ``n_sample_queries`` of them,
+    taken in turn.  The rate is per injected token, so the time the oracle
+    would take for the whole step is an extrapolation, labelled as such."""
+    Q = int(wl.spec.n_queries)
+    if Q == 1:
+        queries = [0]
+    else:
+        queries = sorted(np.random.default_rng(12345).choice(Q, size=min(n_sample_queries, Q),
+                                                             replace=False).tolist())
+    n_user = [int((wl.fact_user == wl.users[q]).sum()) for q in queries]
+    what = (f"cosine top-{wl.spec.k} over the user's {n_user[0] if len(set(n_user)) == 1 else n_user} "
+            f"facts + fp64 RoPE/scatter of the first {max_facts} retrieved facts")
+    if Q > 1:
+        what = f"queries {queries} of {Q} (seeded random subset) in turn, each: " + what
+    one = oracle_pool(wl.spec, max_facts, 1, [50], budget_s=budget_s, queries=queries)
     cores = host_cores()
-    many = oracle_pool(wl.spec, max_facts, cores, [50] * cores, budget_s=budget_s)
-    return {"value": one["value"], "unit": "tokens/s", "cores": 1, "kind": "oracle",
-            "sample": (f"{one['reps']} x ({what}); {one['tokens']} tokens in {one['wall_s']:.1f} s, "
-                       f"numpy fp64, 1 process, BLAS on 1 thread"),
-            "all_cores": {"value": many["value"], "unit": "tokens/s", "cores": cores,
-                          "sample": (f"{cores} processes at once, each {many['reps'] // cores} x the "
-                                     f"same sample; {many['tokens']} tokens in {many['wall_s']:.1f} s")}}
+    many = oracle_pool(wl.spec, max_facts, cores, [50] * cores, budget_s=budget_s, queries=queries)
+    out = {"value": one["value"], "unit": "tokens/s", "cores": 1, "kind": "oracle",
+           "sample": (f"{one['reps']} x ({what}); {one['tokens']} tokens in {one['wall_s']:.1f} s, "
+                      f"numpy fp64, 1 process, BLAS on 1 thread"),
+           "all_cores": {"value": many["value"], "unit": "tokens/s", "cores": cores,
+                         "sample": (f"{cores} processes at once, each {many['reps'] // cores} x the "
+                                    f"same sample; {many['tokens']} tokens in {many['wall_s']:.1f} s")}}
+    if tokens_per_step:
+        out["extrapolated_s_per_step"] = {
+            "cores_1": tokens_per_step / one["value"], "all_cores": tokens_per_step / many["value"],
+            "note": (f"the step's {tokens_per_step} injected tokens at the sampled per-token rate: "
+                     "an extrapolation, not a measurement of the whole step")}
+    return out
+
+
+def cpu_baseline_capture(spec, lengths, window: int, fact_tokens: int, budget_s: float = 20.0,
+                         sample_facts: int = 64) -> dict:
+    """Time the oracle's capture step, as it stands, on a bounded sample: for
+    each of the first ``sample_facts`` facts, an engine layer output of its
+    [window || fact] sequence (seeded values) for every layer, from which
+    oracle.cwe.capture keeps the fact's rows; one process, one thread.  The
+    rate is per captured fact token over all layers, and the time for the
+    whole capture is an extrapolation, labelled as such."""
+    from oracle import cwe
+    rng = np.random.default_rng(7)
+    L, H, D = spec.num_layers, spec.num_kv_heads, spec.head_dim
+    seqs = []
+    for n in lengths[:sample_facts]:
+        T = int(n) + int(window)
+        kv = [(rng.standard_normal((T, H, D)), rng.standard_normal((T, H, D))) for _ in range(L)]
+        seqs.append((kv, int(window)))
+    toks = reps = 0
+    t0 = time.monotonic()
+    while reps < 50 and time.monotonic() - t0 < budget_s:
+        for kv, wl_ in seqs:
+            K, V = cwe.capture(kv, wl_)
+            toks += K.shape[0]
+        reps += 1
+    wall = time.monotonic() - t0
+    value = toks / wall
+    return {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": (f"{reps} x oracle.cwe.capture over {len(seqs)} facts' [window ({window} tokens) || fact] "
+                       f"layer outputs, {L} layers x {H} x {D} fp64; {toks} fact tokens in {wall:.1f} s, "
+                       "1 process"),
+            "extrapolated_s_per_step": {"cores_1": fact_tokens / value,
+                                        "note": "the capture's fact tokens at the sampled rate: an extrapolation"}}
 
 
 def run_reference(args, rank, world):
