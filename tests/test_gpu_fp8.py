@@ -62,9 +62,10 @@ def test_fp8_cache_llama31_8b(api):
     wl = workloads.get("llama31_8b")
     store = staging.load_store(wl, api)
     try:
-        st = gh.check_fused_workload(api, wl, store, sample_tokens=200, cache_dtype="e4m3",
-                                     k_scale=0.5, v_scale=0.75)
+        st = gh.check_fused_workload(api, wl, store, cache_dtype="e4m3", k_scale=0.5, v_scale=0.75,
+                                     all_tokens=True)
         assert st["tokens"] > 50 * 10
+        assert st["n"] == st["tokens"] * wl.spec.token_elems      # every injected key element
     finally:
         store.destroy()
 

@@ -77,8 +77,9 @@ def test_host_store_llama31_8b(api):
     wl = workloads.get("llama31_8b")
     host = staging.load_store(wl, api, kv_placement="host")
     try:
-        st = gh.check_fused_workload(api, wl, host, sample_tokens=200)
+        st = gh.check_fused_workload(api, wl, host, all_tokens=True)
         assert st["tokens"] > 50 * 10
+        assert st["n"] == st["tokens"] * wl.spec.token_elems      # every injected key element
     finally:
         host.destroy()
 

@@ -5,8 +5,10 @@ At these sizes the oracle checks every query's top-k, every request's segment
 length and every slot of the slot mapping; every cache row is checked on the
 device to have changed exactly when its slot was targeted.  The injected
 tokens are compared element by element with the oracle: all of them for the
-Llama-3.1-8B request and for one Qwen2.5-7B user, a sample (first and last
-token of every segment plus random ones, all layers and heads) elsewhere.
+single-request workloads (Llama-3.1-8B, the Mistral-7B k sweep, Qwen3-14B) and
+for one Qwen2.5-7B user; a sample (first and last token of every segment plus
+random ones, all layers and heads) for the other 99 users and for the capacity
+workload's 320 000 tokens.
 """
 import pytest
 
@@ -60,8 +62,9 @@ class TestMistralKSweep:
     @pytest.mark.parametrize("k", [5, 10, 20, 50])
     def test_k(self, api, loaded, k):
         wl, store = loaded
-        st = gh.check_fused_workload(api, wl, store, k=k, sample_tokens=60, seed=k)
+        st = gh.check_fused_workload(api, wl, store, k=k, all_tokens=True)
         assert st["tokens"] >= 10 * k
+        assert st["n"] == st["tokens"] * wl.spec.token_elems
 
 
 class TestQwen100Users:
@@ -105,8 +108,9 @@ class TestQwen3_14B:
 
     def test_fused_parity(self, api, loaded):
         wl, store = loaded
-        st = gh.check_fused_workload(api, wl, store, sample_tokens=200)
+        st = gh.check_fused_workload(api, wl, store, all_tokens=True)
         assert st["tokens"] > 50 * 10
+        assert st["n"] == st["tokens"] * wl.spec.token_elems
 
 
 @pytest.mark.slow
