@@ -238,6 +238,29 @@ __device__ __forceinline__ void st_v2(void* ptr, const uint2& v) {
 // element 0 in the lowest byte): one fp32 multiply each, then the hardware
 // conversion, which rounds to nearest even and saturates to +-448.  With
 // r == 1 (the usual unit scale) the multiplies are exact no-ops and skipped.
+// Two fp32 values in one 64-bit register, and the Blackwell paired-lane
+// multiply and fused multiply-add on them: each lane is rounded to nearest
+// exactly as its scalar form (__fmul_rn, fmaf), in one instruction for both.
+__device__ __forceinline__ unsigned long long pk2(float a, float b) {
+  unsigned long long r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void upk2(unsigned long long r, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+}
+__device__ __forceinline__ unsigned long long mul2_rn(unsigned long long a, unsigned long long b) {
+  unsigned long long d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ unsigned long long fma2_rn(unsigned long long a, unsigned long long b,
+                                                      unsigned long long c) {
+  unsigned long long d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+
 __device__ __forceinline__ uint2 to_e4m3x8(const float* x, float r) {
   uint32_t w[4];
   if (r == 1.0f) {
@@ -245,10 +268,13 @@ __device__ __forceinline__ uint2 to_e4m3x8(const float* x, float r) {
     for (int e = 0; e < 4; ++e)
       w[e] = __nv_cvt_float2_to_fp8x2(make_float2(x[2 * e], x[2 * e + 1]), __NV_SATFINITE, __NV_E4M3);
   } else {
+    const unsigned long long rr = pk2(r, r);
 #pragma unroll
-    for (int e = 0; e < 4; ++e)
-      w[e] = __nv_cvt_float2_to_fp8x2(make_float2(__fmul_rn(x[2 * e], r), __fmul_rn(x[2 * e + 1], r)),
-                                      __NV_SATFINITE, __NV_E4M3);
+    for (int e = 0; e < 4; ++e) {
+      float a, b;
+      upk2(mul2_rn(pk2(x[2 * e], x[2 * e + 1]), rr), a, b);
+      w[e] = __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
+    }
   }
   return make_uint2(w[0] | (w[1] << 16), w[2] | (w[3] << 16));
 }

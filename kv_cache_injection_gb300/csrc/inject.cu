@@ -132,6 +132,21 @@ __device__ __forceinline__ void rotate_vec(const float* x, const float* z, bool 
   }
 }
 
+// NeoX rotation of one vector with the sines already signed for the lane's
+// half of the pair (sx = -sin for the first half, +sin for the second):
+// y = x cos + z sx, two lanes per instruction.  Each element is rounded
+// exactly as rotate_vec rounds it (-(z sin) is exact), so the two agree bit
+// for bit.
+template <int VE>
+__device__ __forceinline__ void rotate_neox_x2(const float* x, const float* z, const float* cs,
+                                               const float* sx, float* y) {
+#pragma unroll
+  for (int e = 0; e < VE; e += 2) {
+    const unsigned long long t = mul2_rn(pk2(z[e], z[e + 1]), pk2(sx[e], sx[e + 1]));
+    upk2(fma2_rn(pk2(x[e], x[e + 1]), pk2(cs[e], cs[e + 1]), t), y[e], y[e + 1]);
+  }
+}
+
 // Rotated key vector v of a row at dk: 16 bytes in the store's type, or 8
 // E4M3 bytes (times fp32(1 / k_scale)) for an FP8 cache.
 template <typename T, bool F8>
@@ -507,10 +522,16 @@ __global__ void __launch_bounds__(kInjectWarpsMax * 32) inject_kernel(const Inje
   }
   __syncwarp();
 
-  float cs[NF], sn[NF];
+  float cs[NF], sn[NF], sx[NF];
   int32_t cur_p = -1;
   bool aborted = false;
   int s = 0;
+  // NeoX with half a head under 32 vectors: vector v = c * 32 + lane is in the
+  // first half of its pair exactly when lane & half_vecs is 0, for every c, so
+  // each lane signs its sines once per position and rotates two lanes per
+  // instruction.
+  const bool paired = STYLE == 0 && (VE % 2) == 0 && hv < 32;
+  const bool lane_first = (lane & hv) == 0;
   for (int64_t i = 0; i < issued; ++i) {
     const StageMeta m = meta[s];
     if (m.slot >= 0) {
@@ -530,6 +551,7 @@ __global__ void __launch_bounds__(kInjectWarpsMax * 32) inject_kernel(const Inje
         for (int e = 0; e < NF; ++e) {
           const float fr = angle_turns(pf, rt.hi[fbase + e], rt.lo[fbase + e]);
           sincospif(2.0f * fr, &sn[e], &cs[e]);
+          sx[e] = lane_first ? -sn[e] : sn[e];
         }
       }
       for (int gl = 0; gl < m.nl; ++gl) {
@@ -542,7 +564,10 @@ __global__ void __launch_bounds__(kInjectWarpsMax * 32) inject_kernel(const Inje
           float x[VE], z[VE], y[VE];
           Vec<T>::unpack(ld_shared_v4(kst + v * 16), x);
           if (STYLE == 0) Vec<T>::unpack(ld_shared_v4(kst + (v ^ hv) * 16), z);
-          rotate_vec<T, STYLE>(x, z, (v & hv) == 0, cs, sn, y);
+          if (paired)
+            rotate_neox_x2<VE>(x, z, cs, sx, y);
+          else
+            rotate_vec<T, STYLE>(x, z, (v & hv) == 0, cs, sn, y);
           if (F8) {
             // 8-bit cache: V is converted on the way too (no bulk store).
             float xv[VE];
