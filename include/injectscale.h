@@ -375,6 +375,29 @@ is_status_t is_retrieve_and_inject_host(is_store_t* store, int32_t Q, const int3
                                         void* kv_cache, int64_t* ids_out_host, float* scores_out_host,
                                         int32_t* seg_len_out_host, cudaStream_t stream);
 
+/* ---- prepared host calls ------------------------------------------------------
+ * A serving loop that calls is_retrieve_and_inject_host on the same host
+ * buffers every time (their contents change, their addresses do not) can bind
+ * them once.  is_host_call_prepare checks and keeps every argument of the call,
+ * with copies of *rope and *cache.  is_host_call_run(call) then performs the
+ * call exactly as is_retrieve_and_inject_host would with those arguments,
+ * reading the buffers' current contents.  A run takes one argument, so a
+ * caller going through a foreign-function layer no longer pays to convert
+ * fifteen arguments on every request.  The bound buffers, the store, kv_cache
+ * and the stream must outlive the call object, and is_host_call_destroy frees
+ * it (the store is not touched).  Errors: prepare returns IS_ERR_INVALID_ARG
+ * or IS_ERR_OUT_OF_RANGE for the argument checks of is_retrieve_and_inject_host
+ * that need no device, and IS_ERR_OOM; run returns what that call returns. */
+typedef struct is_host_call is_host_call_t;
+is_status_t is_host_call_prepare(is_store_t* store, int32_t Q, const int32_t* users_host,
+                                 const void* q_emb_host, int32_t k, const int32_t* seg_start_host,
+                                 const is_rope_params_t* rope, const int32_t* block_table_host,
+                                 int32_t max_blocks_per_seq, const is_cache_desc_t* cache, void* kv_cache,
+                                 int64_t* ids_out_host, float* scores_out_host, int32_t* seg_len_out_host,
+                                 cudaStream_t stream, is_host_call_t** call_out);
+is_status_t is_host_call_run(is_host_call_t* call);
+is_status_t is_host_call_destroy(is_host_call_t* call);
+
 /* ---- is_inject_noalloc ------------------------------------------------------
  * The paper has no counterpart to this call; it exists for callers that
  * cannot allocate device memory: code whose device memory is all owned by

@@ -79,6 +79,11 @@ SIGNATURES = {
     "is_retrieve_and_inject_host": [c_void_p, c_int32, c_void_p, c_void_p, c_int32, c_void_p,
                                     POINTER(RopeParams), c_void_p, c_int32, POINTER(CacheDesc),
                                     c_void_p, c_void_p, c_void_p, c_void_p, c_void_p],
+    "is_host_call_prepare": [c_void_p, c_int32, c_void_p, c_void_p, c_int32, c_void_p,
+                             POINTER(RopeParams), c_void_p, c_int32, POINTER(CacheDesc),
+                             c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, POINTER(c_void_p)],
+    "is_host_call_run": [c_void_p],
+    "is_host_call_destroy": [c_void_p],
     "is_inject_noalloc": [c_void_p, c_int64, c_void_p, c_void_p, c_int64, c_int32, c_int32, c_int32,
                           c_int32, c_int32, c_int32, c_void_p, c_void_p, c_int32, c_void_p,
                           POINTER(RopeParams), c_void_p, c_int32, POINTER(CacheDesc), c_void_p,

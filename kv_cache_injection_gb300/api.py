@@ -233,25 +233,49 @@ def _hptr(a) -> int | None:
     return a.ctypes.data
 
 
-def prepare_retrieve_and_inject_host(store: Store, users, q_emb, k: int, seg_start, rope: RopeParams,
-                                     block_table, cache: CacheDesc, kv_cache, ids_out=None, scores_out=None,
-                                     seg_len_out=None, stream=None):
-    """is_retrieve_and_inject_host with every argument marshalled once: inputs
-    and outputs are host arrays (numpy or CPU tensors; contents may change
-    between calls), kv_cache a device tensor.  Returns a callable; each call is
-    synchronous and raises ISError on a non-OK status."""
-    fn = _lib.load().is_retrieve_and_inject_host
-    args = (c_void_p(store.handle), int(users.shape[0]), _hptr(users), _hptr(q_emb), int(k), _hptr(seg_start),
-            byref(rope), _hptr(block_table), int(block_table.shape[1]), byref(cache), _ptr(kv_cache),
-            _hptr(ids_out), _hptr(scores_out), _hptr(seg_len_out), _stream(stream))
-    keep = (rope, cache, users, q_emb, seg_start, block_table, ids_out, scores_out, seg_len_out)
+class HostCall:
+    """A prepared is_retrieve_and_inject_host (is_host_call_prepare): the
+    arguments are bound once, and each call runs the step on the buffers'
+    current contents through is_host_call_run, one pointer argument."""
 
-    def call():
-        st = fn(*args)
+    def __init__(self, handle: int, keep):
+        self._lib = _lib.load()
+        self._handle = c_void_p(handle)
+        self._run = self._lib.is_host_call_run
+        self._keep = keep                     # the bound arrays must outlive the handle
+
+    def __call__(self) -> None:
+        st = self._run(self._handle)
         if st != _lib.IS_OK:
             _check(st)
-        return keep is not None
-    return call
+
+    def close(self) -> None:
+        if self._handle:
+            self._lib.is_host_call_destroy(self._handle)
+            self._handle = c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:      # interpreter shutdown
+            pass
+
+
+def prepare_retrieve_and_inject_host(store: Store, users, q_emb, k: int, seg_start, rope: RopeParams,
+                                     block_table, cache: CacheDesc, kv_cache, ids_out=None, scores_out=None,
+                                     seg_len_out=None, stream=None) -> HostCall:
+    """is_retrieve_and_inject_host with every argument bound once
+    (is_host_call_prepare): inputs and outputs are host arrays (numpy or CPU
+    tensors; contents may change between calls), kv_cache a device tensor.
+    Returns a callable; each call is synchronous and raises ISError on a
+    non-OK status."""
+    out = c_void_p()
+    _check(_lib.load().is_host_call_prepare(
+        c_void_p(store.handle), int(users.shape[0]), _hptr(users), _hptr(q_emb), int(k), _hptr(seg_start),
+        byref(rope), _hptr(block_table), int(block_table.shape[1]), byref(cache), _ptr(kv_cache),
+        _hptr(ids_out), _hptr(scores_out), _hptr(seg_len_out), _stream(stream), byref(out)))
+    return HostCall(out.value, (store, users, q_emb, seg_start, block_table, ids_out, scores_out, seg_len_out,
+                                kv_cache))
 
 
 def is_retrieve_and_inject_host(store: Store, users, q_emb, k: int, seg_start, rope: RopeParams, block_table,

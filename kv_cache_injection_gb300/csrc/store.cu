@@ -6,6 +6,7 @@
 #include <cstdio>
 #include <cstring>
 #include <mutex>
+#include <new>
 #include <string>
 #include <vector>
 
@@ -1254,6 +1255,56 @@ is_status_t is_retrieve_and_inject_host(is_store_t* s, int32_t Q, const int32_t*
   if (ids_out) std::memcpy(ids_out, hout, (size_t)Q * k * 8);
   if (scores_out) std::memcpy(scores_out, hout + b_ids, (size_t)Q * k * 4);
   if (seg_len_out) std::memcpy(seg_len_out, hout + b_ids + b_sc, (size_t)Q * 4);
+  return IS_OK;
+}
+
+struct is_host_call {
+  is_store_t* s;
+  int32_t Q, k, max_blocks;
+  const int32_t* users;
+  const void* q_emb;
+  const int32_t* seg_start;
+  const int32_t* block_table;
+  is_rope_params_t rope;
+  is_cache_desc_t cache;
+  void* kv_cache;
+  int64_t* ids;
+  float* scores;
+  int32_t* seg_len;
+  cudaStream_t stream;
+};
+
+is_status_t is_host_call_prepare(is_store_t* s, int32_t Q, const int32_t* users, const void* q_emb, int32_t k,
+                                 const int32_t* seg_start, const is_rope_params_t* rope,
+                                 const int32_t* block_table, int32_t max_blocks, const is_cache_desc_t* cache,
+                                 void* kv_cache, int64_t* ids_out, float* scores_out, int32_t* seg_len_out,
+                                 cudaStream_t stream, is_host_call_t** call_out) {
+  if (!call_out) return fail(IS_ERR_INVALID_ARG, "call_out is NULL");
+  *call_out = nullptr;
+  if (!s) return fail(IS_ERR_INVALID_ARG, "NULL store");
+  if (Q < 1 || Q > s->cfg.max_queries)
+    return fail(IS_ERR_INVALID_ARG, "Q=%d outside [1, %d]", Q, s->cfg.max_queries);
+  if (k < 1 || k > s->cfg.max_k) return fail(IS_ERR_OUT_OF_RANGE, "k=%d outside [1, %d]", k, s->cfg.max_k);
+  if (!users || !q_emb || !seg_start || !block_table || !rope || !cache || !kv_cache)
+    return fail(IS_ERR_INVALID_ARG, "users, q_emb, seg_start, block_table, rope, cache or kv_cache is NULL");
+  if (max_blocks < 1) return fail(IS_ERR_INVALID_ARG, "max_blocks_per_seq=%d must be >= 1", max_blocks);
+  is_host_call_t* c = new (std::nothrow) is_host_call_t();
+  if (!c) return fail(IS_ERR_OOM, "host call object");
+  *c = is_host_call_t{s, Q, k, max_blocks, users, q_emb, seg_start, block_table, *rope, *cache, kv_cache,
+                      ids_out, scores_out, seg_len_out, stream};
+  *call_out = c;
+  return IS_OK;
+}
+
+is_status_t is_host_call_run(is_host_call_t* c) {
+  if (!c) return fail(IS_ERR_INVALID_ARG, "NULL host call");
+  return is_retrieve_and_inject_host(c->s, c->Q, c->users, c->q_emb, c->k, c->seg_start, &c->rope,
+                                     c->block_table, c->max_blocks, &c->cache, c->kv_cache, c->ids, c->scores,
+                                     c->seg_len, c->stream);
+}
+
+is_status_t is_host_call_destroy(is_host_call_t* c) {
+  delete c;
   return IS_OK;
 }
 

@@ -100,3 +100,20 @@ def test_binding_constants_match_the_header():
             assert getattr(_lib, name) == value, name
             checked += 1
     assert checked >= 6
+
+
+def test_host_call_prepare_checks_before_the_device(lib):
+    """is_host_call_prepare refuses a missing store or output slot, and
+    is_host_call_run a missing handle, without touching a device."""
+    out = ctypes.c_void_p()
+    rope = api.make_rope(1e4)
+    cache = api.make_cache_desc(16, 1, "bf16")
+    buf = np.zeros(4, dtype=np.int32)
+    p = buf.ctypes.data
+    assert lib.is_host_call_prepare(None, 1, p, p, 1, p, ctypes.byref(rope), p, 1, ctypes.byref(cache), p,
+                                    None, None, None, None, ctypes.byref(out)) == 1
+    assert out.value is None
+    assert lib.is_host_call_prepare(None, 1, p, p, 1, p, ctypes.byref(rope), p, 1, ctypes.byref(cache), p,
+                                    None, None, None, None, None) == 1
+    assert lib.is_host_call_run(None) == 1
+    assert lib.is_host_call_destroy(None) == 0
