@@ -147,3 +147,35 @@ def test_host_validation_errors(env):
                                                                  device="cuda"))
     assert e.value.status == 3
     assert api.is_get_status(store) == 0
+
+
+def test_bad_user_in_one_user_store():
+    """A store of one user, queried with users out of range next to valid
+    ones: each bad row gets the status bit and the empty result, and every
+    other row, call after call, still matches the oracle (the cosine bins
+    are left clean between calls)."""
+    import torch
+    from kv_cache_injection_gb300 import _lib
+    from kv_cache_injection_gb300 import api
+    gh.ensure_built()
+    wl = workloads.get("tiny")
+    store = staging.load_store(wl, api, max_queries=4)
+    try:
+        q = torch.from_numpy(np.repeat(wl.queries, 3, axis=0)).cuda()
+        k = wl.spec.k
+        for users, bad in (([0, 3, 0], {1}), ([-1, 0, 1], {0, 2}), ([0, 0, 0], set())):
+            u = torch.tensor(users, dtype=torch.int32, device="cuda")
+            ids = torch.full((3, k), -7, dtype=torch.int64, device="cuda")
+            sc = torch.zeros((3, k), dtype=torch.float32, device="cuda")
+            api.is_retrieve_topk(store, u, q, k, ids, sc)
+            bits = api.is_get_status(store)
+            assert bits == (_lib.IS_ST_USER_RANGE if bad else 0), hex(bits)
+            g, s = ids.cpu().numpy(), sc.cpu().numpy()
+            o_ids, o_sc, score_of = parity.oracle_retrieve(wl, 0, k)
+            for r in range(3):
+                if r in bad:
+                    assert np.all(g[r] == -1) and np.all(np.isneginf(s[r]))
+                else:
+                    parity.check_topk(g[r], s[r], o_ids, o_sc, score_of, k)
+    finally:
+        store.destroy()
