@@ -361,8 +361,14 @@ is_status_t is_retrieve_and_inject(is_store_t* store, int32_t Q, const int32_t* 
  * seg_len_out (int32[Q]) into the buffer, and the call copies them to the
  * caller's host arrays, which may each be NULL.  The store and the paged
  * cache stay on the device (kv_cache is a device pointer).  Synchronous:
- * returns once the outputs are in host memory, waiting by polling the stream
- * (the calling thread spins meanwhile).  The staging buffer belongs to the
+ * returns once the outputs are in host memory and every cache write of the
+ * call is complete; the calling thread spins meanwhile.  With the inputs in
+ * the mapped buffer it polls a word of mapped host memory that the inject
+ * kernel's last CTA sets when the work is done, so the kernel may still be
+ * retiring when the call returns: work on `stream` is ordered after it as
+ * usual, and work on another stream that must follow it should be ordered
+ * after `stream` (an event), not after the return alone.  With the inputs
+ * copied, it polls the stream.  The staging buffer belongs to the
  * store; a call that needs more than the last one had grows it (a
  * synchronisation and an allocation; IS_ERR_OOM if that fails,
  * IS_ERR_UNSUPPORTED if the device cannot address it at its host address).

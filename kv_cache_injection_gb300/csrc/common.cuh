@@ -59,6 +59,9 @@ struct InjectArgs {
   uint32_t* work_ctr;           // kPoolCtrs counters of pool claims in this launch (zero at its start)
   uint32_t* work_ctr_next;      // the counters of the next launch, zeroed by this one
   int32_t chunk_items;          // items per pool chunk (set by the launcher)
+  uint32_t* done_ctr;           // CTAs of this launch that have finished (zero between launches)
+  uint32_t* host_done;          // mapped host word the last CTA sets to done_seq, or null
+  uint32_t done_seq;
   int32_t per_layer;            // 1: layer l of this call is written to layer_cache[l]
   uint8_t* layer_cache[IS_MAX_LAYERS_PER_CALL];   // per_layer: each layer's own [2][nb][bs][H][D]
 };
@@ -114,6 +117,10 @@ struct PlanArgs {
 constexpr int kPoolCtrs = 16;
 constexpr int kCtrStride = 32;
 constexpr int kPoolCtrWords = kPoolCtrs * kCtrStride;
+// The store's counter block: two sets of pool counters, then the inject
+// kernel's CTA arrival counter of host-buffer calls on a line of its own.
+constexpr int kDoneCtrWord = 2 * kPoolCtrWords;
+constexpr int kCtrBlockWords = kDoneCtrWord + kCtrStride;
 
 // Uniform bins of the cosine in [-1, 1] used by the top-k's first pass.
 constexpr int kCosBins = 2048;

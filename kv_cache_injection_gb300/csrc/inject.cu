@@ -363,6 +363,26 @@ struct TokenCursor {
   }
 };
 
+// A host-buffer call learns that the launch's work is done from a word of
+// mapped host memory (a.host_done) rather than from the stream: once a CTA's
+// writes are complete it arrives on a.done_ctr, and the last CTA to arrive
+// resets the counter and stores a.done_seq into that word.  The calling
+// thread polls it and sees the store before the stream reports the grid
+// retired.  Every CTA reaches this point exactly once per launch (the kernels
+// have no early exit), so the counter is back at zero for the next launch.
+__device__ __forceinline__ void signal_host_done(const InjectArgs& a) {
+  if (a.host_done == nullptr) return;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    if (atomicAdd(a.done_ctr, 1u) == gridDim.x - 1) {
+      *a.done_ctr = 0u;
+      __threadfence_system();
+      *reinterpret_cast<volatile uint32_t*>(a.host_done) = a.done_seq;
+    }
+  }
+}
+
 template <typename T, int STYLE, bool F8>
 __global__ void __launch_bounds__(kInjectWarpsMax * 32) inject_kernel(const InjectArgs a,
                                                                       const RopeTurns rt, int P, int G) {
@@ -606,6 +626,7 @@ __global__ void __launch_bounds__(kInjectWarpsMax * 32) inject_kernel(const Inje
   }
   if (lane == 0) bulk_wait_all();
   __syncwarp();
+  signal_host_done(a);
 }
 
 // ---------------------------------------------------------------------------
@@ -703,6 +724,7 @@ __global__ void __launch_bounds__(kHostWarps * 32) inject_host_kernel(const Inje
         }
     }
   }
+  signal_host_done(a);
 }
 
 // ---------------------------------------------------------------------------

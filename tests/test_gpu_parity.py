@@ -360,6 +360,53 @@ def test_host_buffer_call_equals_device_call(api):
         store.destroy()
 
 
+def test_prepared_host_call_outputs_follow_each_call(api):
+    """A prepared host call run back to back, with the rows of users and
+    queries rotated between calls: each return hands back that call's ids,
+    scores and segment lengths.  On the mapped path the calling thread
+    returns on the completion word the inject kernel's last CTA writes, so
+    the retrieval's outputs must be in the buffer by then; a stale buffer
+    would return the previous rotation."""
+    wl = workloads.generate(SMALL_BF16)
+    s = wl.spec
+    store = staging.load_store(wl, api)
+    try:
+        out = gh.run_fused(api, store, wl, staging.device_inputs(wl), staging.canary_cache(wl))
+        assert out["status"] == 0
+        rope = staging.rope_params(wl, api)
+        cd = api.make_cache_desc(s.block_size, wl.num_blocks, s.kv_dtype)
+        edt = np.float16 if s.emb_dtype == "f16" else np.float32
+        Q, k = len(wl.users), s.k
+        base_users = np.array(wl.users, dtype=np.int32)          # copies: the bound arrays are rewritten
+        base_q = np.array(wl.queries, dtype=edt)
+        users = base_users.copy()
+        q = base_q.copy()
+        start = np.ascontiguousarray(wl.seg_start, dtype=np.int32)
+        bt = np.ascontiguousarray(wl.block_table, dtype=np.int32)
+        ids = np.empty((Q, k), dtype=np.int64)
+        sc = np.empty((Q, k), dtype=np.float32)
+        ln = np.empty(Q, dtype=np.int32)
+        call = api.prepare_retrieve_and_inject_host(store, users, q, k, start, rope, bt, cd,
+                                                    staging.canary_cache(wl), ids, sc, ln)
+        try:
+            for i in range(16):
+                r = (i * 3) % Q
+                np.copyto(users, np.roll(base_users, r))
+                np.copyto(q, np.roll(base_q, r, axis=0))
+                ids.fill(-5)
+                sc.fill(0.0)
+                ln.fill(-5)
+                call()
+                assert np.array_equal(ids, np.roll(out["ids"], r, axis=0)), (i, r)
+                assert np.array_equal(sc.view(np.uint32), np.roll(out["scores"], r, axis=0).view(np.uint32))
+                assert np.array_equal(ln, np.roll(out["seg_len"], r)), (i, r)
+        finally:
+            call.close()
+        assert api.is_get_status(store) == 0
+    finally:
+        store.destroy()
+
+
 @pytest.mark.parametrize("n", [4096, 4097, 6000])
 def test_per_query_topk_on_large_users(api, n):
     """The per-query retrieval kernel on users of 4096 facts (keys staged in
