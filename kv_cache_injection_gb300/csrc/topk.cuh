@@ -133,12 +133,21 @@ __device__ void topk_block(const TopkArgs& a, TopkShared& sh, uint32_t* s_keys, 
   if (reg) {
     // All n scores and this thread's bins in one round of loads; the bins are
     // then zeroed for the next call (this CTA is their only reader).
+    // A thread's bins hi - BPT + 1 .. hi are consecutive words, 16-byte
+    // aligned in groups of four: two vector loads and stores each.
+    static_assert(BPT % 4 == 0, "bins per thread in whole 16-byte groups");
     uint32_t* hg = a.hist + (size_t)q * kCosBins;
     load_batch(0);
 #pragma unroll
-    for (int i = 0; i < BPT; ++i) c[i] = __ldcg(hg + hi - i);
+    for (int i = 0; i < BPT; i += 4) {
+      const uint4 w = __ldcg(reinterpret_cast<const uint4*>(hg + hi - i - 3));
+      c[i] = w.w;
+      c[i + 1] = w.z;
+      c[i + 2] = w.y;
+      c[i + 3] = w.x;
+    }
 #pragma unroll
-    for (int i = 0; i < BPT; ++i) __stcg(hg + hi - i, 0u);
+    for (int i = 0; i < BPT; i += 4) __stcg(reinterpret_cast<uint4*>(hg + hi - i - 3), make_uint4(0u, 0u, 0u, 0u));
     if (tid == 0) sh.cnt = 0;
   } else {
     if (kk > 0) load_batch(0);
