@@ -189,6 +189,16 @@ __device__ void topk_block(const TopkArgs& a, TopkShared& sh, uint32_t* s_keys, 
     }
     int32_t tot;
     const uint32_t before = (uint32_t)block_exclusive_scan_1bar<kRetThreads / 32>((int32_t)sum, sh.scratch, &tot);
+    if (reg) {
+      // Rows in the bins above each of this thread's bins: a candidate's
+      // first free slot in bin order (the shared histogram is unused here).
+      uint32_t run = before;
+#pragma unroll
+      for (int i = 0; i < BPT; ++i) {
+        sh.hist[hi - i] = run;
+        run += c[i];
+      }
+    }
     if (before < (uint32_t)kk && before + sum >= (uint32_t)kk) {
       uint32_t run = before;
 #pragma unroll
@@ -209,21 +219,16 @@ __device__ void topk_block(const TopkArgs& a, TopkShared& sh, uint32_t* s_keys, 
     const int bstar = sh.bstar;
     C = sh.above + sh.eq;
     if (reg) {
-      // Scores in registers: mark this thread's candidates, one block scan
-      // gives its first slot.
-      uint32_t take = 0;
+      // Scores in registers: a candidate takes the next slot of its bin
+      // (bins hold their first slot, in descending bin order); the order
+      // within a bin does not matter, the ranking below counts.
 #pragma unroll
       for (int u = 0; u < kRegPer; ++u) {
         const int j = u * kRetThreads + tid;
-        if (j < n && cos_bin(v[u]) >= bstar) take |= 1u << u;
-      }
-      int32_t tot;
-      uint32_t slot = (uint32_t)block_exclusive_scan_1bar<kRetThreads / 32>((int32_t)__popc(take), sh.scratch2, &tot);
-#pragma unroll
-      for (int u = 0; u < kRegPer; ++u) {
-        if (take & (1u << u)) {
-          sh.sel[slot] = sel_entry(score_key(v[u]), (uint32_t)(u * kRetThreads + tid), slot);
-          ++slot;
+        const int b = cos_bin(v[u]);
+        if (j < n && b >= bstar) {
+          const uint32_t slot = atomicAdd(&sh.hist[b], 1u);
+          sh.sel[slot] = sel_entry(score_key(v[u]), (uint32_t)j, slot);
         }
       }
     } else if (SMEM_KEYS) {
