@@ -431,7 +431,7 @@ is_status_t is_host_call_destroy(is_host_call_t* call);
  * Other arguments as in is_inject (no user check).  Sizes beyond the limits
  * return IS_ERR_UNSUPPORTED before anything is enqueued.  The first call on a
  * device looks up the static array's device address (once per device, under
- * a lock); make that first call before any stream capture.  Every call uses
+ * a lock).  Every call uses
  * the same static array: its planning kernel writes the plan entries and
  * zeroes the work counters its injection kernel then uses, so a call depends
  * on nothing an earlier call left there, but two calls whose kernels overlap
