@@ -407,6 +407,54 @@ def test_prepared_host_call_outputs_follow_each_call(api):
         store.destroy()
 
 
+def test_host_call_with_nothing_to_inject(api):
+    """Host-buffer calls whose inject launch has no token to move: a user
+    without facts, then a user out of range.  Each call still returns (the
+    inject kernel's last CTA writes the completion word with no work done)
+    with the empty result and the cache untouched; the status bit comes only
+    with the bad user; the call after them matches the device call."""
+    import torch
+    from kv_cache_injection_gb300 import _lib
+    wl = workloads.generate(SMALL_BF16)
+    s = wl.spec
+    store = staging.load_store(wl, api, max_users=s.n_users + 1)      # the last user has no facts
+    try:
+        rope = staging.rope_params(wl, api)
+        cd = api.make_cache_desc(s.block_size, wl.num_blocks, s.kv_dtype)
+        edt = np.float16 if s.emb_dtype == "f16" else np.float32
+        k = s.k
+        q = np.array(wl.queries[:1], dtype=edt)
+        start = np.array(wl.seg_start[:1], dtype=np.int32)
+        bt = np.array(wl.block_table[:1], dtype=np.int32)
+        for user, bits in ((s.n_users, 0), (s.n_users + 7, _lib.IS_ST_USER_RANGE)):
+            cache = staging.canary_cache(wl)
+            ids = np.full((1, k), 5, dtype=np.int64)
+            sc = np.zeros((1, k), dtype=np.float32)
+            ln = np.full(1, 5, dtype=np.int32)
+            api.is_retrieve_and_inject_host(store, np.array([user], dtype=np.int32), q, k, start, rope, bt, cd,
+                                            cache, ids, sc, ln)
+            assert np.all(ids == -1) and np.all(np.isneginf(sc)) and ln[0] == 0, user
+            assert torch.equal(cache.view(torch.int16), staging.canary_cache(wl).view(torch.int16))
+            assert api.is_get_status(store) == bits, user
+        inp = {"users": torch.tensor([int(wl.users[0])], dtype=torch.int32, device="cuda"),
+               "q_emb": torch.from_numpy(q).cuda(), "seg_start": torch.from_numpy(start).cuda(),
+               "block_table": torch.from_numpy(bt).cuda()}
+        want_cache = staging.canary_cache(wl)
+        want = gh.run_fused(api, store, wl, inp, want_cache)
+        assert want["status"] == 0
+        cache = staging.canary_cache(wl)
+        ids = np.empty((1, k), dtype=np.int64)
+        sc = np.empty((1, k), dtype=np.float32)
+        ln = np.empty(1, dtype=np.int32)
+        api.is_retrieve_and_inject_host(store, np.array([wl.users[0]], dtype=np.int32), q, k, start, rope, bt,
+                                        cd, cache, ids, sc, ln)
+        assert np.array_equal(ids, want["ids"]) and np.array_equal(ln, want["seg_len"])
+        assert np.array_equal(sc.view(np.uint32), want["scores"].view(np.uint32))
+        assert torch.equal(cache.view(torch.int16), want_cache.view(torch.int16))
+    finally:
+        store.destroy()
+
+
 @pytest.mark.parametrize("n", [4096, 4097, 6000])
 def test_per_query_topk_on_large_users(api, n):
     """The per-query retrieval kernel on users of 4096 facts (keys staged in
