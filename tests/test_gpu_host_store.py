@@ -116,3 +116,45 @@ def test_host_store_rejects_bad_placement(api):
     with pytest.raises(api.ISError) as e:
         staging.load_store(wl, api, kv_placement=2)
     assert e.value.status == 1
+
+
+@pytest.mark.parametrize("cache_dtype,scales", [(None, (1.0, 1.0)), ("e4m3", (0.37, 1.9))], ids=["bf16", "e4m3"])
+def test_host_buffer_call_on_host_store(api, cache_dtype, scales):
+    """is_retrieve_and_inject_host on a store in host DRAM (the host-memory
+    inject kernel, which also writes the call's completion word): the ids,
+    scores, segment lengths and every cache byte equal the device call on a
+    device-resident store, call after call."""
+    import torch
+    wl = workloads.generate(SHAPES[0])
+    s = wl.spec
+    host = staging.load_store(wl, api, kv_placement="host")
+    dev = staging.load_store(wl, api)
+    try:
+        inp = staging.device_inputs(wl)
+        ref = staging.canary_cache(wl, cache_dtype=cache_dtype)
+        out = gh.run_fused(api, dev, wl, inp, ref, cache_dtype=cache_dtype, k_scale=scales[0], v_scale=scales[1])
+        assert out["status"] == 0
+        rope = staging.rope_params(wl, api)
+        cd = api.make_cache_desc(s.block_size, wl.num_blocks, cache_dtype or s.kv_dtype, scales[0], scales[1])
+        Q, k = s.n_queries, s.k
+        users = np.array(wl.users, dtype=np.int32)
+        q = np.array(wl.queries, dtype=np.float16)
+        start = np.array(wl.seg_start, dtype=np.int32)
+        bt = np.array(wl.block_table, dtype=np.int32)
+        for _ in range(2):
+            cache = staging.canary_cache(wl, cache_dtype=cache_dtype)
+            ids = np.full((Q, k), -5, dtype=np.int64)
+            sc = np.zeros((Q, k), dtype=np.float32)
+            ln = np.full(Q, -5, dtype=np.int32)
+            api.is_retrieve_and_inject_host(host, users, q, k, start, rope, bt, cd, cache, ids, sc, ln)
+            assert np.array_equal(ids, out["ids"])
+            assert np.array_equal(sc.view(np.uint32), out["scores"].view(np.uint32))
+            assert np.array_equal(ln, out["seg_len"])
+            if cache_dtype:
+                assert torch.equal(cache, ref)
+            else:
+                assert torch.equal(_raw(cache), _raw(ref))
+        assert api.is_get_status(host) == 0
+    finally:
+        host.destroy()
+        dev.destroy()
